@@ -1,0 +1,560 @@
+#!/usr/bin/env python
+"""Benchmark of the external-KV biased GQA attention hot path on GB300.
+
+One step = the whole hot path over one batch of the decode workload
+(B=8, Hq=16, Hkv=8, D=256, S_q=1, max_seq=4096, nonpad ~ U[512,4096], causal +
+sliding window 1024, bf16): TensorScatter of the new K/V rows, the
+(B,1,S_q,max_seq) bias build, and attention over the static cache.
+
+Prints ONE JSON line (rank 0).  `value` is whole-job algorithmic GB/s with the
+inputs resident in HBM; `e2e` is the same metric through the public API with
+pinned host inputs copied in and the output copied out every step.  The
+`roofline` object covers the attention kernel (the dominant one); `secondary`
+adds the other workloads' attention kernels (prefill in TFLOP/s).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs its own replica (weak scaling: independent
+batches, no collective on the data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from biased_gqa_attention_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "ext-KV biased GQA attn: decode HBM GB/s, prefill TFLOP/s (% of GB300 peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (host logic; covered by a gloo test on CPU)
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, local, world
+
+
+def dist_init(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def reduce_max(x: float, world: int, device="cpu") -> float:
+    if world == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(units_per_rank: float, world: int, seconds_max: float) -> float:
+    """Units all ranks processed divided by the slowest rank's time."""
+    return units_per_rank * world / seconds_max
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work (what the method must move or compute; no skipped work is
+# counted and no redundant work is credited)
+
+def allowed_counts(w: wl.Workload, nonpad: np.ndarray, spans) -> np.ndarray:
+    """|U| per (b, i): allowed keys of each query row, from the workload's
+    causal / window / span structure (the definition of the bias)."""
+    out = np.zeros((w.B, w.S_q), np.int64)
+    for b in range(w.B):
+        npb = int(nonpad[b])
+        qs = max(npb - w.S_q, 0)
+        p = qs + np.arange(w.S_q, dtype=np.int64)
+        band_lo = p - w.window + 1 if w.window > 0 else np.full_like(p, -(1 << 40))
+        band_hi = p + 1 if w.causal else np.full_like(p, 1 << 40)
+        lo = np.clip(band_lo, 0, npb)
+        hi = np.clip(band_hi, 0, npb)
+        cnt = np.maximum(hi - lo, 0)
+        for (s, L) in spans[b]:
+            inside = (p >= s) & (p < s + L)
+            s_lo, s_hi = np.clip(s, 0, npb), np.clip(s + L, 0, npb)
+            extra = np.maximum(s_hi - np.maximum(s_lo, hi), 0) + np.maximum(np.minimum(s_hi, lo) - s_lo, 0)
+            cnt = np.where(inside, cnt + extra, cnt)
+        out[b] = cnt
+    return out
+
+
+def attention_work(w: wl.Workload, nonpad: np.ndarray, spans, mode: str):
+    """(bytes, flops) of one attention call.
+
+    Decode: K and V rows of every allowed slot once per KV head (the group's
+    query heads share them), Q in, Y out, and, with a materialised bias, the
+    bias row over the valid slots.  Prefill flops: 4*D per (query head, allowed
+    key) pair (QK^T and PV)."""
+    es = 4 if w.dtype == torch.float32 else 2
+    U = allowed_counts(w, nonpad, spans)
+    if w.S_q == 1:
+        kv = int(U[:, 0].sum()) * w.Hkv * w.D * es * 2
+    else:
+        kv = 0
+        for b in range(w.B):  # union of the rows' key sets, read once
+            kv += min(int(nonpad[b]), int(U[b].max()) + w.S_q) * w.Hkv * w.D * es * 2
+    qy = 2 * w.B * w.Hq * w.S_q * w.D * es
+    bias = int(nonpad.sum()) * w.S_q * es if mode == "bias" else 0
+    extra = int(U.sum()) * es if (w.extra and mode == "fused") else 0
+    flops = 4.0 * w.D * w.Hq * float(U.sum())
+    return kv + qy + bias + extra, flops
+
+
+def step_bytes(w: wl.Workload, nonpad: np.ndarray, spans, mode: str) -> int:
+    es = 4 if w.dtype == torch.float32 else 2
+    scatter = 2 * 2 * w.B * w.Hkv * w.S_q * w.D * es  # K and V, read + write
+    bias = w.B * w.S_q * w.max_seq * es if mode == "bias" else 0
+    if mode == "bias" and w.extra:
+        bias *= 2
+    attn, _ = attention_work(w, nonpad, spans, mode)
+    return scatter + bias + attn
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.bus = None
+        try:
+            props = torch.cuda.get_device_properties(device)
+            dom = getattr(props, "pci_domain_id", 0)
+            self.bus = f"{dom:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+        except Exception:
+            pass
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            if self.bus and parts[0].upper() not in (self.bus.upper(), self.bus.upper()[4:]):
+                if not parts[0].upper().endswith(self.bus.upper()[-12:]):
+                    continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+def _rotation(touched_bytes: int, device) -> int:
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    # enough distinct input sets that the bytes touched between two uses of
+    # one set exceed twice the L2 size
+    return max(2, math.ceil(2 * l2 / max(touched_bytes, 1)) + 1)
+
+
+class Decoder:
+    """Device-resident state for one workload: R rotating input sets."""
+
+    def __init__(self, w: wl.Workload, device, mode: str, sets: int):
+        from biased_gqa_attention_gb300 import extkv as ek
+        self.ek, self.w, self.mode, self.device = ek, w, mode, device
+        base = wl.make_inputs(w, device)
+        self.base = base
+        self.sets = []
+        for r in range(sets):
+            s = dict(q=base.q.clone(), k_new=base.k_new.clone(), v_new=base.v_new.clone(),
+                     k=base.k_cache.clone(), v=base.v_cache.clone(), write_idx=base.write_idx.clone(),
+                     nonpad=base.nonpad.clone(), y=torch.empty_like(base.q),
+                     bias=torch.empty((w.B, 1, w.S_q, w.max_seq), dtype=w.dtype, device=device),
+                     extra=None if base.extra is None else base.extra.clone())
+            s["spec"] = ek.BiasSpec(causal=w.causal, window=w.window, span_offsets=base.span_offsets,
+                                    spans=base.span_table, extra=s["extra"])
+            self.sets.append(s)
+        self.status = ek.new_status(device)
+
+    def scatter(self, r):
+        s = self.sets[r]
+        self.ek.ext_kv_scatter(s["k"], s["v"], s["k_new"], s["v_new"], s["write_idx"], status=self.status)
+
+    def bias(self, r):
+        s = self.sets[r]
+        self.ek.build_static_cache_bias(s["bias"], s["spec"], s["nonpad"], status=self.status)
+
+    def attention(self, r):
+        s = self.sets[r]
+        self.ek.attention_ext_kv(s["y"], s["q"], s["k"], s["v"], s["nonpad"], self.w.scale,
+                                 bias=s["bias"] if self.mode == "bias" else None,
+                                 fused=s["spec"] if self.mode == "fused" else None, status=self.status)
+
+    def step(self, r, ev=None):
+        self.scatter(r)
+        if self.mode == "bias":
+            self.bias(r)
+        if ev:
+            ev[0].record()
+        self.attention(r)
+        if ev:
+            ev[1].record()
+
+    def kernels_per_step(self):
+        return 1 + (1 if self.mode == "bias" else 0) + 1
+
+
+def _events(n, external):
+    return [(torch.cuda.Event(enable_timing=True, external=external),
+             torch.cuda.Event(enable_timing=True, external=external)) for _ in range(n)]
+
+
+def time_graph(dec: Decoder, K: int, W: int, stream):
+    """Warm-up W eager steps, capture K steps (with event records around each
+    attention call), replay once untimed (graph upload), then time one replay."""
+    R = len(dec.sets)
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            dec.step(i % R)
+    torch.cuda.synchronize()
+    try:
+        evs = _events(K, external=True)
+        use_ev = True
+    except TypeError:
+        evs, use_ev = None, False
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for k in range(K):
+            dec.step(k % R, ev=evs[k] if use_ev else None)
+    g.replay()
+    torch.cuda.synchronize()
+    return g, evs
+
+
+def run_ours(args, rank, local, world):
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    dist_init(world, "nccl")
+    from biased_gqa_attention_gb300 import build as bld
+    bld.build()
+    from biased_gqa_attention_gb300 import extkv as ek
+
+    w = wl.BY_NAME[args.workload]
+    nonpad, _, spans = wl.structure(w)
+    nonpad = nonpad.numpy()
+    sb = step_bytes(w, nonpad, spans, args.mode)
+    attn_b, attn_f = attention_work(w, nonpad, spans, args.mode)
+    R = _rotation(sb, device)
+    dec = Decoder(w, device, args.mode, R)
+    stream = torch.cuda.Stream(device)
+    K, W = args.steps, args.warmup
+
+    g, evs = time_graph(dec, K, W, stream)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        # keep the GPU busy on the same graph for ~1 s so clock samples land under load
+        tl = time.time()
+        while time.time() - tl < args.clock_load_s:
+            g.replay()
+            torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            t0.record()
+            g.replay()
+            t1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+    ms_total = t0.elapsed_time(t1)
+    attn_ms = [a.elapsed_time(b) for a, b in evs] if evs else None
+    ms_max = reduce_max(ms_total, world, device)
+    ms_per_step = ms_max / K
+    value = whole_job_value(sb * K, world, ms_max / 1e3) / 1e9
+
+    # status after the timed region: no device-side error may hide in the numbers
+    assert ek.extkv_read_status(dec.status) == ek.EXTKV_OK, ek.extkv_last_error()
+    kernel = ek.extkv_last_kernel()
+
+    # e2e: the public API with pinned host buffers, copies inside the timed region
+    e2e = run_e2e(dec, K, W, world, device)
+
+    peaks, peak_src = read_peaks()
+    attn_avg_ms = statistics.mean(attn_ms) if attn_ms else None
+    roof = None
+    if attn_avg_ms:
+        achieved = attn_b / (attn_avg_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": args.traffic,
+                "kernel": kernel, "launch_us": round(attn_avg_ms * 1e3, 3),
+                "algorithmic_bytes": attn_b, "peak_source": peak_src}
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded N(0,1) values, nonpad ~ U[512,4096]; no dataset)",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "S_q": w.S_q,
+                   "max_seq": w.max_seq, "window": w.window, "bias_mode": args.mode,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": f"{R} rotating input sets, >2x L2 touched between reuses",
+                   "timing": "CUDA graph of K steps, CUDA events on the launching stream",
+                   "step": "ext_kv_scatter + build_static_cache_bias + attention_ext_kv",
+                   "step_algorithmic_bytes": sb},
+        "gpu_launches": K * dec.kernels_per_step(),
+        "roofline": roof,
+        "clocks": clk.summary(),
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, dec.base, args.mode, sb, args.cpu_seconds)
+    if not args.no_secondary:
+        out["secondary"] = secondary(args, device, peaks, peak_src)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(dec: Decoder, K: int, W: int, world: int, device):
+    w = dec.w
+    s = dec.sets[0]
+    host = {k: torch.empty(s[k].shape, dtype=s[k].dtype, pin_memory=True)
+            for k in ("q", "k_new", "v_new", "write_idx", "nonpad")}
+    for k, t in host.items():
+        t.copy_(s[k].cpu())
+    y_host = torch.empty(s["y"].shape, dtype=s["y"].dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = y_host.numel() * y_host.element_size()
+    R = len(dec.sets)
+
+    def one(r):
+        d = dec.sets[r]
+        for k, t in host.items():
+            d[k].copy_(t, non_blocking=True)
+        dec.step(r)
+        y_host.copy_(d["y"], non_blocking=True)
+
+    for i in range(W):
+        one(i % R)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for k in range(K):
+        one(k % R)
+    torch.cuda.synchronize()
+    sec = time.perf_counter() - t0
+    sec = reduce_max(sec, world, device)
+    nonpad, _, spans = wl.structure(w)
+    sb = step_bytes(w, nonpad.numpy(), spans, dec.mode)
+    return {"value": round(whole_job_value(sb * K, world, sec) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(sec * 1e3 / K, 4),
+            "timing": "host wall clock around K eager steps through the Python binding"}
+
+
+def secondary(args, device, peaks, peak_src):
+    """The other workloads' attention kernels, each timed alone with CUDA
+    events over rotating input sets."""
+    from biased_gqa_attention_gb300 import extkv as ek
+    res = {}
+    for w in (wl.C3, wl.C4, wl.C5):
+        nonpad, _, spans = wl.structure(w)
+        nonpad = nonpad.numpy()
+        ab, af = attention_work(w, nonpad, spans, args.mode)
+        touched = ab if w.S_q == 1 else ab + w.B * w.S_q * w.max_seq * 2
+        R = min(_rotation(touched, device), 6)
+        dec = Decoder(w, device, args.mode, R)
+        for r in range(R):
+            dec.scatter(r)
+            if args.mode == "bias":
+                dec.bias(r)
+        for i in range(3):
+            dec.attention(i % R)
+        torch.cuda.synchronize()
+        n = 20
+        evs = _events(n, external=False)
+        for i in range(n):
+            evs[i][0].record()
+            dec.attention(i % R)
+            evs[i][1].record()
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        assert ek.extkv_read_status(dec.status) == ek.EXTKV_OK, ek.extkv_last_error()
+        if w.S_q == 1:
+            ach = ab / (ms / 1e3) / 1e9
+            res[w.name] = {"bound": "hbm", "achieved": round(ach, 1), "unit": "GB/s",
+                           "peak": peaks["hbm_gbs"], "frac": round(ach / peaks["hbm_gbs"], 4),
+                           "launch_us": round(ms * 1e3, 2), "kernel": ek.extkv_last_kernel()}
+        else:
+            ach = af / (ms / 1e3) / 1e12
+            res[w.name] = {"bound": "tensor", "achieved": round(ach, 2), "unit": "TFLOP/s",
+                           "peak": peaks["bf16_tflops"], "frac": round(ach / peaks["bf16_tflops"], 4),
+                           "launch_us": round(ms * 1e3, 2), "kernel": ek.extkv_last_kernel(),
+                           "algorithmic_flops": af}
+        res[w.name]["peak_source"] = peak_src
+        del dec
+        torch.cuda.empty_cache()
+    return res
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline and the reference arm)
+
+def _oracle_inputs(w: wl.Workload, base):
+    """Host copies of one input set in the oracle's raw element types."""
+    def raw(t):
+        t = t.detach().contiguous().cpu()
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy().view(np.uint16).copy()
+        return t.numpy().copy()
+    return {k: (None if getattr(base, k) is None else raw(getattr(base, k)))
+            for k in ("q", "k_new", "v_new", "k_cache", "v_cache", "write_idx", "nonpad", "extra")}
+
+
+def oracle_step(w: wl.Workload, h, spans, mode: str):
+    import oracle
+    dt = "f32" if w.dtype == torch.float32 else "bf16"
+    oracle.scatter(h["k_cache"], h["v_cache"], h["k_new"], h["v_new"], h["write_idx"])
+    b = None
+    if mode in ("bias", "fused"):
+        b, _ = oracle.bias(h["nonpad"], w.S_q, w.max_seq, dt, causal=w.causal, window=w.window,
+                           spans=spans if any(spans) else None, extra=h["extra"])
+    return oracle.attention(h["q"], h["k_cache"], h["v_cache"], b, h["nonpad"], np.float32(w.scale))
+
+
+def cpu_baseline(w, base, mode, sb, seconds):
+    import oracle
+    _, _, spans = wl.structure(w)
+    h = _oracle_inputs(w, base)
+    oracle_step(w, h, spans, mode)  # warm-up (also builds the oracle library)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(w, h, spans, mode)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or n >= 200:
+            break
+    return {"value": round(sb * n / el / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": f"{n} full steps of {w.name} (scatter + bias + attention over "
+            f"all rows), {el:.1f} s, fp64, OpenMP over query rows"}
+
+
+def run_reference(args, rank, local, world):
+    """The oracle as it stands, on the host cores, for the same workload and metric."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = wl.BY_NAME[args.workload]
+    base = wl.make_inputs(w, "cpu")
+    nonpad, _, spans = wl.structure(w)
+    sb = step_bytes(w, nonpad.numpy(), spans, args.mode)
+    h = _oracle_inputs(w, base)
+    for _ in range(args.warmup):
+        oracle_step(w, h, spans, args.mode)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, h, spans, args.mode)
+    el = time.perf_counter() - t0
+    value = sb * args.steps / el / 1e9
+    out = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded N(0,1) values; no dataset)", "impl": "reference",
+           "config": {"workload": w.name, "bias_mode": args.mode, "step_algorithmic_bytes": sb},
+           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                            "kind": "oracle", "sample": f"{args.steps} full steps of {w.name}"},
+           "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0},
+           "gpu_launches": 0}
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=wl.C2.name, choices=sorted(wl.BY_NAME))
+    ap.add_argument("--mode", choices=["bias", "fused"], default="bias")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--clock-load-s", type=float, default=1.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per attention launch for the current kernel, if captured")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    rank, local, world = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, local, world)
+    else:
+        run_ours(args, rank, local, world)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,239 @@
+// extkv_api.cu -- the C ABI: argument validation, kernel choice, error
+// reporting.  Every check here happens on the host before any launch; the
+// kernels themselves only see data-dependent errors (status word).
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/extkv.h"
+#include "internal.h"
+
+namespace extkv {
+
+namespace {
+
+thread_local char g_error[512] = "";
+thread_local const char* g_last_kernel = "";
+thread_local int g_algo = EXTKV_ALGO_AUTO;
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_error, sizeof g_error, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(EXTKV_ERR_CUDA, "%s: CUDA error %d (%s)", what, static_cast<int>(e),
+              cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t elem_size(int dtype) { return dtype == EXTKV_F32 ? 4 : 2; }
+
+bool valid_dtype(int dtype) { return dtype == EXTKV_F32 || dtype == EXTKV_BF16; }
+
+}  // namespace
+
+int num_sms() {
+  // Cached per device; the SM count never changes for a device.
+  static thread_local int cached_dev = -1, cached = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (dev != cached_dev) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 152;
+    cached = n;
+    cached_dev = dev;
+  }
+  return cached;
+}
+
+}  // namespace extkv
+
+using namespace extkv;
+
+extern "C" {
+
+int ext_kv_scatter(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                   const int64_t* write_idx, int64_t B, int64_t Hkv, int64_t S_new,
+                   int64_t max_seq, int64_t D, int dtype, int32_t* status, void* stream) {
+  g_error[0] = 0;
+  if (!valid_dtype(dtype)) return fail(EXTKV_ERR_INVALID_ARG, "ext_kv_scatter: unknown dtype %d", dtype);
+  if (B < 0 || Hkv <= 0 || S_new < 0 || max_seq <= 0 || D <= 0)
+    return fail(EXTKV_ERR_INVALID_ARG,
+                "ext_kv_scatter: bad sizes B=%lld Hkv=%lld S_new=%lld max_seq=%lld D=%lld",
+                (long long)B, (long long)Hkv, (long long)S_new, (long long)max_seq, (long long)D);
+  if (S_new > max_seq)
+    return fail(EXTKV_ERR_INVALID_ARG, "ext_kv_scatter: S_new=%lld exceeds max_seq=%lld",
+                (long long)S_new, (long long)max_seq);
+  if (B == 0 || S_new == 0) return EXTKV_OK;  // an empty update writes nothing
+  if (!k_cache || !v_cache || !k_new || !v_new || !write_idx)
+    return fail(EXTKV_ERR_INVALID_ARG, "ext_kv_scatter: null pointer");
+  if ((D * elem_size(dtype)) % 16)
+    return fail(EXTKV_ERR_UNSUPPORTED, "ext_kv_scatter: D*sizeof(T) must be a multiple of 16 (D=%lld)",
+                (long long)D);
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) ||
+      !aligned(write_idx, 8) || !aligned(status, 4))
+    return fail(EXTKV_ERR_INVALID_ARG, "ext_kv_scatter: tensors must be 16-byte aligned");
+  cudaError_t e = launch_scatter(k_cache, v_cache, k_new, v_new, write_idx, B, Hkv, S_new, max_seq,
+                                 D, dtype, status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "ext_kv_scatter launch");
+  return EXTKV_OK;
+}
+
+int build_static_cache_bias(void* bias, const extkv_bias_spec* spec, const int64_t* nonpad,
+                            int64_t B, int64_t S_q, int64_t max_seq, int dtype, int32_t* status,
+                            void* stream) {
+  g_error[0] = 0;
+  if (!valid_dtype(dtype)) return fail(EXTKV_ERR_INVALID_ARG, "build_static_cache_bias: unknown dtype %d", dtype);
+  if (B < 0 || S_q < 0 || max_seq <= 0)
+    return fail(EXTKV_ERR_INVALID_ARG, "build_static_cache_bias: bad sizes B=%lld S_q=%lld max_seq=%lld",
+                (long long)B, (long long)S_q, (long long)max_seq);
+  if (B == 0 || S_q == 0) return EXTKV_OK;
+  if (!bias || !spec || !nonpad) return fail(EXTKV_ERR_INVALID_ARG, "build_static_cache_bias: null pointer");
+  if ((spec->span_offsets == nullptr) != (spec->spans == nullptr))
+    return fail(EXTKV_ERR_INVALID_ARG, "build_static_cache_bias: span_offsets and spans must be given together");
+  if ((max_seq * elem_size(dtype)) % 16)
+    return fail(EXTKV_ERR_UNSUPPORTED,
+                "build_static_cache_bias: max_seq*sizeof(T) must be a multiple of 16 (max_seq=%lld)",
+                (long long)max_seq);
+  if (!aligned(bias, 16) || (spec->extra && !aligned(spec->extra, 16)) || !aligned(status, 4))
+    return fail(EXTKV_ERR_INVALID_ARG, "build_static_cache_bias: bias/extra must be 16-byte aligned");
+  cudaError_t e = launch_bias(bias, *spec, nonpad, B, S_q, max_seq, dtype, status,
+                              static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "build_static_cache_bias launch");
+  return EXTKV_OK;
+}
+
+size_t attention_ext_kv_workspace_size(int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int) {
+  return 0;
+}
+
+int attention_ext_kv(void* y, const void* q, const void* k_cache, const void* v_cache,
+                     const void* bias, const extkv_bias_spec* fused, const int64_t* nonpad,
+                     float scale, int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq,
+                     int64_t D, int dtype, void* workspace, size_t ws_bytes, int32_t* status,
+                     void* stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  g_error[0] = 0;
+  if (!valid_dtype(dtype)) return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv: unknown dtype %d", dtype);
+  if (B < 0 || S_q < 0 || Hq <= 0 || Hkv <= 0 || max_seq <= 0 || D <= 0)
+    return fail(EXTKV_ERR_INVALID_ARG,
+                "attention_ext_kv: bad sizes B=%lld Hq=%lld Hkv=%lld S_q=%lld max_seq=%lld D=%lld",
+                (long long)B, (long long)Hq, (long long)Hkv, (long long)S_q, (long long)max_seq,
+                (long long)D);
+  if (Hq % Hkv)
+    return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv: Hq=%lld is not a multiple of Hkv=%lld",
+                (long long)Hq, (long long)Hkv);
+  if (D % 8 || D > 512)
+    return fail(EXTKV_ERR_UNSUPPORTED, "attention_ext_kv: D=%lld unsupported (need D %% 8 == 0, D <= 512)",
+                (long long)D);
+  if (bias && fused)
+    return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv: pass either a materialised bias or a fused spec, not both");
+  if (B == 0 || S_q == 0) return EXTKV_OK;
+  if (!y || !q || !k_cache || !v_cache || !nonpad)
+    return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv: null pointer");
+  if (fused && ((fused->span_offsets == nullptr) != (fused->spans == nullptr)))
+    return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv: span_offsets and spans must be given together");
+  const size_t al = 16;
+  if (!aligned(y, al) || !aligned(q, al) || !aligned(k_cache, al) || !aligned(v_cache, al) ||
+      (bias && !aligned(bias, al)) || (fused && fused->extra && !aligned(fused->extra, al)) ||
+      !aligned(nonpad, 8) || !aligned(status, 4))
+    return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv: tensors must be 16-byte aligned");
+
+  AttnArgs a{};
+  a.y = y;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.bias = bias;
+  a.fused = fused != nullptr;
+  if (fused) {
+    a.extra = fused->extra;
+    a.span_offsets = fused->span_offsets;
+    a.spans = fused->spans;
+    a.q_start = fused->q_start;
+    a.causal = fused->causal;
+    a.window = fused->window;
+  }
+  a.nonpad = nonpad;
+  a.scale = scale;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.S_q = S_q;
+  a.max_seq = max_seq;
+  a.D = D;
+  a.dtype = dtype;
+  a.status = status;
+  a.stream = static_cast<cudaStream_t>(stream);
+
+  const char* name = "";
+  cudaError_t e;
+  switch (g_algo) {
+    case EXTKV_ALGO_GENERIC:
+      e = launch_attn_generic(a, &name);
+      break;
+    case EXTKV_ALGO_DECODE:
+      if (!decode_supported(a))
+        return fail(EXTKV_ERR_UNSUPPORTED, "attention_ext_kv: the decode kernel cannot run this shape/type");
+      e = launch_attn_decode(a, &name);
+      break;
+    case EXTKV_ALGO_PREFILL:
+      if (!prefill_supported(a))
+        return fail(EXTKV_ERR_UNSUPPORTED, "attention_ext_kv: the prefill kernel cannot run this shape/type");
+      e = launch_attn_prefill(a, &name);
+      break;
+    default:
+      if (decode_supported(a)) e = launch_attn_decode(a, &name);
+      else if (prefill_supported(a)) e = launch_attn_prefill(a, &name);
+      else e = launch_attn_generic(a, &name);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "attention_ext_kv launch");
+  g_last_kernel = name;
+  return EXTKV_OK;
+}
+
+int extkv_clear_status(int32_t* status, void* stream) {
+  g_error[0] = 0;
+  if (!status || !aligned(status, 4)) return fail(EXTKV_ERR_INVALID_ARG, "extkv_clear_status: bad pointer");
+  cudaError_t e = cudaMemsetAsync(status, 0, 16, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "extkv_clear_status");
+  return EXTKV_OK;
+}
+
+int extkv_read_status(const int32_t* status, void* stream) {
+  g_error[0] = 0;
+  if (!status || !aligned(status, 4)) return fail(EXTKV_ERR_INVALID_ARG, "extkv_read_status: bad pointer");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "extkv_read_status: stream sync");
+  int32_t h[4] = {0, 0, 0, 0};
+  e = cudaMemcpy(h, status, sizeof h, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "extkv_read_status: copy");
+  if (h[0] == 0) return EXTKV_OK;
+  return fail(EXTKV_ERR_DEVICE, "device status 0x%x (%d unit(s) skipped):%s%s%s", h[0], h[1],
+              (h[0] & EXTKV_DEV_BAD_WRITE_IDX) ? " write_idx out of range;" : "",
+              (h[0] & EXTKV_DEV_BAD_NONPAD) ? " nonpad out of range;" : "",
+              (h[0] & EXTKV_DEV_TIMEOUT) ? " pipeline wait timed out;" : "");
+}
+
+const char* extkv_last_error(void) { return g_error; }
+
+const char* extkv_last_kernel(void) { return g_last_kernel; }
+
+int extkv_set_algo(int algo) {
+  if (algo < EXTKV_ALGO_AUTO || algo > EXTKV_ALGO_PREFILL)
+    return fail(EXTKV_ERR_INVALID_ARG, "extkv_set_algo: unknown algorithm %d", algo);
+  int prev = g_algo;
+  g_algo = algo;
+  return prev;
+}
+
+}  // extern "C"

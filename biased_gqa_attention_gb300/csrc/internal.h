@@ -1,0 +1,52 @@
+// internal.h -- launchers shared between the extkv translation units (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/extkv.h"
+
+namespace extkv {
+
+struct BiasSpec;  // common.cuh
+
+struct AttnArgs {
+  void* y;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const void* bias;       // materialised bias or nullptr
+  const void* extra;      // fused spec's extra term or nullptr
+  const int64_t* span_offsets;
+  const int64_t* spans;
+  const int64_t* q_start;
+  int32_t causal, window;
+  int fused;              // evaluate the spec in registers
+  const int64_t* nonpad;
+  float scale;
+  int64_t B, Hq, Hkv, S_q, max_seq, D;
+  int dtype;
+  int32_t* status;
+  cudaStream_t stream;
+};
+
+// Each launcher returns cudaSuccess or the launch error; `name` receives the
+// kernel's name for extkv_last_kernel().
+cudaError_t launch_scatter(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                           const int64_t* write_idx, int64_t B, int64_t Hkv, int64_t S_new,
+                           int64_t max_seq, int64_t D, int dtype, int32_t* status,
+                           cudaStream_t stream);
+cudaError_t launch_bias(void* bias, const extkv_bias_spec& spec, const int64_t* nonpad, int64_t B,
+                        int64_t S_q, int64_t max_seq, int dtype, int32_t* status,
+                        cudaStream_t stream);
+cudaError_t launch_attn_generic(const AttnArgs& a, const char** name);
+
+// Fast paths: `supported` says whether the shape can run; launch returns the error.
+bool decode_supported(const AttnArgs& a);
+cudaError_t launch_attn_decode(const AttnArgs& a, const char** name);
+bool prefill_supported(const AttnArgs& a);
+cudaError_t launch_attn_prefill(const AttnArgs& a, const char** name);
+
+int num_sms();
+
+}  // namespace extkv

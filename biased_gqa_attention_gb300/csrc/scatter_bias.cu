@@ -1,0 +1,132 @@
+// scatter_bias.cu -- the TensorScatter write into the static cache and the
+// static-cache bias builder.  Both are pure HBM streams: 16-byte vector loads
+// and stores, grid-stride loops over a grid sized to the SM count.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace extkv {
+
+// ---- TensorScatter ----------------------------------------------------------
+// "Skill: Attention Optimization", "In-place KV for ONNX Attention via
+// TensorScatter (static cache)": new rows go to slot write_idx[b] + s of the
+// preallocated (B,Hkv,max_seq,D) buffer; nothing is concatenated.
+//
+// One 16-byte vector per loop trip, for K and for V.  Row r of the update
+// (b,h,s) is contiguous, as is its destination row, so consecutive threads
+// touch consecutive vectors on both sides.
+__global__ void __launch_bounds__(256) scatter_kernel(uint4* __restrict__ k_cache,
+                                                      uint4* __restrict__ v_cache,
+                                                      const uint4* __restrict__ k_new,
+                                                      const uint4* __restrict__ v_new,
+                                                      const int64_t* __restrict__ write_idx,
+                                                      int64_t Hkv, int64_t S_new, int64_t max_seq,
+                                                      int64_t row_vecs, int64_t total,
+                                                      int32_t* status) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += stride) {
+    const int64_t v = idx % row_vecs;
+    const int64_t r = idx / row_vecs;  // (b*Hkv + h)*S_new + s
+    const int64_t s = r % S_new;
+    const int64_t bh = r / S_new;
+    const int64_t b = bh / Hkv;
+    const int64_t w = write_idx[b];
+    if (w < 0 || w > max_seq - S_new) {
+      if (v == 0 && s == 0 && bh % Hkv == 0) report(status, EXTKV_DEV_BAD_WRITE_IDX);
+      continue;
+    }
+    const int64_t dst = (bh * max_seq + w + s) * row_vecs + v;
+    const uint4 kx = __ldg(k_new + idx);
+    const uint4 vx = __ldg(v_new + idx);
+    k_cache[dst] = kx;
+    v_cache[dst] = vx;
+  }
+}
+
+cudaError_t launch_scatter(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                           const int64_t* write_idx, int64_t B, int64_t Hkv, int64_t S_new,
+                           int64_t max_seq, int64_t D, int dtype, int32_t* status,
+                           cudaStream_t stream) {
+  const int64_t es = dtype == EXTKV_F32 ? 4 : 2;
+  const int64_t row_vecs = D * es / 16;
+  const int64_t total = B * Hkv * S_new * row_vecs;
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t want = (total + threads - 1) / threads;
+  const int blocks = static_cast<int>(std::min<int64_t>(want, int64_t(num_sms()) * 8));
+  scatter_kernel<<<blocks, threads, 0, stream>>>(
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), write_idx, Hkv, S_new,
+      max_seq, row_vecs, total, status);
+  return cudaGetLastError();
+}
+
+// ---- static-cache bias ------------------------------------------------------
+// mobius issue #366, deliverable: the (B,1,S_q,max_seq) additive bias keyed on
+// absolute query positions (causal + sliding + block overlay + padding, valid
+// only where slot < nonpad).  Each thread writes one 16-byte vector of one
+// row; the row's two allowed intervals are recomputed per vector from the
+// position (cheap integer work next to the 16-byte store).
+template <typename T>
+__global__ void __launch_bounds__(256) bias_kernel(uint4* __restrict__ bias, BiasSpec spec,
+                                                   const int64_t* __restrict__ nonpad, int64_t S_q,
+                                                   int64_t max_seq, int64_t row_vecs,
+                                                   int64_t total, int32_t* status) {
+  constexpr int kVec = 16 / sizeof(T);
+  using E = Elem<T>;
+  const uint4* extra = static_cast<const uint4*>(spec.extra);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += stride) {
+    const int64_t jv = idx % row_vecs;
+    const int64_t r = idx / row_vecs;  // b*S_q + i
+    const int64_t i = r % S_q;
+    const int64_t b = r / S_q;
+    const int64_t np = nonpad[b];
+    if (bad_nonpad(np, max_seq)) {
+      if (jv == 0 && i == 0) report(status, EXTKV_DEV_BAD_NONPAD);
+      continue;
+    }
+    const int64_t p = query_start(spec.q_start, b, np, S_q) + i;
+    const RowWindow w = row_window(spec, b, p, np);
+    union {
+      uint4 u;
+      T e[kVec];
+    } out, ex;
+    if (extra) ex.u = __ldg(extra + idx);
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) {
+      const int64_t j = jv * kVec + e;
+      if (w.allowed(j)) {
+        out.e[e] = extra ? ex.e[e] : E::from_float(0.0f);
+      } else {
+        out.e[e] = E::from_float(E::lowest());
+      }
+    }
+    bias[idx] = out.u;
+  }
+}
+
+cudaError_t launch_bias(void* bias, const extkv_bias_spec& s, const int64_t* nonpad, int64_t B,
+                        int64_t S_q, int64_t max_seq, int dtype, int32_t* status,
+                        cudaStream_t stream) {
+  const int64_t es = dtype == EXTKV_F32 ? 4 : 2;
+  const int64_t row_vecs = max_seq * es / 16;
+  const int64_t total = B * S_q * row_vecs;
+  if (total == 0) return cudaSuccess;
+  BiasSpec spec{s.causal, s.window, s.span_offsets, s.spans, s.extra, s.q_start};
+  const int threads = 256;
+  const int64_t want = (total + threads - 1) / threads;
+  const int blocks = static_cast<int>(std::min<int64_t>(want, int64_t(num_sms()) * 8));
+  if (dtype == EXTKV_F32)
+    bias_kernel<float><<<blocks, threads, 0, stream>>>(static_cast<uint4*>(bias), spec, nonpad,
+                                                       S_q, max_seq, row_vecs, total, status);
+  else
+    bias_kernel<__nv_bfloat16><<<blocks, threads, 0, stream>>>(
+        static_cast<uint4*>(bias), spec, nonpad, S_q, max_seq, row_vecs, total, status);
+  return cudaGetLastError();
+}
+
+}  // namespace extkv

@@ -1,0 +1,220 @@
+"""Thin ctypes binding over libextkv (include/extkv.h).
+
+Argument marshalling only: torch tensors supply device memory and the current
+CUDA stream; every step of the path runs in the library's kernels.  There is
+no fallback: if libextkv.so is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libextkv.so")
+
+EXTKV_F32, EXTKV_BF16 = 0, 1
+EXTKV_OK, EXTKV_ERR_INVALID_ARG, EXTKV_ERR_UNSUPPORTED, EXTKV_ERR_CUDA, EXTKV_ERR_DEVICE = 0, -1, -2, -3, -4
+EXTKV_DEV_BAD_WRITE_IDX, EXTKV_DEV_BAD_NONPAD, EXTKV_DEV_TIMEOUT = 0x1, 0x2, 0x4
+ALGO_AUTO, ALGO_GENERIC, ALGO_DECODE, ALGO_PREFILL = 0, 1, 2, 3
+
+# Every symbol include/extkv.h declares.
+SYMBOLS = ("ext_kv_scatter", "build_static_cache_bias", "attention_ext_kv_workspace_size",
+           "attention_ext_kv", "extkv_clear_status", "extkv_read_status", "extkv_last_error",
+           "extkv_last_kernel", "extkv_set_algo")
+
+
+class ExtKVError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"extkv error {code}: {message}")
+        self.code = code
+
+
+class _BiasSpec(ctypes.Structure):
+    _fields_ = [("causal", ctypes.c_int32), ("window", ctypes.c_int32),
+                ("span_offsets", ctypes.c_void_p), ("spans", ctypes.c_void_p),
+                ("extra", ctypes.c_void_p), ("q_start", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libextkv.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with biased_gqa_attention_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P, I64, I, I32P = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+    lib.ext_kv_scatter.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I, I32P, P]
+    lib.build_static_cache_bias.argtypes = [P, ctypes.POINTER(_BiasSpec), P, I64, I64, I64, I, I32P, P]
+    lib.attention_ext_kv_workspace_size.argtypes = [I64, I64, I64, I64, I64, I64, I]
+    lib.attention_ext_kv_workspace_size.restype = ctypes.c_size_t
+    lib.attention_ext_kv.argtypes = [P, P, P, P, P, ctypes.POINTER(_BiasSpec), P, ctypes.c_float,
+                                     I64, I64, I64, I64, I64, I64, I, P, ctypes.c_size_t, I32P, P]
+    lib.extkv_clear_status.argtypes = [I32P, P]
+    lib.extkv_read_status.argtypes = [I32P, P]
+    lib.extkv_last_error.restype = ctypes.c_char_p
+    lib.extkv_last_kernel.restype = ctypes.c_char_p
+    lib.extkv_set_algo.argtypes = [I]
+    for name in ("ext_kv_scatter", "build_static_cache_bias", "attention_ext_kv",
+                 "extkv_clear_status", "extkv_read_status", "extkv_set_algo"):
+        getattr(lib, name).restype = I
+    _lib = lib
+    return lib
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return EXTKV_F32
+    if t.dtype == torch.bfloat16:
+        return EXTKV_BF16
+    raise TypeError(f"unsupported element type {t.dtype}")
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(code: int):
+    if code != EXTKV_OK:
+        raise ExtKVError(code, load().extkv_last_error().decode())
+
+
+def _need(t, name, dims=None, dtype=None):
+    if t is None:
+        return
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dims is not None and t.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dims, got {tuple(t.shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+@dataclass
+class BiasSpec:
+    """extkv_bias_spec: causal + sliding window + image spans + padding, with an
+    optional dense extra term; tensors live on the device."""
+    causal: bool = True
+    window: int = 0
+    span_offsets: Optional[torch.Tensor] = None  # (B+1,) int64
+    spans: Optional[torch.Tensor] = None         # (n,2) int64
+    extra: Optional[torch.Tensor] = None         # (B,1,S_q,max_seq)
+    q_start: Optional[torch.Tensor] = None       # (B,) int64
+
+    def _c(self) -> _BiasSpec:
+        for t, n in ((self.span_offsets, "span_offsets"), (self.spans, "spans"),
+                     (self.q_start, "q_start")):
+            _need(t, n, dtype=torch.int64)
+        _need(self.extra, "extra", dims=4)
+        return _BiasSpec(int(bool(self.causal)), int(self.window), _p(self.span_offsets),
+                         _p(self.spans), _p(self.extra), _p(self.q_start))
+
+
+def ext_kv_scatter(k_cache, v_cache, k_new, v_new, write_idx, status=None, stream=None):
+    """TensorScatter of (B,Hkv,S_new,D) rows into the (B,Hkv,max_seq,D) caches at write_idx."""
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (k_new, "k_new"), (v_new, "v_new")):
+        _need(t, n, dims=4, dtype=k_cache.dtype)
+    _need(write_idx, "write_idx", dims=1, dtype=torch.int64)
+    B, Hkv, max_seq, D = k_cache.shape
+    if v_cache.shape != k_cache.shape or k_new.shape != v_new.shape or k_new.shape[:2] != (B, Hkv) \
+            or k_new.shape[3] != D:
+        raise ValueError("inconsistent cache / update shapes")
+    _check(load().ext_kv_scatter(_p(k_cache), _p(v_cache), _p(k_new), _p(v_new), _p(write_idx), B,
+                                 Hkv, k_new.shape[2], max_seq, D, _dt(k_cache), _p(status),
+                                 _stream(stream)))
+
+
+def build_static_cache_bias(bias, spec: BiasSpec, nonpad, status=None, stream=None):
+    """Materialise the (B,1,S_q,max_seq) bias of ``spec`` into ``bias``."""
+    _need(bias, "bias", dims=4)
+    _need(nonpad, "nonpad", dims=1, dtype=torch.int64)
+    B, one, S_q, max_seq = bias.shape
+    if one != 1:
+        raise ValueError("bias must be (B,1,S_q,max_seq)")
+    c = spec._c()
+    _check(load().build_static_cache_bias(_p(bias), ctypes.byref(c), _p(nonpad), B, S_q, max_seq,
+                                          _dt(bias), _p(status), _stream(stream)))
+
+
+def attention_ext_kv_workspace_size(B, Hq, Hkv, S_q, max_seq, D, dtype) -> int:
+    return int(load().attention_ext_kv_workspace_size(B, Hq, Hkv, S_q, max_seq, D,
+                                                      EXTKV_F32 if dtype == torch.float32 else EXTKV_BF16))
+
+
+def attention_ext_kv(y, q, k_cache, v_cache, nonpad, scale, bias=None, fused: Optional[BiasSpec] = None,
+                     workspace=None, status=None, stream=None):
+    """Y = softmax(scale*QK^T + bias)V over the external cache; writes ``y`` (B,Hq,S_q,D)."""
+    for t, n in ((y, "y"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, dims=4, dtype=q.dtype)
+    _need(bias, "bias", dims=4, dtype=q.dtype)
+    _need(nonpad, "nonpad", dims=1, dtype=torch.int64)
+    B, Hq, S_q, D = q.shape
+    Hkv, max_seq = k_cache.shape[1], k_cache.shape[2]
+    if y.shape != q.shape or v_cache.shape != k_cache.shape or k_cache.shape[0] != B or \
+            k_cache.shape[3] != D:
+        raise ValueError("inconsistent q / y / cache shapes")
+    c = None if fused is None else fused._c()
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().attention_ext_kv(_p(y), _p(q), _p(k_cache), _p(v_cache), _p(bias),
+                                   None if c is None else ctypes.byref(c), _p(nonpad), float(scale),
+                                   B, Hq, Hkv, S_q, max_seq, D, _dt(q), _p(workspace), ws, _p(status),
+                                   _stream(stream)))
+
+
+def new_status(device="cuda") -> torch.Tensor:
+    """A zeroed 16-byte device status word."""
+    return torch.zeros(4, dtype=torch.int32, device=device)
+
+
+def extkv_clear_status(status, stream=None):
+    _check(load().extkv_clear_status(_p(status), _stream(stream)))
+
+
+def extkv_read_status(status, stream=None) -> int:
+    """Synchronises; returns EXTKV_OK or EXTKV_ERR_DEVICE (message in extkv_last_error)."""
+    code = load().extkv_read_status(_p(status), _stream(stream))
+    if code not in (EXTKV_OK, EXTKV_ERR_DEVICE):
+        _check(code)
+    return code
+
+
+def extkv_last_error() -> str:
+    return load().extkv_last_error().decode()
+
+
+def extkv_last_kernel() -> str:
+    return load().extkv_last_kernel().decode()
+
+
+def extkv_set_algo(algo: int) -> int:
+    prev = load().extkv_set_algo(int(algo))
+    if prev < 0:
+        _check(prev)
+    return prev
+
+
+class use_algo:
+    """Context manager forcing one attention kernel for the calling thread."""
+
+    def __init__(self, algo: int):
+        self.algo = algo
+
+    def __enter__(self):
+        self.prev = extkv_set_algo(self.algo)
+        return self
+
+    def __exit__(self, *exc):
+        extkv_set_algo(self.prev)

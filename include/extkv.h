@@ -1,0 +1,200 @@
+/*
+ * extkv.h -- C ABI of libextkv: biased grouped-query attention over an
+ * external static KV cache, native to GB300 (sm_103a).
+ *
+ * The three operations are the three nodes of the static-cache graph the
+ * pages describe ("Skill: Attention Optimization", section "In-place KV for
+ * ONNX Attention via TensorScatter (static cache)"; mobius issue #366,
+ * "Emit bias-aware external-KV (TensorScatter + nonpad_kv_seqlen) attention for
+ * float-bias decoders"):
+ *     cache' = TensorScatter(cache, new_rows, write_indices)      -> ext_kv_scatter
+ *     bias   = create_static_cache_attention_bias(...)            -> build_static_cache_bias
+ *     Y      = Attention(Q, K cache', V cache', bias, nonpad_kv_seqlen,
+ *                        q_num_heads, kv_num_heads, is_causal=0)  -> attention_ext_kv
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named *_cache, q, y, bias, extra, status, workspace, nonpad,
+ *     write_idx, q_start, spans, span_offsets are DEVICE pointers, owned by
+ *     the caller.  The library allocates no memory and keeps no pointer after
+ *     a call returns.  Structs passed by pointer (extkv_bias_spec) are HOST
+ *     memory, read during the call only.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL is the legacy default stream) and never synchronises, except
+ *     extkv_read_status.
+ *   - All tensors are dense, row-major, in BNSH order:
+ *       q, y           (B, Hq,  S_q,     D)
+ *       k/v cache      (B, Hkv, max_seq, D)
+ *       k/v new rows   (B, Hkv, S_new,   D)
+ *       bias, extra    (B, 1,   S_q,     max_seq)   broadcast over heads
+ *       nonpad, write_idx, q_start   (B,) int64
+ *     Element type of q, y, caches, new rows, bias and extra: extkv_dtype.
+ *   - Return value: EXTKV_OK, or a negative extkv_status with a stable
+ *     message available from extkv_last_error() (thread-local).  Argument
+ *     errors are detected on the host before anything is launched.
+ *   - Data-dependent errors (an out-of-range write index or nonpad value)
+ *     cannot be seen on the host without a sync: the kernels skip the
+ *     offending batch and OR a flag into status[0] (EXTKV_DEV_*) and add one
+ *     to status[1].  `status` is NULL (no report) or 16 bytes of device
+ *     memory, 4-byte aligned, zeroed by extkv_clear_status or by the caller.
+ *   - Integer arithmetic on positions and lengths is signed 64-bit, so
+ *     differences such as nonpad - S_q may go negative without wrapping
+ *     ("ONNX Domain Attention (Opset 23/24) CUDA Patterns", section 12).
+ */
+#ifndef EXTKV_H_
+#define EXTKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { EXTKV_F32 = 0, EXTKV_BF16 = 1 } extkv_dtype;
+
+typedef enum {
+  EXTKV_OK = 0,
+  EXTKV_ERR_INVALID_ARG = -1, /* a null pointer, a bad size or a misaligned pointer */
+  EXTKV_ERR_UNSUPPORTED = -2, /* valid but not implemented (e.g. a forced kernel that cannot run) */
+  EXTKV_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed */
+  EXTKV_ERR_DEVICE = -4       /* extkv_read_status found a device-side flag */
+} extkv_status;
+
+/* Flags OR-ed into status[0] by the kernels. */
+#define EXTKV_DEV_BAD_WRITE_IDX 0x1 /* write_idx[b] < 0 or write_idx[b] + S_new > max_seq */
+#define EXTKV_DEV_BAD_NONPAD 0x2    /* nonpad[b] < 0 or nonpad[b] > max_seq */
+#define EXTKV_DEV_TIMEOUT 0x4       /* a bounded pipeline wait gave up; the tile was abandoned */
+
+/*
+ * The bias specification of mobius issue #366 (deliverable: causal + sliding
+ * window + bidirectional block overlay + padding, keyed on absolute query
+ * positions, valid only where slot < nonpad_kv_seqlen[b]).
+ *
+ * Query position of row i of batch b: p = q_start[b] + i, or, with q_start
+ * NULL, the bottom-right alignment of an external cache,
+ * p = max(nonpad[b] - S_q, 0) + i ("ONNX Domain Attention (Opset 23/24) CUDA
+ * Patterns", section 11).  Key slot j is allowed iff
+ *     j < nonpad[b]  and  ( (causal_ok and window_ok) or same_span )
+ *     causal_ok = !causal || j <= p
+ *     window_ok = window <= 0 || p - j < window   (keys p-W+1 .. p; "Skill:
+ *                 Attention Optimization", "GQA sliding window")
+ *     same_span = some span (start, len) of batch b holds both p and j
+ * An allowed slot carries extra[b,0,i,j] (or 0 when extra is NULL); any other
+ * slot carries the element type's lowest finite value (the CPU reference's
+ * sentinel, "ONNX Domain Attention ...", section 8).
+ *
+ * Spans: span_offsets (B+1,) int64 indexes rows of spans (n,2) int64 holding
+ * (start, len) in absolute positions; both NULL for no spans.  All pointer
+ * fields are device pointers and may be NULL.
+ */
+typedef struct {
+  int32_t causal;
+  int32_t window;
+  const int64_t *span_offsets;
+  const int64_t *spans;
+  const void *extra;
+  const int64_t *q_start;
+} extkv_bias_spec;
+
+/*
+ * TensorScatter of new K/V rows into the static cache, in place
+ * ("Skill: Attention Optimization", "In-place KV for ONNX Attention via
+ * TensorScatter (static cache)"): for every b < B, h < Hkv, s < S_new
+ *     k_cache[b,h,write_idx[b]+s,:] = k_new[b,h,s,:]   (and the same for V).
+ * The scatter runs along the sequence axis of the BNSH cache.  A bit-exact
+ * copy.  S_new == 0 (a KV-shared layer, which writes no K/V) is a no-op.
+ * Requires D * sizeof(T) % 16 == 0 and 16-byte aligned tensors.  A batch whose
+ * rows would leave [0, max_seq) is skipped and flagged EXTKV_DEV_BAD_WRITE_IDX.
+ */
+int ext_kv_scatter(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                   const int64_t *write_idx, int64_t B, int64_t Hkv, int64_t S_new,
+                   int64_t max_seq, int64_t D, int dtype, int32_t *status, void *stream);
+
+/*
+ * Materialises the (B,1,S_q,max_seq) additive bias of `spec` (see
+ * extkv_bias_spec; mobius issue #366, deliverable and acceptance criteria)
+ * into `bias`.  Bit-exact: every entry is either the extra term, +0, or
+ * lowest(T).  Requires max_seq * sizeof(T) % 16 == 0 and a 16-byte aligned
+ * `bias` (and `extra`).  A batch with nonpad outside [0, max_seq] is left
+ * untouched and flagged EXTKV_DEV_BAD_NONPAD.
+ */
+int build_static_cache_bias(void *bias, const extkv_bias_spec *spec, const int64_t *nonpad,
+                            int64_t B, int64_t S_q, int64_t max_seq, int dtype,
+                            int32_t *status, void *stream);
+
+/*
+ * Bytes of device workspace attention_ext_kv needs for these sizes.  The
+ * current kernels need none (0); callers pass the returned size anyway.
+ */
+size_t attention_ext_kv_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q,
+                                       int64_t max_seq, int64_t D, int dtype);
+
+/*
+ * Y = softmax(scale * Q K^T + bias) V over the external static cache, for
+ * a prefill chunk (S_q > 1) or a decode step (S_q == 1).
+ *   - Op order: scale*(Q@K^T), then + bias, then softmax, then @V
+ *     ("ONNX Domain Attention (Opset 23/24) CUDA Patterns", section 4; no
+ *     softcap).
+ *   - Grouped-query heads: query head h reads KV head h / (Hq/Hkv), no KV
+ *     replication (section 1, the reshape-Q trick).
+ *   - Masking: key j of row (b,i) is masked iff j >= nonpad[b] or its bias
+ *     is <= lowest(T) (the sentinel, or -inf).  A finite very negative bias
+ *     is not masked.  A row with no unmasked key, and every row of a batch
+ *     with nonpad[b] == 0, is written as exact zeros (section 6).  Cache slots
+ *     at or beyond nonpad[b] and masked slots are never read into the result,
+ *     whatever they hold (NaN included).
+ *   - The bias is one of: `bias` (a materialised (B,1,S_q,max_seq) tensor,
+ *     16-byte aligned), `fused` (the same specification evaluated in
+ *     registers, never materialised; results equal those of
+ *     build_static_cache_bias + `bias`), or neither (only nonpad masks).
+ *     Passing both is EXTKV_ERR_INVALID_ARG.
+ *   - A KV-shared layer ("[GQA] Support KV-shared layers with empty K/V
+ *     inputs", Design) is this call on the borrowed cache with no scatter.
+ *   - Accumulation is fp32; Y is rounded to T (nearest even).
+ *   - Requires Hq % Hkv == 0, 8 <= D <= 512 with D % 8 == 0.  A batch with
+ *     nonpad outside [0, max_seq] gets zero rows and EXTKV_DEV_BAD_NONPAD.
+ * `workspace` may be NULL when attention_ext_kv_workspace_size returns 0.
+ */
+int attention_ext_kv(void *y, const void *q, const void *k_cache, const void *v_cache,
+                     const void *bias, const extkv_bias_spec *fused, const int64_t *nonpad,
+                     float scale, int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q,
+                     int64_t max_seq, int64_t D, int dtype, void *workspace, size_t ws_bytes,
+                     int32_t *status, void *stream);
+
+/* Zeroes the 16-byte status word on `stream` (asynchronous). */
+int extkv_clear_status(int32_t *status, void *stream);
+
+/*
+ * Synchronises `stream`, copies the status word to the host and returns
+ * EXTKV_OK when no flag is set, else EXTKV_ERR_DEVICE with the flags spelled
+ * out in extkv_last_error().  The word is not cleared.
+ */
+int extkv_read_status(const int32_t *status, void *stream);
+
+/* Message of the calling thread's last failed call ("" if none). */
+const char *extkv_last_error(void);
+
+/*
+ * Name of the kernel the calling thread's last successful attention_ext_kv
+ * launched, so a test can check which path ran instead of trusting a
+ * fallback ("ONNX Domain Attention ...", section 7: always verify which
+ * runner a test actually hits).
+ */
+const char *extkv_last_kernel(void);
+
+/*
+ * Attention kernel selection for the calling thread.  EXTKV_ALGO_AUTO picks
+ * by shape and type; the others force one kernel, and attention_ext_kv then
+ * returns EXTKV_ERR_UNSUPPORTED for shapes that kernel cannot run.  Returns
+ * the previous setting, or EXTKV_ERR_INVALID_ARG for an unknown value.
+ */
+#define EXTKV_ALGO_AUTO 0
+#define EXTKV_ALGO_GENERIC 1 /* fp32 SIMT, one warp per query row: any supported shape */
+#define EXTKV_ALGO_DECODE 2  /* split-KV decode: bf16, S_q*Hq/Hkv <= 16, D in {64,128,256,512} */
+#define EXTKV_ALGO_PREFILL 3 /* tcgen05/TMEM prefill: bf16, D in {64,128,256} */
+int extkv_set_algo(int algo);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EXTKV_H_ */

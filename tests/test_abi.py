@@ -1,0 +1,83 @@
+"""The C ABI library loads and exports every symbol include/extkv.h declares,
+and rejects bad arguments on the host (CPU only: no call here reaches a
+kernel launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from biased_gqa_attention_gb300 import build as B
+from biased_gqa_attention_gb300 import extkv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "extkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return extkv.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_binding_symbols():
+    assert declared_functions() == sorted(extkv.SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    P = ctypes.c_void_p
+    fake = P(0x10000)  # never dereferenced: validation fails first
+    # Hq not a multiple of Hkv
+    rc = lib.attention_ext_kv(fake, fake, fake, fake, None, None, fake, 1.0, 1, 6, 4, 1, 64, 64,
+                              extkv.EXTKV_BF16, None, 0, None, None)
+    assert rc == extkv.EXTKV_ERR_INVALID_ARG
+    assert "multiple of Hkv" in extkv.extkv_last_error()
+    # D not supported
+    rc = lib.attention_ext_kv(fake, fake, fake, fake, None, None, fake, 1.0, 1, 4, 2, 1, 64, 12,
+                              extkv.EXTKV_BF16, None, 0, None, None)
+    assert rc == extkv.EXTKV_ERR_UNSUPPORTED
+    # both a materialised bias and a fused spec
+    spec = extkv._BiasSpec(1, 0, None, None, None, None)
+    rc = lib.attention_ext_kv(fake, fake, fake, fake, fake, ctypes.byref(spec), fake, 1.0, 1, 4, 2,
+                              1, 64, 64, extkv.EXTKV_BF16, None, 0, None, None)
+    assert rc == extkv.EXTKV_ERR_INVALID_ARG
+    # misaligned tensors
+    odd = P(0x10002)
+    rc = lib.attention_ext_kv(odd, fake, fake, fake, None, None, fake, 1.0, 1, 4, 2, 1, 64, 64,
+                              extkv.EXTKV_BF16, None, 0, None, None)
+    assert rc == extkv.EXTKV_ERR_INVALID_ARG
+    # unknown dtype
+    rc = lib.ext_kv_scatter(fake, fake, fake, fake, fake, 1, 1, 1, 8, 64, 7, None, None)
+    assert rc == extkv.EXTKV_ERR_INVALID_ARG
+    # S_new larger than the cache
+    rc = lib.ext_kv_scatter(fake, fake, fake, fake, fake, 1, 1, 9, 8, 64, extkv.EXTKV_BF16, None, None)
+    assert rc == extkv.EXTKV_ERR_INVALID_ARG
+    # bias row stride not a multiple of 16 bytes
+    rc = lib.build_static_cache_bias(fake, ctypes.byref(spec), fake, 1, 1, 12, extkv.EXTKV_BF16,
+                                     None, None)
+    assert rc == extkv.EXTKV_ERR_UNSUPPORTED
+    # empty problems are valid no-ops (nothing is launched)
+    assert lib.attention_ext_kv(None, None, None, None, None, None, None, 1.0, 0, 4, 2, 1, 64, 64,
+                                extkv.EXTKV_BF16, None, 0, None, None) == extkv.EXTKV_OK
+    assert lib.ext_kv_scatter(None, None, None, None, None, 2, 2, 0, 64, 64, extkv.EXTKV_BF16, None,
+                              None) == extkv.EXTKV_OK
+    # algorithm selection
+    assert lib.extkv_set_algo(99) == extkv.EXTKV_ERR_INVALID_ARG
+    prev = lib.extkv_set_algo(extkv.ALGO_GENERIC)
+    assert lib.extkv_set_algo(prev) == extkv.ALGO_GENERIC
+
+
+def test_workspace_size_is_queryable(lib):
+    assert extkv.attention_ext_kv_workspace_size(8, 16, 8, 1, 4096, 256, None) >= 0
