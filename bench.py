@@ -237,6 +237,7 @@ class Decoder:
                                     spans=base.span_table, extra=s["extra"])
             self.sets.append(s)
         self.status = ek.new_status(device)
+        self.workspace = ek.new_workspace(base.q, base.k_cache)
 
     def scatter(self, r):
         s = self.sets[r]
@@ -250,7 +251,8 @@ class Decoder:
         s = self.sets[r]
         self.ek.attention_ext_kv(s["y"], s["q"], s["k"], s["v"], s["nonpad"], self.w.scale,
                                  bias=s["bias"] if self.mode == "bias" else None,
-                                 fused=s["spec"] if self.mode == "fused" else None, status=self.status)
+                                 fused=s["spec"] if self.mode == "fused" else None,
+                                 workspace=self.workspace, status=self.status)
 
     def step(self, r, ev=None):
         self.scatter(r)
@@ -263,7 +265,10 @@ class Decoder:
             ev[1].record()
 
     def kernels_per_step(self):
-        return 1 + (1 if self.mode == "bias" else 0) + 1
+        # scatter, bias build, attention (the decode path launches a plan
+        # kernel and the stream-K kernel)
+        attn = 2 if self.workspace is not None else 1
+        return 1 + (1 if self.mode == "bias" else 0) + attn
 
 
 def _events(n, external):

@@ -10,9 +10,9 @@ built (``biased_gqa_attention_gb300.build.build()``).
 from .extkv import (ALGO_AUTO, ALGO_DECODE, ALGO_GENERIC, ALGO_PREFILL, BiasSpec, ExtKVError,
                     attention_ext_kv, attention_ext_kv_workspace_size, build_static_cache_bias,
                     ext_kv_scatter, extkv_clear_status, extkv_last_error, extkv_last_kernel,
-                    extkv_read_status, extkv_set_algo, new_status, use_algo)
+                    extkv_read_status, extkv_set_algo, new_status, new_workspace, use_algo)
 
 __all__ = ["ALGO_AUTO", "ALGO_DECODE", "ALGO_GENERIC", "ALGO_PREFILL", "BiasSpec", "ExtKVError",
            "attention_ext_kv", "attention_ext_kv_workspace_size", "build_static_cache_bias",
            "ext_kv_scatter", "extkv_clear_status", "extkv_last_error", "extkv_last_kernel",
-           "extkv_read_status", "extkv_set_algo", "new_status", "use_algo"]
+           "extkv_read_status", "extkv_set_algo", "new_status", "new_workspace", "use_algo"]

@@ -37,6 +37,17 @@ int64_t elem_size(int dtype) { return dtype == EXTKV_F32 ? 4 : 2; }
 
 bool valid_dtype(int dtype) { return dtype == EXTKV_F32 || dtype == EXTKV_BF16; }
 
+int check_workspace(const AttnArgs& a) {
+  const size_t need = decode_workspace_bytes(a.B, a.Hq, a.Hkv, a.S_q, a.max_seq, a.D);
+  if (a.ws_bytes < need || (need && !a.workspace))
+    return fail(EXTKV_ERR_INVALID_ARG,
+                "attention_ext_kv: workspace of %zu bytes required (got %zu); query attention_ext_kv_workspace_size",
+                need, a.ws_bytes);
+  if (!aligned(a.workspace, 256))
+    return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv: workspace must be 256-byte aligned");
+  return EXTKV_OK;
+}
+
 }  // namespace
 
 int num_sms() {
@@ -111,8 +122,20 @@ int build_static_cache_bias(void* bias, const extkv_bias_spec* spec, const int64
   return EXTKV_OK;
 }
 
-size_t attention_ext_kv_workspace_size(int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int) {
-  return 0;
+size_t attention_ext_kv_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq,
+                                       int64_t D, int dtype) {
+  // Only the decode kernel uses workspace (its plan and its split-unit partials).
+  if (dtype != EXTKV_BF16 || B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || S_q <= 0 || max_seq <= 0) return 0;
+  AttnArgs a{};
+  a.dtype = dtype;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.S_q = S_q;
+  a.max_seq = max_seq;
+  a.D = D;
+  if (!decode_supported(a)) return 0;
+  return decode_workspace_bytes(B, Hq, Hkv, S_q, max_seq, D);
 }
 
 int attention_ext_kv(void* y, const void* q, const void* k_cache, const void* v_cache,
@@ -120,8 +143,6 @@ int attention_ext_kv(void* y, const void* q, const void* k_cache, const void* v_
                      float scale, int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq,
                      int64_t D, int dtype, void* workspace, size_t ws_bytes, int32_t* status,
                      void* stream) {
-  (void)workspace;
-  (void)ws_bytes;
   g_error[0] = 0;
   if (!valid_dtype(dtype)) return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv: unknown dtype %d", dtype);
   if (B < 0 || S_q < 0 || Hq <= 0 || Hkv <= 0 || max_seq <= 0 || D <= 0)
@@ -173,6 +194,8 @@ int attention_ext_kv(void* y, const void* q, const void* k_cache, const void* v_
   a.D = D;
   a.dtype = dtype;
   a.status = status;
+  a.workspace = workspace;
+  a.ws_bytes = ws_bytes;
   a.stream = static_cast<cudaStream_t>(stream);
 
   const char* name = "";
@@ -184,6 +207,7 @@ int attention_ext_kv(void* y, const void* q, const void* k_cache, const void* v_
     case EXTKV_ALGO_DECODE:
       if (!decode_supported(a))
         return fail(EXTKV_ERR_UNSUPPORTED, "attention_ext_kv: the decode kernel cannot run this shape/type");
+      if (int rc = check_workspace(a)) return rc;
       e = launch_attn_decode(a, &name);
       break;
     case EXTKV_ALGO_PREFILL:
@@ -192,7 +216,10 @@ int attention_ext_kv(void* y, const void* q, const void* k_cache, const void* v_
       e = launch_attn_prefill(a, &name);
       break;
     default:
-      if (decode_supported(a)) e = launch_attn_decode(a, &name);
+      if (decode_supported(a)) {
+        if (int rc = check_workspace(a)) return rc;
+        e = launch_attn_decode(a, &name);
+      }
       else if (prefill_supported(a)) e = launch_attn_prefill(a, &name);
       else e = launch_attn_generic(a, &name);
   }

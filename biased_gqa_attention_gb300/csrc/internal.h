@@ -27,6 +27,8 @@ struct AttnArgs {
   int64_t B, Hq, Hkv, S_q, max_seq, D;
   int dtype;
   int32_t* status;
+  void* workspace;
+  size_t ws_bytes;
   cudaStream_t stream;
 };
 
@@ -43,6 +45,7 @@ cudaError_t launch_attn_generic(const AttnArgs& a, const char** name);
 
 // Fast paths: `supported` says whether the shape can run; launch returns the error.
 bool decode_supported(const AttnArgs& a);
+size_t decode_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t D);
 cudaError_t launch_attn_decode(const AttnArgs& a, const char** name);
 bool prefill_supported(const AttnArgs& a);
 cudaError_t launch_attn_prefill(const AttnArgs& a, const char** name);

@@ -5,8 +5,31 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace extkv {
+
+namespace {
+
+cudaLaunchConfig_t pdl_config(int blocks, int threads, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(threads);
+  cfg.stream = stream;
+  return cfg;
+}
+
+// Programmatic dependent launch: the kernel may be scheduled while the
+// previous kernel in the stream drains; it waits (griddepcontrol.wait)
+// before touching global memory.
+void pdl_attr(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr) {
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+}
+
+}  // namespace
 
 // ---- TensorScatter ----------------------------------------------------------
 // "Skill: Attention Optimization", "In-place KV for ONNX Attention via
@@ -24,6 +47,11 @@ __global__ void __launch_bounds__(256) scatter_kernel(uint4* __restrict__ k_cach
                                                       int64_t Hkv, int64_t S_new, int64_t max_seq,
                                                       int64_t row_vecs, int64_t total,
                                                       int32_t* status) {
+  // Launched as a programmatic dependent: wait for the previous grid's memory
+  // (the previous step may still read these cache rows), then let the next
+  // kernel start its prologue.
+  ptx::grid_dependency_wait();
+  ptx::grid_launch_dependents();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += stride) {
@@ -56,11 +84,14 @@ cudaError_t launch_scatter(void* k_cache, void* v_cache, const void* k_new, cons
   const int threads = 256;
   const int64_t want = (total + threads - 1) / threads;
   const int blocks = static_cast<int>(std::min<int64_t>(want, int64_t(num_sms()) * 8));
-  scatter_kernel<<<blocks, threads, 0, stream>>>(
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
-      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), write_idx, Hkv, S_new,
-      max_seq, row_vecs, total, status);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = pdl_config(blocks, threads, stream);
+  cudaLaunchAttribute attr[1];
+  pdl_attr(cfg, attr);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, scatter_kernel, static_cast<uint4*>(k_cache),
+                                     static_cast<uint4*>(v_cache), static_cast<const uint4*>(k_new),
+                                     static_cast<const uint4*>(v_new), write_idx, Hkv, S_new,
+                                     max_seq, row_vecs, total, status);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // ---- static-cache bias ------------------------------------------------------
@@ -76,6 +107,8 @@ __global__ void __launch_bounds__(256) bias_kernel(uint4* __restrict__ bias, Bia
                                                    int64_t total, int32_t* status) {
   constexpr int kVec = 16 / sizeof(T);
   using E = Elem<T>;
+  ptx::grid_dependency_wait();
+  ptx::grid_launch_dependents();
   const uint4* extra = static_cast<const uint4*>(spec.extra);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
@@ -120,13 +153,16 @@ cudaError_t launch_bias(void* bias, const extkv_bias_spec& s, const int64_t* non
   const int threads = 256;
   const int64_t want = (total + threads - 1) / threads;
   const int blocks = static_cast<int>(std::min<int64_t>(want, int64_t(num_sms()) * 8));
-  if (dtype == EXTKV_F32)
-    bias_kernel<float><<<blocks, threads, 0, stream>>>(static_cast<uint4*>(bias), spec, nonpad,
-                                                       S_q, max_seq, row_vecs, total, status);
-  else
-    bias_kernel<__nv_bfloat16><<<blocks, threads, 0, stream>>>(
-        static_cast<uint4*>(bias), spec, nonpad, S_q, max_seq, row_vecs, total, status);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = pdl_config(blocks, threads, stream);
+  cudaLaunchAttribute attr[1];
+  pdl_attr(cfg, attr);
+  cudaError_t e =
+      dtype == EXTKV_F32
+          ? cudaLaunchKernelEx(&cfg, bias_kernel<float>, static_cast<uint4*>(bias), spec, nonpad,
+                               S_q, max_seq, row_vecs, total, status)
+          : cudaLaunchKernelEx(&cfg, bias_kernel<__nv_bfloat16>, static_cast<uint4*>(bias), spec,
+                               nonpad, S_q, max_seq, row_vecs, total, status);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace extkv

@@ -150,13 +150,24 @@ def build_static_cache_bias(bias, spec: BiasSpec, nonpad, status=None, stream=No
 
 
 def attention_ext_kv_workspace_size(B, Hq, Hkv, S_q, max_seq, D, dtype) -> int:
+    """Bytes of device workspace attention_ext_kv needs (queries the current device)."""
     return int(load().attention_ext_kv_workspace_size(B, Hq, Hkv, S_q, max_seq, D,
                                                       EXTKV_F32 if dtype == torch.float32 else EXTKV_BF16))
 
 
+def new_workspace(q: torch.Tensor, k_cache: torch.Tensor) -> Optional[torch.Tensor]:
+    """A workspace sized for attention over these q / cache shapes (None if none is needed)."""
+    B, Hq, S_q, D = q.shape
+    n = attention_ext_kv_workspace_size(B, Hq, k_cache.shape[1], S_q, k_cache.shape[2], D, q.dtype)
+    return torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
+
+
 def attention_ext_kv(y, q, k_cache, v_cache, nonpad, scale, bias=None, fused: Optional[BiasSpec] = None,
                      workspace=None, status=None, stream=None):
-    """Y = softmax(scale*QK^T + bias)V over the external cache; writes ``y`` (B,Hq,S_q,D)."""
+    """Y = softmax(scale*QK^T + bias)V over the external cache; writes ``y`` (B,Hq,S_q,D).
+
+    ``workspace`` (uint8 device tensor of attention_ext_kv_workspace_size bytes)
+    is allocated here when not given."""
     for t, n in ((y, "y"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
         _need(t, n, dims=4, dtype=q.dtype)
     _need(bias, "bias", dims=4, dtype=q.dtype)
@@ -167,6 +178,10 @@ def attention_ext_kv(y, q, k_cache, v_cache, nonpad, scale, bias=None, fused: Op
             k_cache.shape[3] != D:
         raise ValueError("inconsistent q / y / cache shapes")
     c = None if fused is None else fused._c()
+    if workspace is None:
+        need = load().attention_ext_kv_workspace_size(B, Hq, Hkv, S_q, max_seq, D, _dt(q))
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().attention_ext_kv(_p(y), _p(q), _p(k_cache), _p(v_cache), _p(bias),
                                    None if c is None else ctypes.byref(c), _p(nonpad), float(scale),

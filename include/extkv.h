@@ -123,8 +123,12 @@ int build_static_cache_bias(void *bias, const extkv_bias_spec *spec, const int64
                             int32_t *status, void *stream);
 
 /*
- * Bytes of device workspace attention_ext_kv needs for these sizes.  The
- * current kernels need none (0); callers pass the returned size anyway.
+ * Bytes of device workspace attention_ext_kv needs for these sizes on the
+ * current device.  The decode path keeps its live-tile plan and the partial
+ * results of units split across CTAs there; the other paths need none (0).
+ * The caller allocates it, 256-byte aligned, and may reuse it for every call
+ * on one stream; calls that can overlap on the GPU need separate workspaces.
+ * Contents need no initialisation and are not preserved between calls.
  */
 size_t attention_ext_kv_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q,
                                        int64_t max_seq, int64_t D, int dtype);
@@ -153,7 +157,9 @@ size_t attention_ext_kv_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64
  *   - Accumulation is fp32; Y is rounded to T (nearest even).
  *   - Requires Hq % Hkv == 0, 8 <= D <= 512 with D % 8 == 0.  A batch with
  *     nonpad outside [0, max_seq] gets zero rows and EXTKV_DEV_BAD_NONPAD.
- * `workspace` may be NULL when attention_ext_kv_workspace_size returns 0.
+ * `workspace` / `ws_bytes`: at least attention_ext_kv_workspace_size(...)
+ * bytes of device memory (see there); may be NULL when that size is 0.  Too
+ * small a workspace is EXTKV_ERR_INVALID_ARG.
  */
 int attention_ext_kv(void *y, const void *q, const void *k_cache, const void *v_cache,
                      const void *bias, const extkv_bias_spec *fused, const int64_t *nonpad,
@@ -190,7 +196,7 @@ const char *extkv_last_kernel(void);
  */
 #define EXTKV_ALGO_AUTO 0
 #define EXTKV_ALGO_GENERIC 1 /* fp32 SIMT, one warp per query row: any supported shape */
-#define EXTKV_ALGO_DECODE 2  /* split-KV decode: bf16, S_q*Hq/Hkv <= 16, D in {64,128,256,512} */
+#define EXTKV_ALGO_DECODE 2  /* stream-K split-KV decode: bf16, S_q*Hq/Hkv <= 8, D in {64,128,256,512} */
 #define EXTKV_ALGO_PREFILL 3 /* tcgen05/TMEM prefill: bf16, D in {64,128,256} */
 int extkv_set_algo(int algo);
 

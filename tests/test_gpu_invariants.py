@@ -24,7 +24,7 @@ from helpers import raw
 
 pytestmark = pytest.mark.gpu
 
-DEC = "attn_decode_splitkv_mma"
+DEC = "attn_decode_streamk_mma"
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -229,3 +229,21 @@ def test_empty_calls_and_forced_kernel_refusal():
             ek.attention_ext_kv(torch.empty_like(qf), qf, kf, kf,
                                 torch.tensor([17], dtype=torch.int64, device="cuda"), w.scale)
     assert e.value.code == ek.EXTKV_ERR_UNSUPPORTED
+
+
+def test_decode_workspace_is_checked():
+    w = wl.small(wl.C2)
+    inp = wl.make_inputs(w, "cuda")
+    need = ek.attention_ext_kv_workspace_size(w.B, w.Hq, w.Hkv, w.S_q, w.max_seq, w.D, w.dtype)
+    assert need > 0
+    y = torch.empty_like(inp.q)
+    small_ws = torch.empty(need // 2, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ek.ExtKVError) as e:
+        ek.attention_ext_kv(y, inp.q, inp.k_cache, inp.v_cache, inp.nonpad, w.scale, workspace=small_ws)
+    assert e.value.code == ek.EXTKV_ERR_INVALID_ARG and "workspace" in str(e.value)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    # one workspace serves consecutive calls on the stream
+    for _ in range(2):
+        ek.attention_ext_kv(y, inp.q, inp.k_cache, inp.v_cache, inp.nonpad, w.scale, workspace=ws)
+    o = oracle_path(inp, mode="none", scatter=False)
+    assert max_err(y, o["y"]) <= TOL[w.dtype]
