@@ -50,6 +50,8 @@ int check_workspace(const AttnArgs& a) {
 
 }  // namespace
 
+void set_error(const char* msg) { snprintf(g_error, sizeof g_error, "%s", msg); }
+
 int num_sms() {
   // Cached per device; the SM count never changes for a device.
   static thread_local int cached_dev = -1, cached = 0;

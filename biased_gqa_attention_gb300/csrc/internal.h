@@ -52,4 +52,7 @@ cudaError_t launch_attn_prefill(const AttnArgs& a, const char** name);
 
 int num_sms();
 
+// Sets the calling thread's extkv_last_error() message.
+void set_error(const char* msg);
+
 }  // namespace extkv

@@ -24,7 +24,7 @@ ALGO_AUTO, ALGO_GENERIC, ALGO_DECODE, ALGO_PREFILL = 0, 1, 2, 3
 # Every symbol include/extkv.h declares.
 SYMBOLS = ("ext_kv_scatter", "build_static_cache_bias", "attention_ext_kv_workspace_size",
            "attention_ext_kv", "extkv_clear_status", "extkv_read_status", "extkv_last_error",
-           "extkv_last_kernel", "extkv_set_algo")
+           "extkv_last_kernel", "extkv_set_algo", "attention_ext_kv_noalloc")
 
 
 class ExtKVError(RuntimeError):
@@ -57,12 +57,14 @@ def load(path: str = LIB_PATH):
     lib.attention_ext_kv_workspace_size.restype = ctypes.c_size_t
     lib.attention_ext_kv.argtypes = [P, P, P, P, P, ctypes.POINTER(_BiasSpec), P, ctypes.c_float,
                                      I64, I64, I64, I64, I64, I64, I, P, ctypes.c_size_t, I32P, P]
+    lib.attention_ext_kv_noalloc.argtypes = [P, P, P, P, P, ctypes.POINTER(_BiasSpec), P,
+                                             ctypes.c_float, I64, I64, I64, I64, I64, I64, I, I32P, P]
     lib.extkv_clear_status.argtypes = [I32P, P]
     lib.extkv_read_status.argtypes = [I32P, P]
     lib.extkv_last_error.restype = ctypes.c_char_p
     lib.extkv_last_kernel.restype = ctypes.c_char_p
     lib.extkv_set_algo.argtypes = [I]
-    for name in ("ext_kv_scatter", "build_static_cache_bias", "attention_ext_kv",
+    for name in ("ext_kv_scatter", "build_static_cache_bias", "attention_ext_kv", "attention_ext_kv_noalloc",
                  "extkv_clear_status", "extkv_read_status", "extkv_set_algo"):
         getattr(lib, name).restype = I
     _lib = lib
@@ -187,6 +189,29 @@ def attention_ext_kv(y, q, k_cache, v_cache, nonpad, scale, bias=None, fused: Op
                                    None if c is None else ctypes.byref(c), _p(nonpad), float(scale),
                                    B, Hq, Hkv, S_q, max_seq, D, _dt(q), _p(workspace), ws, _p(status),
                                    _stream(stream)))
+
+
+def attention_ext_kv_noalloc(y, q, k_cache, v_cache, nonpad, scale, bias=None,
+                             fused: Optional[BiasSpec] = None, status=None, stream=None):
+    """attention_ext_kv without a workspace, for callers that cannot allocate
+    device memory (for instance an operator that is handed only its input and
+    output buffers).  Decode shapes only; the scratch is a static 16 MiB array
+    inside the library, shared by every call on the device, so calls that may
+    overlap on the GPU must not use it concurrently."""
+    for t, n in ((y, "y"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, dims=4, dtype=q.dtype)
+    _need(bias, "bias", dims=4, dtype=q.dtype)
+    _need(nonpad, "nonpad", dims=1, dtype=torch.int64)
+    B, Hq, S_q, D = q.shape
+    Hkv, max_seq = k_cache.shape[1], k_cache.shape[2]
+    if y.shape != q.shape or v_cache.shape != k_cache.shape or k_cache.shape[0] != B or \
+            k_cache.shape[3] != D:
+        raise ValueError("inconsistent q / y / cache shapes")
+    c = None if fused is None else fused._c()
+    _check(load().attention_ext_kv_noalloc(_p(y), _p(q), _p(k_cache), _p(v_cache), _p(bias),
+                                           None if c is None else ctypes.byref(c), _p(nonpad),
+                                           float(scale), B, Hq, Hkv, S_q, max_seq, D, _dt(q),
+                                           _p(status), _stream(stream)))
 
 
 def new_status(device="cuda") -> torch.Tensor:

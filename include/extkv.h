@@ -167,6 +167,37 @@ int attention_ext_kv(void *y, const void *q, const void *k_cache, const void *v_
                      int64_t max_seq, int64_t D, int dtype, void *workspace, size_t ws_bytes,
                      int32_t *status, void *stream);
 
+/*
+ * Size of the static scratch array behind attention_ext_kv_noalloc: 16 MiB of
+ * device memory, held by every GPU that loads this library until exit.
+ */
+#define EXTKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * attention_ext_kv for callers that cannot allocate device memory.  The pages
+ * have no counterpart; it exists for code that is handed only its input and
+ * output buffers -- e.g. a custom operator of an inference runtime whose
+ * operator interface offers no scratch allocator, or a latency-critical path
+ * where a cudaMalloc (which may synchronise the device) is not acceptable.
+ *   - Same arguments and results as attention_ext_kv without the workspace:
+ *     the decode path's scratch lives in a static device array of
+ *     EXTKV_NOALLOC_SCRATCH_BYTES.  This call allocates nothing.
+ *   - Decode shapes only (bf16, (Hq/Hkv)*S_q <= 8, D in {64,128,256,512});
+ *     other shapes, and sizes whose scratch would exceed the array, return
+ *     EXTKV_ERR_UNSUPPORTED with a message.
+ *   - The first call on a device looks up the array's device address (one
+ *     cudaGetSymbolAddress); make that first call outside any stream capture.
+ *   - Every call on a device shares the one array, and it keeps the previous
+ *     call's contents (the call clears what must start at zero itself).  Calls
+ *     that can overlap on the GPU -- on different streams without ordering --
+ *     race on it.
+ */
+int attention_ext_kv_noalloc(void *y, const void *q, const void *k_cache, const void *v_cache,
+                             const void *bias, const extkv_bias_spec *fused,
+                             const int64_t *nonpad, float scale, int64_t B, int64_t Hq,
+                             int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t D, int dtype,
+                             int32_t *status, void *stream);
+
 /* Zeroes the 16-byte status word on `stream` (asynchronous). */
 int extkv_clear_status(int32_t *status, void *stream);
 
