@@ -14,7 +14,7 @@
 #include <cstdio>
 #include <mutex>
 
-#include "../../include/extkv.h"
+#include "extkv.h"
 #include "internal.h"
 
 namespace extkv {

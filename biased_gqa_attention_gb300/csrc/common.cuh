@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/extkv.h"
+#include "extkv.h"
 
 namespace extkv {
 

@@ -7,7 +7,7 @@
 #include <cstdio>
 #include <cstring>
 
-#include "../../include/extkv.h"
+#include "extkv.h"
 #include "internal.h"
 
 namespace extkv {
