@@ -37,8 +37,7 @@ int64_t elem_size(int dtype) { return dtype == EXTKV_F32 ? 4 : 2; }
 
 bool valid_dtype(int dtype) { return dtype == EXTKV_F32 || dtype == EXTKV_BF16; }
 
-int check_workspace(const AttnArgs& a) {
-  const size_t need = decode_workspace_bytes(a.B, a.Hq, a.Hkv, a.S_q, a.max_seq, a.D);
+int check_workspace(const AttnArgs& a, size_t need) {
   if (a.ws_bytes < need || (need && !a.workspace))
     return fail(EXTKV_ERR_INVALID_ARG,
                 "attention_ext_kv: workspace of %zu bytes required (got %zu); query attention_ext_kv_workspace_size",
@@ -126,7 +125,8 @@ int build_static_cache_bias(void* bias, const extkv_bias_spec* spec, const int64
 
 size_t attention_ext_kv_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq,
                                        int64_t D, int dtype) {
-  // Only the decode kernel uses workspace (its plan and its split-unit partials).
+  // The decode kernel keeps its plan and its split-unit partials there; the
+  // prefill kernel keeps the live key ranges of a materialised bias.
   if (dtype != EXTKV_BF16 || B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || S_q <= 0 || max_seq <= 0) return 0;
   AttnArgs a{};
   a.dtype = dtype;
@@ -136,8 +136,14 @@ size_t attention_ext_kv_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64
   a.S_q = S_q;
   a.max_seq = max_seq;
   a.D = D;
-  if (!decode_supported(a)) return 0;
-  return decode_workspace_bytes(B, Hq, Hkv, S_q, max_seq, D);
+  // enough for whichever kernel runs, automatic or chosen by extkv_set_algo
+  size_t need = 0;
+  if (decode_supported(a)) need = decode_workspace_bytes(B, Hq, Hkv, S_q, max_seq, D);
+  if (prefill_supported(a)) {
+    const size_t pf = prefill_workspace_bytes(B, S_q, max_seq);
+    need = pf > need ? pf : need;
+  }
+  return need;
 }
 
 int attention_ext_kv(void* y, const void* q, const void* k_cache, const void* v_cache,
@@ -202,6 +208,9 @@ int attention_ext_kv(void* y, const void* q, const void* k_cache, const void* v_
 
   const char* name = "";
   cudaError_t e;
+  const size_t decode_ws = decode_workspace_bytes(B, Hq, Hkv, S_q, max_seq, D);
+  // only a materialised bias needs the prefill kernel's range table
+  const size_t prefill_ws = bias ? prefill_workspace_bytes(B, S_q, max_seq) : 0;
   switch (g_algo) {
     case EXTKV_ALGO_GENERIC:
       e = launch_attn_generic(a, &name);
@@ -209,21 +218,25 @@ int attention_ext_kv(void* y, const void* q, const void* k_cache, const void* v_
     case EXTKV_ALGO_DECODE:
       if (!decode_supported(a))
         return fail(EXTKV_ERR_UNSUPPORTED, "attention_ext_kv: the decode kernel cannot run this shape/type");
-      if (int rc = check_workspace(a)) return rc;
+      if (int rc = check_workspace(a, decode_ws)) return rc;
       e = launch_attn_decode(a, &name);
       break;
     case EXTKV_ALGO_PREFILL:
       if (!prefill_supported(a))
         return fail(EXTKV_ERR_UNSUPPORTED, "attention_ext_kv: the prefill kernel cannot run this shape/type");
+      if (int rc = check_workspace(a, prefill_ws)) return rc;
       e = launch_attn_prefill(a, &name);
       break;
     default:
       if (decode_supported(a)) {
-        if (int rc = check_workspace(a)) return rc;
+        if (int rc = check_workspace(a, decode_ws)) return rc;
         e = launch_attn_decode(a, &name);
+      } else if (prefill_supported(a)) {
+        if (int rc = check_workspace(a, prefill_ws)) return rc;
+        e = launch_attn_prefill(a, &name);
+      } else {
+        e = launch_attn_generic(a, &name);
       }
-      else if (prefill_supported(a)) e = launch_attn_prefill(a, &name);
-      else e = launch_attn_generic(a, &name);
   }
   if (e != cudaSuccess) return cuda_fail(e, "attention_ext_kv launch");
   g_last_kernel = name;

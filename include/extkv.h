@@ -124,8 +124,11 @@ int build_static_cache_bias(void *bias, const extkv_bias_spec *spec, const int64
 
 /*
  * Bytes of device workspace attention_ext_kv needs for these sizes on the
- * current device.  The decode path keeps its live-tile plan and the partial
- * results of units split across CTAs there; the other paths need none (0).
+ * current device: enough for whichever kernel runs, chosen automatically or
+ * by extkv_set_algo.  The decode path keeps its live-tile plan and the
+ * partial results of units split across CTAs there; the prefill path, with a
+ * materialised bias, the live key range of every (batch, 128-row query tile,
+ * 512-key chunk); the generic path needs none (0).
  * The caller allocates it, 256-byte aligned, and may reuse it for every call
  * on one stream; calls that can overlap on the GPU need separate workspaces.
  * Contents need no initialisation and are not preserved between calls.
