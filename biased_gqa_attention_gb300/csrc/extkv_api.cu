@@ -209,8 +209,9 @@ int attention_ext_kv(void* y, const void* q, const void* k_cache, const void* v_
   const char* name = "";
   cudaError_t e;
   const size_t decode_ws = decode_workspace_bytes(B, Hq, Hkv, S_q, max_seq, D);
-  // only a materialised bias needs the prefill kernel's range table
-  const size_t prefill_ws = bias ? prefill_workspace_bytes(B, S_q, max_seq) : 0;
+  // a materialised bias or an extra term needs the prefill kernel's column-mask table
+  const size_t prefill_ws =
+      (bias || (fused && fused->extra)) ? prefill_workspace_bytes(B, S_q, max_seq) : 0;
   switch (g_algo) {
     case EXTKV_ALGO_GENERIC:
       e = launch_attn_generic(a, &name);

@@ -127,8 +127,8 @@ int build_static_cache_bias(void *bias, const extkv_bias_spec *spec, const int64
  * current device: enough for whichever kernel runs, chosen automatically or
  * by extkv_set_algo.  The decode path keeps its live-tile plan and the
  * partial results of units split across CTAs there; the prefill path, with a
- * materialised bias, the live key range of every (batch, 128-row query tile,
- * 512-key chunk); the generic path needs none (0).
+ * materialised bias or an extra term, one 64-bit mask of attended keys per
+ * (batch, 128-row query tile, 64-key tile); the generic path needs none (0).
  * The caller allocates it, 256-byte aligned, and may reuse it for every call
  * on one stream; calls that can overlap on the GPU need separate workspaces.
  * Contents need no initialisation and are not preserved between calls.
