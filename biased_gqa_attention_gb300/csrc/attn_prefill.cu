@@ -60,41 +60,53 @@ namespace extkv {
 namespace {
 
 constexpr int kBM = 128;                   // query rows per CTA (M, tensor-memory lanes)
-constexpr int kBN = 64;                    // keys per KV tile
+constexpr int kBN = 128;                   // keys per KV tile (N of S = Q K^T)
 constexpr int kThreads = 192;              // producer, MMA, 4 softmax warps
-constexpr int kPlanKeys = 512;             // keys per plan block
+constexpr int kPlanKeys = 256;             // keys per plan block (8 per lane)
 constexpr int kPlanThreads = 256;
 constexpr uint32_t kWaitPolls = 1u << 22;  // bounded mbarrier waits
-constexpr int kMaxSlots = 8;
+constexpr int kMaxUnits = 8;
 
 enum Mode { kNone = 0, kBias = 1, kFused = 2, kFusedExtra = 3 };
 
+// K/V tiles (128 keys x D) stream through a ring of load units of at most
+// 32 KB: for D = 256 a K tile is two units split by head-dim halves (each
+// feeds half of the K steps of Q K^T) and a V tile two units split by key
+// halves (each feeds half of the K steps of P V); otherwise a tile is one unit.
 template <int D, int MODE>
 struct Cfg {
-  static constexpr bool kTerm = MODE == kBias || MODE == kFusedExtra;  // a 128 x 64 block per tile
-  static constexpr int kSlotBytes = kBN * D * 2;
+  static constexpr bool kTerm = MODE == kBias || MODE == kFusedExtra;  // a 128 x 128 block per tile
+  static constexpr bool kQSmem = D > 128;  // Q as a shared-memory A operand (no tensor-memory room)
+  static constexpr int kParts = D > 128 ? 2 : 1;
+  static constexpr int kUnitBytes = kBN * D * 2 / kParts;
+  static constexpr int kKChunks = D / 64 / kParts;  // 64-column chunks in a K unit
+  static constexpr int kVKeys = kBN / kParts;       // keys in a V unit
+  static constexpr int kQBytes = kQSmem ? kBM * D * 2 : 0;
   static constexpr int kTermBytes = kTerm ? kBM * kBN * 2 : 0;
+  static constexpr int kTermBufs = kTerm ? (kQSmem ? 1 : 2) : 0;
+  static constexpr int kTB = kTermBufs > 0 ? kTermBufs : 1;  // divisor for buffer indexing
   static constexpr int kBudget = 232448 - 1024 - 512;  // opt-in maximum, alignment, barriers
-  static constexpr int kFit = (kBudget - 2 * kTermBytes) / kSlotBytes;
-  static constexpr int kNS = kFit > kMaxSlots ? kMaxSlots : kFit;
-  static constexpr int kOffKV = 0;
-  static constexpr int kOffT = kOffKV + kNS * kSlotBytes;
-  static constexpr int kOffBar = kOffT + 2 * kTermBytes;
+  static constexpr int kFit = (kBudget - kQBytes - kTermBufs * kTermBytes) / kUnitBytes;
+  static constexpr int kNU = kFit > kMaxUnits ? kMaxUnits : kFit;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = kQBytes;
+  static constexpr int kOffT = kOffKV + kNU * kUnitBytes;
+  static constexpr int kOffBar = kOffT + kTermBufs * kTermBytes;
   static constexpr int kSmem = kOffBar + 512 + 1024;
-  // tensor memory: S buffers at columns 0 and 64 (P_j over the first 32
-  // columns of S_j), Q at 128, O at a multiple of its width
-  static constexpr uint32_t kQCol = 128;
-  static constexpr uint32_t kOCol = D == 64 ? 192 : 256;
-  static constexpr uint32_t kTmemCols = D == 64 ? 256 : 512;
+  // tensor memory: S_0, S_1 at columns 0 and 128 (P_j, bf16, over the first 64
+  // columns of S_j), O at 256, Q (when held there) after O
+  static constexpr uint32_t kOCol = 256;
+  static constexpr uint32_t kQCol = kOCol + D;
+  static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kBM, kBN, 0, 0);
   static constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kBM, D, 0, 1);
-  static_assert(kNS >= 2, "shared memory holds fewer than two K/V slots");
-  static_assert(kQCol + D / 2 <= kOCol && kOCol + D <= kTmemCols, "tensor memory columns");
+  static_assert(kNU >= 2, "shared memory holds fewer than two load units");
+  static_assert(kOCol + D + (kQSmem ? 0 : D / 2) <= kTmemCols, "tensor memory columns");
 };
 
 struct Bars {
   uint64_t q_full;
-  uint64_t kv_full[kMaxSlots], kv_empty[kMaxSlots];
+  uint64_t u_full[kMaxUnits], u_empty[kMaxUnits];
   uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t t_full[2], t_empty[2];
   uint64_t drain;
@@ -108,10 +120,10 @@ struct PrefillParams {
   __nv_bfloat16* y;
   const __nv_bfloat16* q;
   const int64_t* nonpad;
-  const uint64_t* colmask;  // bias / extra-term modes: per (b, query tile, key tile) live columns
+  const uint64_t* colmask;  // bias / extra-term modes: per (b, query tile, 64-key tile) live columns
   BiasSpec spec;
   float scale_log2;  // scale * log2(e)
-  int B, Hq, Hkv, S_q, max_seq, n_pt, n_tiles;
+  int B, Hq, Hkv, S_q, max_seq, n_pt, n_tiles;  // n_tiles: 64-key words per colmask row
   int32_t* status;
 };
 
@@ -119,6 +131,25 @@ struct PrefillParams {
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
   for (uint32_t i = 0; i < kWaitPolls; ++i) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((i & 127u) == 127u && *abort) return false;
+  }
+  *abort = 1;
+  return false;
+}
+
+// Bounded wait for up to three barrier phases at once: the polls are issued
+// back to back so their shared-memory round trips overlap (n = 1 .. 3).
+__device__ __forceinline__ bool wait3_or_abort(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1, uint64_t* b2,
+                                               uint32_t p2, int n, volatile int* abort) {
+  bool d0 = false, d1 = n < 2, d2 = n < 3;
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    const bool r0 = d0 || ptx::mbar_try_wait(b0, p0);
+    const bool r1 = d1 || ptx::mbar_try_wait(b1, p1);
+    const bool r2 = d2 || ptx::mbar_try_wait(b2, p2);
+    d0 = r0;
+    d1 = r1;
+    d2 = r2;
+    if (d0 && d1 && d2) return true;
     if ((i & 127u) == 127u && *abort) return false;
   }
   *abort = 1;
@@ -135,8 +166,8 @@ __device__ __forceinline__ uint64_t bit_range(int lo, int hi) {
   return upto_hi & ~below_lo;
 }
 
-// Position of load `idx` in the producer's order K_0, K_1, V_0, K_2, V_1, ...,
-// K_{T-1}, V_{T-2}, V_{T-1}.
+// Tile-level load order K_0, K_1, V_0, K_2, V_1, ..., K_{T-1}, V_{T-2}, V_{T-1}:
+// the position of K_j and V_j in it.
 __device__ __forceinline__ int k_index(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int v_index(int j, int T) { return j == T - 1 ? 2 * T - 1 : 2 * j + 2; }
 
@@ -146,13 +177,15 @@ __device__ __forceinline__ int v_index(int j, int T) { return j == T - 1 ? 2 * T
 // pt of batch b may attend key 64 t + k: key < nonpad[b] and term > lowest,
 // and, for the fused specification's extra term, key inside the row's
 // allowed intervals.  Keys outside the allowed intervals are never read.
-// One block per (512-key chunk, query tile, batch); shared by all heads.
+// One block per (256-key chunk, query tile, batch), shared by all heads; each
+// lane owns 8 keys and keeps the loads of all its rows in flight at once.
 template <bool FUSED>
 __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const __nv_bfloat16* __restrict__ term,
                                                                    const int64_t* __restrict__ nonpad,
                                                                    const BiasSpec spec,
                                                                    uint64_t* __restrict__ colmask, int S_q,
-                                                                   int max_seq, int n_pt, int n_tiles) {
+                                                                   int max_seq, int n_pt, int n_words) {
+  constexpr int kRowsPerWarp = kBM / (kPlanThreads / 32);
   const int ch = blockIdx.x, pt = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   __shared__ uint32_t words[kPlanKeys / 32];
@@ -163,82 +196,150 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const __nv_b
   const bool bad = bad_nonpad(np64, max_seq);
   const int np = bad ? 0 : static_cast<int>(np64);
   const int64_t qs = bad ? 0 : query_start(spec.q_start, b, np64, S_q);
-  const int k_begin = ch * kPlanKeys;
-  const int k_end = min(k_begin + kPlanKeys, np);
   const int q0 = pt * kBM;
   const int rows = min(kBM, S_q - q0);
   const float lowest = Elem<__nv_bfloat16>::lowest();
-  const int kl = k_begin + 16 * lane;  // this lane's 16 keys
+  const int kl = ch * kPlanKeys + 8 * lane;  // this lane's 8 keys
   uint32_t acc = 0;
-  if (kl < k_end) {
+  if (kl < np) {
+    const uint32_t valid = np - kl >= 8 ? 0xFFu : ((1u << (np - kl)) - 1);
     const uint16_t* base = reinterpret_cast<const uint16_t*>(term) +
                            (static_cast<int64_t>(b) * S_q + q0) * max_seq + kl;
-    for (int r0 = warp; r0 < rows; r0 += 32) {
-      uint32_t want[4];
-      uint4 v[4][2];
+    uint32_t want[kRowsPerWarp];
+    uint4 v[kRowsPerWarp];
 #pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        const int r = r0 + 8 * rr;
-        // keys of this lane the row may attend (16 bits)
-        uint32_t m = r < rows ? (k_end - kl >= 16 ? 0xFFFFu : ((1u << (k_end - kl)) - 1)) : 0u;
-        if (FUSED && m) {
-          const RowWindow w = row_window(spec, b, qs + q0 + r, np);
-          uint32_t a = 0;
-          if (w.band_lo < w.band_hi) {
-            const int64_t lo = w.band_lo - kl, hi = w.band_hi - kl;
-            const int l = lo < 0 ? 0 : (lo > 16 ? 16 : static_cast<int>(lo));
-            const int h = hi < 0 ? 0 : (hi > 16 ? 16 : static_cast<int>(hi));
-            if (l < h) a |= ((h >= 16 ? 0xFFFFu : ((1u << h) - 1)) & ~((1u << l) - 1));
-          }
-          if (w.span_lo < w.span_hi) {
-            const int64_t lo = w.span_lo - kl, hi = w.span_hi - kl;
-            const int l = lo < 0 ? 0 : (lo > 16 ? 16 : static_cast<int>(lo));
-            const int h = hi < 0 ? 0 : (hi > 16 ? 16 : static_cast<int>(hi));
-            if (l < h) a |= ((h >= 16 ? 0xFFFFu : ((1u << h) - 1)) & ~((1u << l) - 1));
-          }
-          m &= a;
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+      const int r = warp + (kPlanThreads / 32) * i;
+      uint32_t m = r < rows ? valid : 0u;
+      if (FUSED && m) {
+        const RowWindow w = row_window(spec, b, qs + q0 + r, np);
+        uint32_t a = 0;
+        if (w.band_lo < w.band_hi) {
+          const int64_t lo = w.band_lo - kl, hi = w.band_hi - kl;
+          const int l = lo < 0 ? 0 : (lo > 8 ? 8 : static_cast<int>(lo));
+          const int h = hi < 0 ? 0 : (hi > 8 ? 8 : static_cast<int>(hi));
+          if (l < h) a |= ((1u << h) - 1) & ~((1u << l) - 1);
         }
-        want[rr] = m;
-        const uint16_t* src = base + static_cast<int64_t>(r) * max_seq;
-        const uint4 none = make_uint4(0xFF7FFF7Fu, 0xFF7FFF7Fu, 0xFF7FFF7Fu, 0xFF7FFF7Fu);
-        // the second vector exists whenever one of its keys is below nonpad (max_seq % 8 == 0)
-        v[rr][0] = (m & 0xFFu) ? *reinterpret_cast<const uint4*>(src) : none;
-        v[rr][1] = (m & 0xFF00u) ? *reinterpret_cast<const uint4*>(src + 8) : none;
+        if (w.span_lo < w.span_hi) {
+          const int64_t lo = w.span_lo - kl, hi = w.span_hi - kl;
+          const int l = lo < 0 ? 0 : (lo > 8 ? 8 : static_cast<int>(lo));
+          const int h = hi < 0 ? 0 : (hi > 8 ? 8 : static_cast<int>(hi));
+          if (l < h) a |= ((1u << h) - 1) & ~((1u << l) - 1);
+        }
+        m &= a;
       }
+      want[i] = m;
+      // in bounds whenever some key of the vector is below nonpad (max_seq % 8 == 0)
+      v[i] = make_uint4(0, 0, 0, 0);
+      if (m) {
+        const uint16_t* src = base + static_cast<int64_t>(r) * max_seq;
+        asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v[i].x), "=r"(v[i].y), "=r"(v[i].z), "=r"(v[i].w)
+                     : "l"(src));
+      }
+    }
+    asm volatile("" ::: "memory");  // every row's load is issued before any is consumed
 #pragma unroll
-      for (int rr = 0; rr < 4; ++rr)
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+      const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint16_t* e = reinterpret_cast<const uint16_t*>(&v[rr][h]);
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            if (bf16_bits_to_float(e[q]) > lowest) acc |= (1u << (8 * h + q)) & want[rr];
-        }
+      for (int q = 0; q < 4; ++q) {
+        if (__uint_as_float(w4[q] << 16) > lowest) acc |= (1u << (2 * q)) & want[i];
+        if (__uint_as_float(w4[q] & 0xFFFF0000u) > lowest) acc |= (2u << (2 * q)) & want[i];
+      }
     }
   }
-  if (acc) atomicOr(&words[lane >> 1], acc << (16 * (lane & 1)));
+  // lanes 4i .. 4i+3 share word i (32 keys)
+  if (acc) atomicOr(&words[lane >> 2], acc << (8 * (lane & 3)));
   __syncthreads();
   if (tid < kPlanKeys / 64) {
     const int t = ch * (kPlanKeys / 64) + tid;
-    if (t < n_tiles)
-      colmask[(static_cast<int64_t>(b) * n_pt + pt) * n_tiles + t] =
+    if (t < n_words)
+      colmask[(static_cast<int64_t>(b) * n_pt + pt) * n_words + t] =
+          static_cast<uint64_t>(words[2 * tid]) | (static_cast<uint64_t>(words[2 * tid + 1]) << 32);
+  }
+}
+
+// The same table for a materialised bias: each block stages its 128 x 256
+// bias block in shared memory with one bulk copy per row (all in flight at
+// once), then every thread ORs 16 rows of its 8 keys.
+constexpr int kPlanSmem = kBM * kPlanKeys * 2 + 64;
+
+__global__ void __launch_bounds__(kPlanThreads) prefill_plan_bias_kernel(const __nv_bfloat16* __restrict__ bias,
+                                                                        const int64_t* __restrict__ nonpad,
+                                                                        uint64_t* __restrict__ colmask, int S_q,
+                                                                        int max_seq, int n_pt, int n_words,
+                                                                        int32_t* status) {
+  extern __shared__ __align__(128) uint8_t plan_smem[];
+  uint16_t* rows_s = reinterpret_cast<uint16_t*>(plan_smem);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(plan_smem + kBM * kPlanKeys * 2);
+  __shared__ uint32_t words[kPlanKeys / 32];
+  const int ch = blockIdx.x, pt = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  ptx::grid_launch_dependents();  // the attention kernel may start its prologue
+  const int64_t np64 = nonpad[b];
+  const int np = bad_nonpad(np64, max_seq) ? 0 : static_cast<int>(np64);
+  const int k_begin = ch * kPlanKeys;
+  const int keys = min(kPlanKeys, np - k_begin);  // <= 0: nothing live in this chunk
+  const int q0 = pt * kBM;
+  const int rows = min(kBM, S_q - q0);
+  if (tid < kPlanKeys / 32) words[tid] = 0;
+  if (tid == 0) {
+    ptx::mbar_init(bar, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  bool ok = true;
+  if (keys > 0) {
+    // whole 16-byte pieces: max_seq % 8 == 0 keeps the rounded row inside the tensor
+    const uint32_t row_bytes = static_cast<uint32_t>((keys + 7) / 8) * 16;
+    if (tid == 0) {
+      ptx::mbar_arrive_expect_tx(bar, row_bytes * rows);
+      const __nv_bfloat16* src = bias + (static_cast<int64_t>(b) * S_q + q0) * max_seq + k_begin;
+      for (int r = 0; r < rows; ++r)
+        ptx::bulk_load(rows_s + r * kPlanKeys, src + static_cast<int64_t>(r) * max_seq, row_bytes, bar);
+    }
+    ok = ptx::mbar_wait_bounded(bar, 0, kWaitPolls);
+    if (!ok && tid == 0) report(status, EXTKV_DEV_TIMEOUT);
+    const int kl = 8 * lane;  // this thread's 8 keys of the chunk
+    const uint32_t valid = keys - kl >= 8 ? 0xFFu : (keys - kl > 0 ? ((1u << (keys - kl)) - 1) : 0u);
+    const float lowest = Elem<__nv_bfloat16>::lowest();
+    uint32_t acc = 0;
+    if (ok && valid) {
+      for (int r = warp; r < rows; r += kPlanThreads / 32) {
+        const uint4 v = *reinterpret_cast<const uint4*>(rows_s + r * kPlanKeys + kl);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (__uint_as_float(w4[q] << 16) > lowest) acc |= 1u << (2 * q);
+          if (__uint_as_float(w4[q] & 0xFFFF0000u) > lowest) acc |= 2u << (2 * q);
+        }
+      }
+      acc &= valid;
+    }
+    if (acc) atomicOr(&words[lane >> 2], acc << (8 * (lane & 3)));
+  }
+  __syncthreads();
+  if (tid < kPlanKeys / 64) {
+    const int t = ch * (kPlanKeys / 64) + tid;
+    if (t < n_words)
+      colmask[(static_cast<int64_t>(b) * n_pt + pt) * n_words + t] =
           static_cast<uint64_t>(words[2 * tid]) | (static_cast<uint64_t>(words[2 * tid + 1]) << 32);
   }
 }
 
 // ---- softmax helpers ------------------------------------------------------------------
 
-// Scores of one 64-key tile in base 2: t = scale*log2(e)*s (+ log2(e)*term),
-// -inf where the key is masked: outside the row's allowed keys (PARTIAL
-// tiles only; `allowed` bit c) or, with a term, term <= lowest.
-template <bool TERM, bool PARTIAL>
-__device__ __forceinline__ void tile_scores(float (&t)[kBN], const uint32_t (&sa)[32], const uint32_t (&sb)[32],
-                                            const uint32_t (&tw)[32], uint64_t allowed, float sl2,
-                                            float lowest) {
+// Scores of 64 keys (half H of a tile) in base 2: t = scale*log2(e)*s
+// (+ log2(e)*term), -inf where the key is masked: outside the row's allowed
+// keys (PARTIAL halves only; `allowed` bit c) or, with a term, term <= lowest.
+template <int H, bool TERM, bool PARTIAL>
+__device__ __forceinline__ void half_scores(float (&t)[kBN], const uint32_t (&sa)[32], const uint32_t (&sb)[32],
+                                            const uint32_t (&tw)[32], uint64_t allowed, float sl2, float lowest) {
   const uint64_t sl2x2 = ptx::f2(sl2, sl2);
   const uint64_t l2e = ptx::f2(kLog2e, kLog2e);
 #pragma unroll
-  for (int c = 0; c < kBN / 2; ++c) {
+  for (int c = 0; c < 32; ++c) {
     const uint32_t s0 = c < 16 ? sa[2 * c] : sb[2 * c - 32];
     const uint32_t s1 = c < 16 ? sa[2 * c + 1] : sb[2 * c - 31];
     const uint64_t sv = ptx::f2(__uint_as_float(s0), __uint_as_float(s1));
@@ -256,8 +357,8 @@ __device__ __forceinline__ void tile_scores(float (&t)[kBN], const uint32_t (&sa
       ok0 = ok0 && ((allowed >> (2 * c)) & 1);
       ok1 = ok1 && ((allowed >> (2 * c + 1)) & 1);
     }
-    t[2 * c] = ok0 ? ptx::f2_lo(v) : -INFINITY;
-    t[2 * c + 1] = ok1 ? ptx::f2_hi(v) : -INFINITY;
+    t[64 * H + 2 * c] = ok0 ? ptx::f2_lo(v) : -INFINITY;
+    t[64 * H + 2 * c + 1] = ok1 ? ptx::f2_hi(v) : -INFINITY;
   }
 }
 
@@ -265,24 +366,41 @@ __device__ __forceinline__ float tile_max(const float (&t)[kBN]) {
   float acc[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
+    // the 16 values t[k + 8m], m = 0 .. 15
     acc[k] = ptx::max3(t[k], t[k + 8], t[k + 16]);
-    acc[k] = ptx::max3(acc[k], t[k + 24], t[k + 32]);
-    acc[k] = ptx::max3(acc[k], t[k + 40], t[k + 48]);
-    acc[k] = fmaxf(acc[k], t[k + 56]);
+#pragma unroll
+    for (int m = 3; m + 1 < kBN / 8; m += 2) acc[k] = ptx::max3(acc[k], t[k + 8 * m], t[k + 8 * m + 8]);
+    acc[k] = fmaxf(acc[k], t[k + kBN - 8]);
   }
+  static_assert(kBN == 128, "tile_max covers 16 values per accumulator");
   return ptx::max3(ptx::max3(acc[0], acc[1], acc[2]), ptx::max3(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7]));
+}
+
+// The 128-byte row `row` of a 64-key block stored with the 128-byte swizzle.
+__device__ __forceinline__ void load_swizzled_row(uint32_t (&w)[32], const uint8_t* blk, int row) {
+  const uint8_t* r = blk + row * 128;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const uint4 v = *reinterpret_cast<const uint4*>(r + ((u ^ (row & 7)) << 4));
+    w[4 * u] = v.x;
+    w[4 * u + 1] = v.y;
+    w[4 * u + 2] = v.z;
+    w[4 * u + 3] = v.w;
+  }
 }
 
 // ---- the attention kernel ---------------------------------------------------------
 
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                        const __grid_constant__ CUtensorMap tmap, const PrefillParams p) {
+    attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap tmap,
+                        const PrefillParams p) {
   using C = Cfg<D, MODE>;
   constexpr bool kFusedMode = MODE == kFused || MODE == kFusedExtra;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = sm + C::kOffQ;
   uint8_t* sKV = sm + C::kOffKV;
   uint8_t* sT = sm + C::kOffT;
   Bars& bar = *reinterpret_cast<Bars*>(sm + C::kOffBar);
@@ -295,10 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = pt * kBM;
 
   if (tid == 0) {
-    ptx::mbar_init(&bar.q_full, 4 * 32);
-    for (int s = 0; s < C::kNS; ++s) {
-      ptx::mbar_init(&bar.kv_full[s], 1);
-      ptx::mbar_init(&bar.kv_empty[s], 1);
+    ptx::mbar_init(&bar.q_full, C::kQSmem ? 1 : 4 * 32);
+    for (int s = 0; s < C::kNU; ++s) {
+      ptx::mbar_init(&bar.u_full[s], 1);
+      ptx::mbar_init(&bar.u_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&bar.s_full[s], 1);
@@ -314,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
+    if (C::kQSmem) ptx::prefetch_tensormap(&qmap);
     ptx::prefetch_tensormap(&kmap);
     ptx::prefetch_tensormap(&vmap);
     if (C::kTerm) ptx::prefetch_tensormap(&tmap);
@@ -326,6 +445,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   ptx::grid_dependency_wait();  // the preceding kernels' writes (cache, bias, plan) are visible
+
+  // a shared-memory Q tile is needed whenever any key is live: start it first
+  if (C::kQSmem && warp == 0 && lane == 0) {
+    ptx::mbar_arrive_expect_tx(&bar.q_full, C::kQBytes);
+    ptx::tma_load_3d(sQ, &qmap, &bar.q_full, 0, (b * p.Hq + h) * p.S_q + q0, 0);
+  }
 
   const int64_t np64 = p.nonpad[b];
   const bool bad = bad_nonpad(np64, p.max_seq);
@@ -369,9 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bar.range_hi = np;
     }
   } else if (C::kTerm && warp == 1) {
-    // first and last tile with a live key in the plan's column masks
+    // first and last 64-key block with a live key in the plan's column masks
     int lo = INT_MAX, hi = 0;
-    const int lim = (np + kBN - 1) / kBN;
+    const int lim = (np + 63) / 64;
     for (int t = lane; t < lim; t += 32)
       if (cmrow[t]) {
         lo = min(lo, t);
@@ -383,8 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
     }
     if (lane == 0 && lo < hi) {
-      bar.range_lo = lo * kBN;
-      bar.range_hi = hi * kBN;
+      bar.range_lo = lo * 64;
+      bar.range_hi = min(hi * 64, np);
     }
   }
   __syncthreads();
@@ -398,71 +523,141 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const int unit = b * p.Hkv + hk;
       int issued = 0, t_issued = 0;
-      for (int idx = 0; idx < 2 * T; ++idx) {
+      bool ok = true;
+      auto load_term = [&](int j) -> bool {
+        const int tb = j % C::kTB;
+        if (j >= C::kTB && !wait_or_abort(&bar.t_empty[tb], ((j / C::kTB) - 1) & 1, abort)) return false;
+        uint8_t* dst = sT + tb * C::kTermBytes;
+        ptx::mbar_arrive_expect_tx(&bar.t_full[tb], C::kTermBytes);
+        ptx::tma_load_2d(dst, &tmap, &bar.t_full[tb], (t_lo + j) * kBN, b * p.S_q + q0);
+        ptx::tma_load_2d(dst + C::kTermBytes / 2, &tmap, &bar.t_full[tb], (t_lo + j) * kBN + 64, b * p.S_q + q0);
+        ++t_issued;
+        return true;
+      };
+      for (int idx = 0; idx < 2 * T && ok; ++idx) {
         const bool is_v = idx == 2 * T - 1 ? true : (idx == 0 ? false : (idx & 1) == 0);
         const int j = idx == 2 * T - 1 ? T - 1 : (is_v ? idx / 2 - 1 : (idx + 1) / 2);
-        const int slot = idx % C::kNS;
-        if (idx >= C::kNS && !wait_or_abort(&bar.kv_empty[slot], ((idx / C::kNS) - 1) & 1, abort)) break;
         const int key0 = (t_lo + j) * kBN;
-        ptx::mbar_arrive_expect_tx(&bar.kv_full[slot], C::kSlotBytes);
-        ptx::tma_load_4d(sKV + slot * C::kSlotBytes, is_v ? &vmap : &kmap, &bar.kv_full[slot], 0, key0, 0, unit);
-        ++issued;
-        if (C::kTerm && !is_v) {
-          const int ts = j & 1;
-          if (j >= 2 && !wait_or_abort(&bar.t_empty[ts], ((j >> 1) - 1) & 1, abort)) break;
-          ptx::mbar_arrive_expect_tx(&bar.t_full[ts], C::kTermBytes);
-          ptx::tma_load_2d(sT + ts * C::kTermBytes, &tmap, &bar.t_full[ts], key0, b * p.S_q + q0);
-          ++t_issued;
+        for (int part = 0; part < C::kParts; ++part) {
+          const int u = idx * C::kParts + part, slot = u % C::kNU;
+          if (u >= C::kNU && !wait_or_abort(&bar.u_empty[slot], ((u / C::kNU) - 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&bar.u_full[slot], C::kUnitBytes);
+          uint8_t* dst = sKV + slot * C::kUnitBytes;
+          if (is_v)
+            ptx::tma_load_4d(dst, &vmap, &bar.u_full[slot], 0, key0 + part * C::kVKeys, 0, unit);
+          else
+            ptx::tma_load_4d(dst, &kmap, &bar.u_full[slot], 0, key0, part * C::kKChunks, unit);
+          ++issued;
+        }
+        // the term block of tile j goes out once V_{j-1} (or, for tile 0, K_0) is on its way
+        if (ok && C::kTerm) {
+          if (idx == 0) ok = load_term(0);
+          else if (is_v && j + 1 < T) ok = load_term(j + 1);
         }
       }
       // copies still in flight after an abort land before the CTA leaves
       if (*abort) {
-        for (int idx = issued > C::kNS ? issued - C::kNS : 0; idx < issued; ++idx)
-          ptx::mbar_wait_bounded(&bar.kv_full[idx % C::kNS], (idx / C::kNS) & 1, kWaitPolls);
-        for (int j = t_issued > 2 ? t_issued - 2 : 0; j < t_issued; ++j)
-          ptx::mbar_wait_bounded(&bar.t_full[j & 1], (j >> 1) & 1, kWaitPolls);
+        if (C::kQSmem) ptx::mbar_wait_bounded(&bar.q_full, 0, kWaitPolls);
+        for (int u = issued > C::kNU ? issued - C::kNU : 0; u < issued; ++u)
+          ptx::mbar_wait_bounded(&bar.u_full[u % C::kNU], (u / C::kNU) & 1, kWaitPolls);
+        if (C::kTerm)
+          for (int j = t_issued > C::kTB ? t_issued - C::kTB : 0; j < t_issued; ++j)
+            ptx::mbar_wait_bounded(&bar.t_full[j % C::kTB], (j / C::kTB) & 1, kWaitPolls);
+      } else if (C::kQSmem && T == 0) {
+        ptx::mbar_wait_bounded(&bar.q_full, 0, kWaitPolls);  // no consumer: let it land
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0 && T > 0) {
-      const uint32_t kv_addr = ptx::smem_u32(sKV);
-      auto issue_qk = [&](int j) -> bool {
-        const int idx = k_index(j), slot = idx % C::kNS;
-        if (!wait_or_abort(&bar.kv_full[slot], (idx / C::kNS) & 1, abort)) return false;
-        ptx::tc_fence_after();
+      const uint32_t kv_addr = ptx::smem_u32(sKV), q_addr = ptx::smem_u32(sQ);
+      // Shared-memory descriptors are built once and advanced by adding the
+      // byte offset >> 4 to the start-address field (every operand lies in
+      // the first 256 KB of shared memory, so the 14-bit field never carries).
+      const uint64_t kdesc0 = ptx::smem_desc_sw128(kv_addr, 16, 1024);
+      const uint64_t vdesc0 = ptx::smem_desc_sw128(kv_addr, C::kVKeys * 128, 1024);
+      const uint64_t qdesc0 = ptx::smem_desc_sw128(q_addr, 16, 1024);
+      // Readiness tests of the next batch: the issuing thread blocks while the
+      // tensor pipe's queue is full, so one test placed a few MMAs before the
+      // end of the current batch overlaps its shared-memory round trip with
+      // queued tensor work; the blocking wait remains for what is not there.
+      auto k_ready = [&](int j) -> bool {
+        const int u0 = k_index(j) * C::kParts;
+        bool r = ptx::mbar_test_wait(&bar.u_full[u0 % C::kNU], (u0 / C::kNU) & 1);
+        if (C::kParts > 1) r = ptx::mbar_test_wait(&bar.u_full[(u0 + 1) % C::kNU], ((u0 + 1) / C::kNU) & 1) && r;
+        return r;
+      };
+      auto pv_ready = [&](int j) -> bool {
+        const int u0 = v_index(j, T) * C::kParts;
+        bool r = ptx::mbar_test_wait(&bar.p_full[j & 1], (j >> 1) & 1);
+        r = ptx::mbar_test_wait(&bar.u_full[u0 % C::kNU], (u0 / C::kNU) & 1) && r;
+        if (C::kParts > 1) r = ptx::mbar_test_wait(&bar.u_full[(u0 + 1) % C::kNU], ((u0 + 1) / C::kNU) & 1) && r;
+        return r;
+      };
+      bool k_known = false, pv_known = false;
+      // Q K_j^T into S_{j & 1}; both units of K_j are polled together; tests
+      // P_pj / V_pj on the way when pj >= 0
+      auto issue_qk = [&](int j, int pj) -> bool {
         const uint32_t d = tbase + (j & 1) * kBN;
-        const uint32_t kb = kv_addr + slot * C::kSlotBytes;
+        const int u0 = k_index(j) * C::kParts, s0 = u0 % C::kNU, s1 = (u0 + 1) % C::kNU;
+        if (!k_known && !wait3_or_abort(&bar.u_full[s0], (u0 / C::kNU) & 1, &bar.u_full[s1],
+                                        ((u0 + 1) / C::kNU) & 1, &bar.u_full[s0], 0, C::kParts, abort))
+          return false;
+        k_known = false;
+        ptx::tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t bd = ptx::smem_desc_sw128(kb + (kk >> 2) * (kBN * 128) + (kk & 3) * 32, 16, 1024);
-          ptx::umma_bf16_ts(d, tbase + C::kQCol + kk * 8, bd, C::kIdescQK, kk > 0);
+        for (int part = 0; part < C::kParts; ++part) {
+          const int slot = (u0 + part) % C::kNU;
+          const uint64_t kd = kdesc0 + ((slot * C::kUnitBytes) >> 4);
+#pragma unroll
+          for (int k = 0; k < D / 16 / C::kParts; ++k) {
+            const int kk = part * (D / 16 / C::kParts) + k;  // K step over the head dim
+            const uint64_t bd = kd + (((k >> 2) * (kBN * 128) + (k & 3) * 32) >> 4);
+            if (C::kQSmem) {
+              const uint64_t ad = qdesc0 + (((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
+              ptx::umma_bf16(d, ad, bd, C::kIdescQK, kk > 0);
+            } else {
+              ptx::umma_bf16_ts(d, tbase + C::kQCol + kk * 8, bd, C::kIdescQK, kk > 0);
+            }
+            if (pj >= 0 && kk == D / 16 - 4) pv_known = pv_ready(pj);
+          }
+          ptx::umma_commit(&bar.u_empty[slot]);
         }
         ptx::umma_commit(&bar.s_full[j & 1]);
-        ptx::umma_commit(&bar.kv_empty[slot]);
         return true;
       };
       bool ok = wait_or_abort(&bar.q_full, 0, abort);
       if (ok) {
         ptx::tc_fence_after();
-        ok = issue_qk(0);
+        ok = issue_qk(0, -1);
       }
       for (int j = 0; j < T && ok; ++j) {
-        if (j + 1 < T && !(ok = issue_qk(j + 1))) break;
-        if (!(ok = wait_or_abort(&bar.p_full[j & 1], (j >> 1) & 1, abort))) break;
+        pv_known = false;
+        if (j + 1 < T && !(ok = issue_qk(j + 1, j))) break;
+        // P_j and both units of V_j, polled together
+        const int u0 = v_index(j, T) * C::kParts, s0 = u0 % C::kNU, s1 = (u0 + 1) % C::kNU;
+        if (!pv_known && !(ok = wait3_or_abort(&bar.p_full[j & 1], (j >> 1) & 1, &bar.u_full[s0],
+                                               (u0 / C::kNU) & 1, &bar.u_full[s1], ((u0 + 1) / C::kNU) & 1,
+                                               1 + C::kParts, abort)))
+          break;
         ptx::tc_fence_after();
-        const int idx = v_index(j, T), slot = idx % C::kNS;
-        if (!(ok = wait_or_abort(&bar.kv_full[slot], (idx / C::kNS) & 1, abort))) break;
-        ptx::tc_fence_after();
-        const uint32_t vb = kv_addr + slot * C::kSlotBytes;
 #pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint64_t bd = ptx::smem_desc_sw128(vb + ks * 2048, kBN * 128, 1024);
-          ptx::umma_bf16_ts(tbase + C::kOCol, tbase + (j & 1) * kBN + ks * 8, bd, C::kIdescPV,
-                            (j > 0 || ks > 0) ? 1u : 0u);
+        for (int part = 0; part < C::kParts; ++part) {
+          const int slot = (u0 + part) % C::kNU;
+          const uint64_t vd = vdesc0 + ((slot * C::kUnitBytes) >> 4);
+#pragma unroll
+          for (int k = 0; k < kBN / 16 / C::kParts; ++k) {
+            const int ks = part * (kBN / 16 / C::kParts) + k;  // K step over the keys
+            ptx::umma_bf16_ts(tbase + C::kOCol, tbase + (j & 1) * kBN + ks * 8, vd + ((k * 2048) >> 4),
+                              C::kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
+            if (j + 2 < T && ks == kBN / 16 - 3) k_known = k_ready(j + 2);
+          }
+          ptx::umma_commit(&bar.u_empty[slot]);
         }
         ptx::umma_commit(&bar.pv_done[j & 1]);
-        ptx::umma_commit(&bar.kv_empty[slot]);
       }
       // every MMA issued has completed before tensor memory is released
       ptx::umma_commit(&bar.drain);
@@ -475,9 +670,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float lowest = Elem<__nv_bfloat16>::lowest();
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    if (T > 0) {
+    if (!C::kQSmem && T > 0) {
       // this row of Q into tensor memory (rows past the chunk: zeros)
-      const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((static_cast<int64_t>(b) * p.Hq + h) * p.S_q + q0 + row) * D);
+      const uint4* qrow =
+          reinterpret_cast<const uint4*>(p.q + ((static_cast<int64_t>(b) * p.Hq + h) * p.S_q + q0 + row) * D);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         uint32_t r[32];
@@ -498,42 +694,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < T; ++j) {
       const int tile = t_lo + j, key0 = tile * kBN;
       // keys of the tile no row of the CTA attends (their V rows are zeroed)
-      const uint64_t dead = C::kTerm ? ~cmrow[tile] : ~bit_range(rlo - key0, rhi - key0);
+      uint64_t dead0, dead1;
+      if (C::kTerm) {
+        dead0 = ~cmrow[2 * tile];
+        dead1 = 2 * tile + 1 < p.n_tiles ? ~cmrow[2 * tile + 1] : ~0ull;
+      } else {
+        dead0 = ~bit_range(rlo - key0, rhi - key0);
+        dead1 = ~bit_range(rlo - key0 - 64, rhi - key0 - 64);
+      }
       // this row's allowed keys before the term test
-      const uint64_t allowed = kFusedMode ? (bit_range(a1 - key0, b1 - key0) | bit_range(a2 - key0, b2 - key0))
-                                          : bit_range(-key0, np - key0);
-      const bool partial = !__all_sync(0xffffffffu, allowed == ~0ull);
+      uint64_t al0, al1;
+      if (kFusedMode) {
+        al0 = bit_range(a1 - key0, b1 - key0) | bit_range(a2 - key0, b2 - key0);
+        al1 = bit_range(a1 - key0 - 64, b1 - key0 - 64) | bit_range(a2 - key0 - 64, b2 - key0 - 64);
+      } else {
+        al0 = bit_range(-key0, np - key0);
+        al1 = bit_range(-key0 - 64, np - key0 - 64);
+      }
+      const bool part0 = !__all_sync(0xffffffffu, al0 == ~0ull);
+      const bool part1 = !__all_sync(0xffffffffu, al1 == ~0ull);
       if (!__all_sync(0xffffffffu, wait_or_abort(&bar.s_full[j & 1], (j >> 1) & 1, abort))) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
-      uint32_t sa[32], sb[32], tw[32];
-      ptx::tmem_ld32(tl + (j & 1) * kBN, sa);
-      ptx::tmem_ld32(tl + (j & 1) * kBN + 32, sb);
-      if (C::kTerm) {
-        if (!__all_sync(0xffffffffu, wait_or_abort(&bar.t_full[j & 1], (j >> 1) & 1, abort))) {
+      const uint32_t ts = tl + (j & 1) * kBN;
+      float t[kBN];
+      {
+        const int tb = j % C::kTB;
+        const uint8_t* tblk = sT + tb * C::kTermBytes;
+        if (C::kTerm &&
+            !__all_sync(0xffffffffu, wait_or_abort(&bar.t_full[tb], (j / C::kTB) & 1, abort))) {
           ok = false;
           break;
         }
-        const uint8_t* trow = sT + (j & 1) * C::kTermBytes + row * 128;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 v = *reinterpret_cast<const uint4*>(trow + ((u ^ (row & 7)) << 4));
-          tw[4 * u] = v.x;
-          tw[4 * u + 1] = v.y;
-          tw[4 * u + 2] = v.z;
-          tw[4 * u + 3] = v.w;
+        uint32_t sa[32], sb[32], tw[32];
+        ptx::tmem_ld32(ts, sa);
+        ptx::tmem_ld32(ts + 32, sb);
+        if (C::kTerm) load_swizzled_row(tw, tblk, row);
+        ptx::tmem_wait_ld();
+        if (part0)
+          half_scores<0, C::kTerm, true>(t, sa, sb, tw, al0, sl2, lowest);
+        else
+          half_scores<0, C::kTerm, false>(t, sa, sb, tw, al0, sl2, lowest);
+        ptx::tmem_ld32(ts + 64, sa);
+        ptx::tmem_ld32(ts + 96, sb);
+        if (C::kTerm) {
+          load_swizzled_row(tw, tblk + C::kTermBytes / 2, row);
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&bar.t_empty[tb]);
         }
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&bar.t_empty[j & 1]);
+        ptx::tmem_wait_ld();
+        if (part1)
+          half_scores<1, C::kTerm, true>(t, sa, sb, tw, al1, sl2, lowest);
+        else
+          half_scores<1, C::kTerm, false>(t, sa, sb, tw, al1, sl2, lowest);
       }
-      ptx::tmem_wait_ld();
-      float t[kBN];
-      if (partial)
-        tile_scores<C::kTerm, true>(t, sa, sb, tw, allowed, sl2, lowest);
-      else
-        tile_scores<C::kTerm, false>(t, sa, sb, tw, allowed, sl2, lowest);
       const float mt = tile_max(t);
       // lazy rescale: only when the running maximum grows by more than 2^8
       const float m_new = fmaxf(m_run, mt);
@@ -565,36 +781,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_use = m_run == -INFINITY ? 0.f : m_run;
       const uint64_t nm = ptx::f2(-m_use, -m_use);
       uint64_t ls[4] = {0, 0, 0, 0};
-      uint32_t pk[kBN / 2];
 #pragma unroll
-      for (int c = 0; c < kBN / 2; ++c) {
-        const uint64_t d = ptx::add2(ptx::f2(t[2 * c], t[2 * c + 1]), nm);
-        const float e0 = ptx::ex2(ptx::f2_lo(d)), e1 = ptx::ex2(ptx::f2_hi(d));
-        ls[c & 3] = ptx::add2(ls[c & 3], ptx::f2(e0, e1));
-        pk[c] = ptx::pack_bf16x2(e0, e1);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const uint64_t d = ptx::add2(ptx::f2(t[64 * hh + 2 * c], t[64 * hh + 2 * c + 1]), nm);
+          const float e0 = ptx::ex2(ptx::f2_lo(d)), e1 = ptx::ex2(ptx::f2_hi(d));
+          ls[c & 3] = ptx::add2(ls[c & 3], ptx::f2(e0, e1));
+          pk[c] = ptx::pack_bf16x2(e0, e1);
+        }
+        // P_j over the first half of S_j: QK_{j+2}, the next writer of this
+        // buffer, is issued after P_j V_j and the tensor pipe runs in order
+        ptx::tmem_st32(ts + 32 * hh, pk);
       }
-      const uint64_t l01 = ptx::add2(ls[0], ls[1]), l23 = ptx::add2(ls[2], ls[3]);
-      const uint64_t lsum = ptx::add2(l01, l23);
+      const uint64_t lsum = ptx::add2(ptx::add2(ls[0], ls[1]), ptx::add2(ls[2], ls[3]));
       l_run += ptx::f2_lo(lsum) + ptx::f2_hi(lsum);
-      // P_j over the first half of S_j: QK_{j+2}, the next writer of this
-      // buffer, is issued after P_j V_j and the tensor pipe runs in order
-      ptx::tmem_st32(tl + (j & 1) * kBN, pk);
-      if (dead) {
-        const int idx = v_index(j, T), slot = idx % C::kNS;
-        if (!__all_sync(0xffffffffu, wait_or_abort(&bar.kv_full[slot], (idx / C::kNS) & 1, abort))) {
-          ok = false;
-          break;
+      if (dead0 | dead1) {
+        // zero the V rows of dead keys once their unit has landed
+#pragma unroll
+        for (int part = 0; part < C::kParts && ok; ++part) {
+          const int u = v_index(j, T) * C::kParts + part, slot = u % C::kNU;
+          if (!__all_sync(0xffffffffu, wait_or_abort(&bar.u_full[slot], (u / C::kNU) & 1, abort))) {
+            ok = false;
+            break;
+          }
+          uint8_t* vt = sKV + slot * C::kUnitBytes;
+          constexpr int kLines = C::kVKeys * (D / 64) * 8;  // 16-byte pieces of the unit
+          for (int w = tid - 64; w < kLines; w += 128) {
+            const int kl = w / ((D / 64) * 8), rem = w % ((D / 64) * 8);
+            const int key = part * C::kVKeys + kl;
+            const uint64_t dm = key < 64 ? dead0 : dead1;
+            if ((dm >> (key & 63)) & 1)
+              *reinterpret_cast<uint4*>(vt + (rem >> 3) * (C::kVKeys * 128) + kl * 128 + (rem & 7) * 16) =
+                  make_uint4(0, 0, 0, 0);
+          }
         }
-        uint8_t* vt = sKV + slot * C::kSlotBytes;
-        for (int w = tid - 64; w < kBN * (D / 64) * 8; w += 128) {
-          const int key = w / ((D / 64) * 8), rem = w % ((D / 64) * 8);
-          if ((dead >> key) & 1)
-            *reinterpret_cast<uint4*>(vt + (rem >> 3) * (kBN * 128) + key * 128 + (rem & 7) * 16) =
-                make_uint4(0, 0, 0, 0);
-        }
+        if (!ok) break;
+        ptx::fence_proxy_async_smem();  // zeroed V rows visible to the tensor cores
       }
       ptx::tmem_wait_st();
-      if (dead) ptx::fence_proxy_async_smem();  // zeroed V rows visible to the tensor cores
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bar.p_full[j & 1]);
     }
@@ -641,7 +867,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int n_query_tiles(int64_t S_q) { return static_cast<int>((S_q + kBM - 1) / kBM); }
 int n_plan_chunks(int64_t max_seq) { return static_cast<int>((max_seq + kPlanKeys - 1) / kPlanKeys); }
-int n_key_tiles(int64_t max_seq) { return static_cast<int>((max_seq + kBN - 1) / kBN); }
+// the plan's column-mask table: one 64-bit word per 64 keys
+int n_mask_words(int64_t max_seq) { return static_cast<int>((max_seq + 63) / 64); }
 
 template <int D, int MODE>
 cudaError_t launch_dm(const AttnArgs& a, const char** name) {
@@ -654,20 +881,31 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
   });
   if (attr_err != cudaSuccess) return attr_err;
 
-  CUtensorMap kmap, vmap, tmap;
+  // permuted views (64 columns, key, 64-column chunk, batch x KV head): one
+  // request lands a whole unit in the 128-byte-swizzled per-chunk layout
+  CUtensorMap qmap, kmap, vmap, tmap;
   const uint64_t kv_dims[4] = {64, static_cast<uint64_t>(a.max_seq), static_cast<uint64_t>(D / 64),
                                static_cast<uint64_t>(a.B * a.Hkv)};
   const uint64_t kv_strides[3] = {static_cast<uint64_t>(D) * 2, 128, static_cast<uint64_t>(a.max_seq) * D * 2};
-  const uint32_t kv_box[4] = {64, kBN, static_cast<uint32_t>(D / 64), 1};
-  if (!make_tensor_map_bf16(&kmap, a.k_cache, 4, kv_dims, kv_strides, kv_box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tensor_map_bf16(&vmap, a.v_cache, 4, kv_dims, kv_strides, kv_box, CU_TENSOR_MAP_SWIZZLE_128B))
+  const uint32_t k_box[4] = {64, kBN, static_cast<uint32_t>(C::kKChunks), 1};
+  const uint32_t v_box[4] = {64, static_cast<uint32_t>(C::kVKeys), static_cast<uint32_t>(D / 64), 1};
+  if (!make_tensor_map_bf16(&kmap, a.k_cache, 4, kv_dims, kv_strides, k_box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tensor_map_bf16(&vmap, a.v_cache, 4, kv_dims, kv_strides, v_box, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  std::memset(&qmap, 0, sizeof qmap);
+  if (C::kQSmem) {
+    const uint64_t q_dims[3] = {64, static_cast<uint64_t>(a.B * a.Hq * a.S_q), static_cast<uint64_t>(D / 64)};
+    const uint64_t q_strides[2] = {static_cast<uint64_t>(D) * 2, 128};
+    const uint32_t q_box[3] = {64, kBM, static_cast<uint32_t>(D / 64)};
+    if (!make_tensor_map_bf16(&qmap, a.q, 3, q_dims, q_strides, q_box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   std::memset(&tmap, 0, sizeof tmap);
   const void* term = MODE == kBias ? a.bias : (MODE == kFusedExtra ? a.extra : nullptr);
   if (term) {
     const uint64_t t_dims[2] = {static_cast<uint64_t>(a.max_seq), static_cast<uint64_t>(a.B * a.S_q)};
     const uint64_t t_strides[1] = {static_cast<uint64_t>(a.max_seq) * 2};
-    const uint32_t t_box[2] = {kBN, kBM};
+    const uint32_t t_box[2] = {64, kBM};  // two requests per 128-key tile
     if (!make_tensor_map_bf16(&tmap, term, 2, t_dims, t_strides, t_box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
@@ -685,14 +923,27 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
   prm.S_q = static_cast<int>(a.S_q);
   prm.max_seq = static_cast<int>(a.max_seq);
   prm.n_pt = n_query_tiles(a.S_q);
-  prm.n_tiles = n_key_tiles(a.max_seq);
+  prm.n_tiles = n_mask_words(a.max_seq);
   prm.status = a.status;
 
-  if (C::kTerm) {
-    prefill_plan_kernel<MODE == kFusedExtra><<<dim3(n_plan_chunks(a.max_seq), prm.n_pt, prm.B), kPlanThreads, 0,
-                                                a.stream>>>(static_cast<const __nv_bfloat16*>(term), a.nonpad,
-                                                            prm.spec, static_cast<uint64_t*>(a.workspace),
-                                                            prm.S_q, prm.max_seq, prm.n_pt, prm.n_tiles);
+  if (MODE == kBias) {
+    static std::once_flag plan_once;
+    static cudaError_t plan_err = cudaSuccess;
+    std::call_once(plan_once, [] {
+      plan_err = cudaFuncSetAttribute(prefill_plan_bias_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      kPlanSmem);
+    });
+    if (plan_err != cudaSuccess) return plan_err;
+    prefill_plan_bias_kernel<<<dim3(n_plan_chunks(a.max_seq), prm.n_pt, prm.B), kPlanThreads, kPlanSmem,
+                               a.stream>>>(static_cast<const __nv_bfloat16*>(term), a.nonpad,
+                                           static_cast<uint64_t*>(a.workspace), prm.S_q, prm.max_seq,
+                                           prm.n_pt, prm.n_tiles, a.status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  } else if (MODE == kFusedExtra) {
+    prefill_plan_kernel<true><<<dim3(n_plan_chunks(a.max_seq), prm.n_pt, prm.B), kPlanThreads, 0, a.stream>>>(
+        static_cast<const __nv_bfloat16*>(term), a.nonpad, prm.spec, static_cast<uint64_t*>(a.workspace),
+        prm.S_q, prm.max_seq, prm.n_pt, prm.n_tiles);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -707,7 +958,7 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_prefill_kernel<D, MODE>, kmap, vmap, tmap, prm);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_prefill_kernel<D, MODE>, qmap, kmap, vmap, tmap, prm);
   if (e != cudaSuccess) return e;
   *name = "attn_prefill_tcgen05";
   return cudaGetLastError();
@@ -723,7 +974,7 @@ cudaError_t launch_d(const AttnArgs& a, const char** name) {
 }  // namespace
 
 size_t prefill_workspace_bytes(int64_t B, int64_t S_q, int64_t max_seq) {
-  return static_cast<size_t>(B) * n_query_tiles(S_q) * n_key_tiles(max_seq) * sizeof(uint64_t);
+  return static_cast<size_t>(B) * n_query_tiles(S_q) * n_mask_words(max_seq) * sizeof(uint64_t);
 }
 
 bool prefill_supported(const AttnArgs& a) {

@@ -115,6 +115,9 @@ int build_static_cache_bias(void* bias, const extkv_bias_spec* spec, const int64
     return fail(EXTKV_ERR_UNSUPPORTED,
                 "build_static_cache_bias: max_seq*sizeof(T) must be a multiple of 16 (max_seq=%lld)",
                 (long long)max_seq);
+  if (max_seq > 0x7fffff00)
+    return fail(EXTKV_ERR_UNSUPPORTED, "build_static_cache_bias: max_seq=%lld exceeds 2^31 - 256",
+                (long long)max_seq);
   if (!aligned(bias, 16) || (spec->extra && !aligned(spec->extra, 16)) || !aligned(status, 4))
     return fail(EXTKV_ERR_INVALID_ARG, "build_static_cache_bias: bias/extra must be 16-byte aligned");
   cudaError_t e = launch_bias(bias, *spec, nonpad, B, S_q, max_seq, dtype, status,

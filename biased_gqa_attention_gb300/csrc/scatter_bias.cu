@@ -97,48 +97,68 @@ cudaError_t launch_scatter(void* k_cache, void* v_cache, const void* k_new, cons
 // ---- static-cache bias ------------------------------------------------------
 // mobius issue #366, deliverable: the (B,1,S_q,max_seq) additive bias keyed on
 // absolute query positions (causal + sliding + block overlay + padding, valid
-// only where slot < nonpad).  Each thread writes one 16-byte vector of one
-// row; the row's two allowed intervals are recomputed per vector from the
-// position (cheap integer work next to the 16-byte store).
+// only where slot < nonpad).  One block per row (grid-stride over rows): the
+// row's allowed keys are two intervals, computed once; the block's threads
+// then stream the row's 16-byte vectors (coalesced stores; with an extra term
+// each vector is a select between it and the sentinel).
 template <typename T>
 __global__ void __launch_bounds__(256) bias_kernel(uint4* __restrict__ bias, BiasSpec spec,
                                                    const int64_t* __restrict__ nonpad, int64_t S_q,
-                                                   int64_t max_seq, int64_t row_vecs,
-                                                   int64_t total, int32_t* status) {
+                                                   int64_t max_seq, int64_t row_vecs, int64_t rows,
+                                                   int32_t* status) {
   constexpr int kVec = 16 / sizeof(T);
   using E = Elem<T>;
   ptx::grid_dependency_wait();
   ptx::grid_launch_dependents();
   const uint4* extra = static_cast<const uint4*>(spec.extra);
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += stride) {
-    const int64_t jv = idx % row_vecs;
-    const int64_t r = idx / row_vecs;  // b*S_q + i
+  union Vec {
+    uint4 u;
+    T e[kVec];
+  };
+  Vec low, zero;
+#pragma unroll
+  for (int e = 0; e < kVec; ++e) {
+    low.e[e] = E::from_float(E::lowest());
+    zero.e[e] = E::from_float(0.0f);
+  }
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {  // r = b*S_q + i
     const int64_t i = r % S_q;
     const int64_t b = r / S_q;
     const int64_t np = nonpad[b];
+    uint4* out = bias + r * row_vecs;
+    const uint4* ext = extra ? extra + r * row_vecs : nullptr;
     if (bad_nonpad(np, max_seq)) {
-      if (jv == 0 && i == 0) report(status, EXTKV_DEV_BAD_NONPAD);
+      if (i == 0 && threadIdx.x == 0) report(status, EXTKV_DEV_BAD_NONPAD);
       continue;
     }
     const int64_t p = query_start(spec.q_start, b, np, S_q) + i;
     const RowWindow w = row_window(spec, b, p, np);
-    union {
-      uint4 u;
-      T e[kVec];
-    } out, ex;
-    if (extra) ex.u = __ldg(extra + idx);
-#pragma unroll
-    for (int e = 0; e < kVec; ++e) {
-      const int64_t j = jv * kVec + e;
-      if (w.allowed(j)) {
-        out.e[e] = extra ? ex.e[e] : E::from_float(0.0f);
+    // allowed keys: [a1, b1) U [a2, b2), both inside [0, nonpad)
+    const int64_t bl = w.band_lo < 0 ? 0 : w.band_lo, bh = w.band_hi < np ? w.band_hi : np;
+    const int64_t sl = w.span_lo < 0 ? 0 : w.span_lo, sh = w.span_hi < np ? w.span_hi : np;
+    const int a1 = static_cast<int>(bl < bh ? bl : 0), b1 = static_cast<int>(bl < bh ? bh : 0);
+    const int a2 = static_cast<int>(sl < sh ? sl : 0), b2 = static_cast<int>(sl < sh ? sh : 0);
+    for (int64_t jv = threadIdx.x; jv < row_vecs; jv += blockDim.x) {
+      const int j0 = static_cast<int>(jv * kVec);
+      const bool all_in = (j0 >= a1 && j0 + kVec <= b1) || (j0 >= a2 && j0 + kVec <= b2);
+      const bool all_out = (j0 + kVec <= a1 || j0 >= b1) && (j0 + kVec <= a2 || j0 >= b2);
+      Vec v;
+      if (all_out) {
+        v = low;
+      } else if (all_in) {
+        v.u = ext ? __ldg(ext + jv) : zero.u;
       } else {
-        out.e[e] = E::from_float(E::lowest());
+        Vec x;
+        x.u = ext ? __ldg(ext + jv) : zero.u;
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+          const int j = j0 + e;
+          const bool ok = (j >= a1 && j < b1) || (j >= a2 && j < b2);
+          v.e[e] = ok ? x.e[e] : low.e[e];
+        }
       }
+      out[jv] = v.u;
     }
-    bias[idx] = out.u;
   }
 }
 
@@ -147,21 +167,20 @@ cudaError_t launch_bias(void* bias, const extkv_bias_spec& s, const int64_t* non
                         cudaStream_t stream) {
   const int64_t es = dtype == EXTKV_F32 ? 4 : 2;
   const int64_t row_vecs = max_seq * es / 16;
-  const int64_t total = B * S_q * row_vecs;
-  if (total == 0) return cudaSuccess;
+  const int64_t rows = B * S_q;
+  if (rows == 0) return cudaSuccess;
   BiasSpec spec{s.causal, s.window, s.span_offsets, s.spans, s.extra, s.q_start};
   const int threads = 256;
-  const int64_t want = (total + threads - 1) / threads;
-  const int blocks = static_cast<int>(std::min<int64_t>(want, int64_t(num_sms()) * 8));
+  const int blocks = static_cast<int>(std::min<int64_t>(rows, int64_t(num_sms()) * 8));
   cudaLaunchConfig_t cfg = pdl_config(blocks, threads, stream);
   cudaLaunchAttribute attr[1];
   pdl_attr(cfg, attr);
   cudaError_t e =
       dtype == EXTKV_F32
           ? cudaLaunchKernelEx(&cfg, bias_kernel<float>, static_cast<uint4*>(bias), spec, nonpad,
-                               S_q, max_seq, row_vecs, total, status)
+                               S_q, max_seq, row_vecs, rows, status)
           : cudaLaunchKernelEx(&cfg, bias_kernel<__nv_bfloat16>, static_cast<uint4*>(bias), spec,
-                               nonpad, S_q, max_seq, row_vecs, total, status);
+                               nonpad, S_q, max_seq, row_vecs, rows, status);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

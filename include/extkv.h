@@ -114,7 +114,8 @@ int ext_kv_scatter(void *k_cache, void *v_cache, const void *k_new, const void *
  * Materialises the (B,1,S_q,max_seq) additive bias of `spec` (see
  * extkv_bias_spec; mobius issue #366, deliverable and acceptance criteria)
  * into `bias`.  Bit-exact: every entry is either the extra term, +0, or
- * lowest(T).  Requires max_seq * sizeof(T) % 16 == 0 and a 16-byte aligned
+ * lowest(T).  Requires max_seq * sizeof(T) % 16 == 0, max_seq <= 2^31 - 256
+ * (else EXTKV_ERR_UNSUPPORTED) and a 16-byte aligned
  * `bias` (and `extra`).  A batch with nonpad outside [0, max_seq] is left
  * untouched and flagged EXTKV_DEV_BAD_NONPAD.
  */
