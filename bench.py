@@ -7,10 +7,11 @@ sliding window 1024, bf16): TensorScatter of the new K/V rows, the
 (B,1,S_q,max_seq) bias build, and attention over the static cache.
 
 Prints ONE JSON line (rank 0).  `value` is whole-job algorithmic GB/s with the
-inputs resident in HBM; `e2e` is the same metric through the public API with
-pinned host inputs copied in and the output copied out every step.  The
-`roofline` object covers the attention kernel (the dominant one); `secondary`
-adds the other workloads' attention kernels (prefill in TFLOP/s).
+inputs resident in HBM (for a prefill workload given with --workload: the
+attention's algorithmic TFLOP/s); `e2e` is the same metric through the public
+API with pinned host inputs copied in and the output copied out every step.
+The `roofline` object covers the attention kernel (the dominant one);
+`secondary` adds the other workloads' attention calls (prefill in TFLOP/s).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs its own replica (weak scaling: independent
@@ -131,6 +132,17 @@ def step_bytes(w: wl.Workload, nonpad: np.ndarray, spans, mode: str) -> int:
         bias *= 2
     attn, _ = attention_work(w, nonpad, spans, mode)
     return scatter + bias + attn
+
+
+def step_work(w: wl.Workload, nonpad: np.ndarray, spans, mode: str):
+    """(amount, scale, unit) of the metric for one step: algorithmic GB/s of
+    the whole step for decode, the attention's algorithmic TFLOP/s for a
+    prefill chunk (the tensor-bound part; the scatter and the bias build are
+    byte-bound and reported in their own kernels' shares)."""
+    if w.S_q > 1:
+        _, flops = attention_work(w, nonpad, spans, mode)
+        return flops, 1e12, "TFLOP/s"
+    return step_bytes(w, nonpad, spans, mode), 1e9, "GB/s"
 
 
 def read_peaks():
@@ -265,10 +277,8 @@ class Decoder:
             ev[1].record()
 
     def kernels_per_step(self):
-        # scatter, bias build, attention (the decode path launches a plan
-        # kernel and the stream-K kernel)
-        attn = 2 if self.workspace is not None else 1
-        return 1 + (1 if self.mode == "bias" else 0) + attn
+        # scatter, bias build, and what the attention call reported launching
+        return 1 + (1 if self.mode == "bias" else 0) + self.ek.extkv_last_launches()
 
 
 def _events(n, external):
@@ -310,6 +320,8 @@ def run_ours(args, rank, local, world):
     nonpad, _, spans = wl.structure(w)
     nonpad = nonpad.numpy()
     sb = step_bytes(w, nonpad, spans, args.mode)
+    amount, scale, unit = step_work(w, nonpad, spans, args.mode)
+    prefill = w.S_q > 1
     attn_b, attn_f = attention_work(w, nonpad, spans, args.mode)
     R = _rotation(sb, device)
     dec = Decoder(w, device, args.mode, R)
@@ -336,7 +348,7 @@ def run_ours(args, rank, local, world):
     attn_ms = [a.elapsed_time(b) for a, b in evs] if evs else None
     ms_max = reduce_max(ms_total, world, device)
     ms_per_step = ms_max / K
-    value = whole_job_value(sb * K, world, ms_max / 1e3) / 1e9
+    value = whole_job_value(amount * K, world, ms_max / 1e3) / scale
 
     # status after the timed region: no device-side error may hide in the numbers
     assert ek.extkv_read_status(dec.status) == ek.EXTKV_OK, ek.extkv_last_error()
@@ -348,7 +360,13 @@ def run_ours(args, rank, local, world):
     peaks, peak_src = read_peaks()
     attn_avg_ms = statistics.mean(attn_ms) if attn_ms else None
     roof = None
-    if attn_avg_ms:
+    if attn_avg_ms and prefill:
+        achieved = attn_f / (attn_avg_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": args.traffic,
+                "kernel": kernel, "launch_us": round(attn_avg_ms * 1e3, 3),
+                "algorithmic_flops": attn_f, "peak_source": peak_src}
+    elif attn_avg_ms:
         achieved = attn_b / (attn_avg_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": args.traffic,
@@ -356,7 +374,7 @@ def run_ours(args, rank, local, world):
                 "algorithmic_bytes": attn_b, "peak_source": peak_src}
 
     out = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
         "data": "synthetic (seeded N(0,1) values, nonpad ~ U[512,4096]; no dataset)",
@@ -373,7 +391,7 @@ def run_ours(args, rank, local, world):
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(w, dec.base, args.mode, sb, args.cpu_seconds)
+        out["cpu_baseline"] = cpu_baseline(w, dec.base, args.mode, amount, scale, unit, args.cpu_seconds)
     if not args.no_secondary:
         out["secondary"] = secondary(args, device, peaks, peak_src)
     if rank == 0:
@@ -412,18 +430,20 @@ def run_e2e(dec: Decoder, K: int, W: int, world: int, device):
     sec = time.perf_counter() - t0
     sec = reduce_max(sec, world, device)
     nonpad, _, spans = wl.structure(w)
-    sb = step_bytes(w, nonpad.numpy(), spans, dec.mode)
-    return {"value": round(whole_job_value(sb * K, world, sec) / 1e9, 2), "unit": "GB/s",
+    amount, scale, unit = step_work(w, nonpad.numpy(), spans, dec.mode)
+    return {"value": round(whole_job_value(amount * K, world, sec) / scale, 2), "unit": unit,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(sec * 1e3 / K, 4),
             "timing": "host wall clock around K eager steps through the Python binding"}
 
 
 def secondary(args, device, peaks, peak_src):
-    """The other workloads' attention kernels, each timed alone with CUDA
-    events over rotating input sets."""
+    """The other workloads' attention calls, each timed alone: a CUDA graph of
+    n calls over rotating input sets (no host launch overhead in the number),
+    CUDA events on the launching stream around one replay."""
     from biased_gqa_attention_gb300 import extkv as ek
     res = {}
+    stream = torch.cuda.Stream(device)
     for w in (wl.C3, wl.C4, wl.C5):
         nonpad, _, spans = wl.structure(w)
         nonpad = nonpad.numpy()
@@ -431,35 +451,43 @@ def secondary(args, device, peaks, peak_src):
         touched = ab if w.S_q == 1 else ab + w.B * w.S_q * w.max_seq * 2
         R = min(_rotation(touched, device), 6)
         dec = Decoder(w, device, args.mode, R)
-        for r in range(R):
-            dec.scatter(r)
-            if args.mode == "bias":
-                dec.bias(r)
-        for i in range(3):
-            dec.attention(i % R)
+        with torch.cuda.stream(stream):
+            for r in range(R):
+                dec.scatter(r)
+                if args.mode == "bias":
+                    dec.bias(r)
+            for i in range(3):
+                dec.attention(i % R)
         torch.cuda.synchronize()
         n = 20
-        evs = _events(n, external=False)
-        for i in range(n):
-            evs[i][0].record()
-            dec.attention(i % R)
-            evs[i][1].record()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                dec.attention(i % R)
+        with torch.cuda.stream(stream):
+            g.replay()  # upload
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            g.replay()
+            t1.record(stream)
         torch.cuda.synchronize()
-        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        ms = t0.elapsed_time(t1) / n
         assert ek.extkv_read_status(dec.status) == ek.EXTKV_OK, ek.extkv_last_error()
         if w.S_q == 1:
             ach = ab / (ms / 1e3) / 1e9
             res[w.name] = {"bound": "hbm", "achieved": round(ach, 1), "unit": "GB/s",
                            "peak": peaks["hbm_gbs"], "frac": round(ach / peaks["hbm_gbs"], 4),
-                           "launch_us": round(ms * 1e3, 2), "kernel": ek.extkv_last_kernel()}
+                           "launch_us": round(ms * 1e3, 2), "kernel": ek.extkv_last_kernel(),
+                           "launches": ek.extkv_last_launches(), "algorithmic_bytes": ab}
         else:
             ach = af / (ms / 1e3) / 1e12
             res[w.name] = {"bound": "tensor", "achieved": round(ach, 2), "unit": "TFLOP/s",
                            "peak": peaks["bf16_tflops"], "frac": round(ach / peaks["bf16_tflops"], 4),
                            "launch_us": round(ms * 1e3, 2), "kernel": ek.extkv_last_kernel(),
-                           "algorithmic_flops": af}
+                           "launches": ek.extkv_last_launches(), "algorithmic_flops": af}
         res[w.name]["peak_source"] = peak_src
-        del dec
+        res[w.name]["timing"] = f"CUDA graph of {n} attention calls over {R} rotating input sets"
+        del dec, g
         torch.cuda.empty_cache()
     return res
 
@@ -489,7 +517,7 @@ def oracle_step(w: wl.Workload, h, spans, mode: str):
     return oracle.attention(h["q"], h["k_cache"], h["v_cache"], b, h["nonpad"], np.float32(w.scale))
 
 
-def cpu_baseline(w, base, mode, sb, seconds):
+def cpu_baseline(w, base, mode, amount, scale, unit, seconds):
     import oracle
     _, _, spans = wl.structure(w)
     h = _oracle_inputs(w, base)
@@ -501,7 +529,7 @@ def cpu_baseline(w, base, mode, sb, seconds):
         el = time.perf_counter() - t0
         if el >= seconds or n >= 200:
             break
-    return {"value": round(sb * n / el / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+    return {"value": round(amount * n / el / scale, 6), "unit": unit, "cores": oracle.num_threads(),
             "kind": "oracle", "sample": f"{n} full steps of {w.name} (scatter + bias + attention over "
             f"all rows), {el:.1f} s, fp64, OpenMP over query rows"}
 
@@ -516,6 +544,7 @@ def run_reference(args, rank, local, world):
     base = wl.make_inputs(w, "cpu")
     nonpad, _, spans = wl.structure(w)
     sb = step_bytes(w, nonpad.numpy(), spans, args.mode)
+    amount, scale, unit = step_work(w, nonpad.numpy(), spans, args.mode)
     h = _oracle_inputs(w, base)
     for _ in range(args.warmup):
         oracle_step(w, h, spans, args.mode)
@@ -523,15 +552,15 @@ def run_reference(args, rank, local, world):
     for _ in range(args.steps):
         oracle_step(w, h, spans, args.mode)
     el = time.perf_counter() - t0
-    value = sb * args.steps / el / 1e9
-    out = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+    value = amount * args.steps / el / scale
+    out = {"metric": METRIC, "value": round(value, 6), "unit": unit, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic (seeded N(0,1) values; no dataset)", "impl": "reference",
            "config": {"workload": w.name, "bias_mode": args.mode, "step_algorithmic_bytes": sb},
-           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+           "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": oracle.num_threads(),
                             "kind": "oracle", "sample": f"{args.steps} full steps of {w.name}"},
-           "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+           "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0},
            "gpu_launches": 0}
     print(json.dumps(out), flush=True)

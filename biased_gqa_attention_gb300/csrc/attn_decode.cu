@@ -954,7 +954,9 @@ cudaError_t launch_dm(const AttnArgs& a, const DecodeParams& prm, const CUtensor
   e = cudaFuncSetAttribute(decode_merge_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(cfg.dynamicSmemBytes));
   if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<MODE>, prm);
+  e = cudaLaunchKernelEx(&cfg, decode_merge_kernel<MODE>, prm);
+  if (e == cudaSuccess) note_launches(prm.plan ? 3 : 2);
+  return e;
 }
 
 template <int D>

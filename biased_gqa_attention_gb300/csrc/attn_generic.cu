@@ -157,6 +157,7 @@ cudaError_t launch_typed(const AttnArgs& a) {
 cudaError_t launch_attn_generic(const AttnArgs& a, const char** name) {
   *name = a.dtype == EXTKV_F32 ? "attn_generic_f32" : "attn_generic_bf16";
   if (a.B * a.Hq * a.S_q == 0) return cudaSuccess;
+  note_launches(1);
   return a.dtype == EXTKV_F32 ? launch_typed<float>(a) : launch_typed<__nv_bfloat16>(a);
 }
 

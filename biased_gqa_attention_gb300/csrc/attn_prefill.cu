@@ -961,6 +961,7 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
   cudaError_t e = cudaLaunchKernelEx(&cfg, attn_prefill_kernel<D, MODE>, qmap, kmap, vmap, tmap, prm);
   if (e != cudaSuccess) return e;
   *name = "attn_prefill_tcgen05";
+  note_launches(C::kTerm ? 2 : 1);  // the plan kernel, then the attention kernel
   return cudaGetLastError();
 }
 

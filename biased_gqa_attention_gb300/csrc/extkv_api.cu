@@ -16,6 +16,7 @@ namespace {
 
 thread_local char g_error[512] = "";
 thread_local const char* g_last_kernel = "";
+thread_local int g_launches = 0, g_last_launches = 0;
 thread_local int g_algo = EXTKV_ALGO_AUTO;
 
 int fail(int code, const char* fmt, ...) {
@@ -50,6 +51,8 @@ int check_workspace(const AttnArgs& a, size_t need) {
 }  // namespace
 
 void set_error(const char* msg) { snprintf(g_error, sizeof g_error, "%s", msg); }
+
+void note_launches(int n) { g_launches = n; }
 
 int num_sms() {
   // Cached per device; the SM count never changes for a device.
@@ -211,6 +214,7 @@ int attention_ext_kv(void* y, const void* q, const void* k_cache, const void* v_
 
   const char* name = "";
   cudaError_t e;
+  g_launches = 0;
   const size_t decode_ws = decode_workspace_bytes(B, Hq, Hkv, S_q, max_seq, D);
   // a materialised bias or an extra term needs the prefill kernel's column-mask table
   const size_t prefill_ws =
@@ -244,6 +248,7 @@ int attention_ext_kv(void* y, const void* q, const void* k_cache, const void* v_
   }
   if (e != cudaSuccess) return cuda_fail(e, "attention_ext_kv launch");
   g_last_kernel = name;
+  g_last_launches = g_launches;
   return EXTKV_OK;
 }
 
@@ -273,6 +278,8 @@ int extkv_read_status(const int32_t* status, void* stream) {
 const char* extkv_last_error(void) { return g_error; }
 
 const char* extkv_last_kernel(void) { return g_last_kernel; }
+
+int extkv_last_launches(void) { return g_last_launches; }
 
 int extkv_set_algo(int algo) {
   if (algo < EXTKV_ALGO_AUTO || algo > EXTKV_ALGO_PREFILL)

@@ -56,4 +56,8 @@ int num_sms();
 // Sets the calling thread's extkv_last_error() message.
 void set_error(const char* msg);
 
+// Records how many kernels the attention launcher just launched (read back
+// through extkv_last_launches()).
+void note_launches(int n);
+
 }  // namespace extkv

@@ -24,7 +24,7 @@ ALGO_AUTO, ALGO_GENERIC, ALGO_DECODE, ALGO_PREFILL = 0, 1, 2, 3
 # Every symbol include/extkv.h declares.
 SYMBOLS = ("ext_kv_scatter", "build_static_cache_bias", "attention_ext_kv_workspace_size",
            "attention_ext_kv", "extkv_clear_status", "extkv_read_status", "extkv_last_error",
-           "extkv_last_kernel", "extkv_set_algo", "attention_ext_kv_noalloc")
+           "extkv_last_kernel", "extkv_last_launches", "extkv_set_algo", "attention_ext_kv_noalloc")
 
 
 class ExtKVError(RuntimeError):
@@ -63,6 +63,7 @@ def load(path: str = LIB_PATH):
     lib.extkv_read_status.argtypes = [I32P, P]
     lib.extkv_last_error.restype = ctypes.c_char_p
     lib.extkv_last_kernel.restype = ctypes.c_char_p
+    lib.extkv_last_launches.restype = ctypes.c_int
     lib.extkv_set_algo.argtypes = [I]
     for name in ("ext_kv_scatter", "build_static_cache_bias", "attention_ext_kv", "attention_ext_kv_noalloc",
                  "extkv_clear_status", "extkv_read_status", "extkv_set_algo"):
@@ -237,6 +238,11 @@ def extkv_last_error() -> str:
 
 def extkv_last_kernel() -> str:
     return load().extkv_last_kernel().decode()
+
+
+def extkv_last_launches() -> int:
+    """Kernels the calling thread's last attention_ext_kv launched."""
+    return int(load().extkv_last_launches())
 
 
 def extkv_set_algo(algo: int) -> int:

@@ -224,6 +224,13 @@ const char *extkv_last_error(void);
 const char *extkv_last_kernel(void);
 
 /*
+ * Number of kernels the calling thread's last successful attention_ext_kv
+ * launched (a plan kernel, the attention kernel, a merge kernel), for callers
+ * and benchmarks that account for launches.  0 before any call.
+ */
+int extkv_last_launches(void);
+
+/*
  * Attention kernel selection for the calling thread.  EXTKV_ALGO_AUTO picks
  * by shape and type; the others force one kernel, and attention_ext_kv then
  * returns EXTKV_ERR_UNSUPPORTED for shapes that kernel cannot run.  Returns
