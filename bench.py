@@ -566,6 +566,15 @@ def run_reference(args, rank, local, world):
     print(json.dumps(out), flush=True)
 
 
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel, from
+# `ncu --set full` captures of the kernels as committed (decode: attn_decode_kernel<256, 2, kBias>;
+# prefill: attn_prefill_kernel<256, kBias>).  A kernel change makes these stale: drop the entry.
+NCU_TRAFFIC = {
+    ("decode_b8_hq16_hkv8_d256_w1024", "bias"): 65.40e6,
+    ("prefill_s2048_hq16_hkv8_d256_w1024_spans", "bias"): 47.8e6,
+}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -579,8 +588,11 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--clock-load-s", type=float, default=1.0)
     ap.add_argument("--traffic", type=float, default=None,
-                    help="ncu dram bytes per attention launch for the current kernel, if captured")
+                    help="ncu dram bytes per launch of the dominant kernel (default: the committed capture "
+                         "for this workload and mode, if any)")
     args = ap.parse_args(argv)
+    if args.traffic is None:
+        args.traffic = NCU_TRAFFIC.get((args.workload, args.mode))
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     rank, local, world = dist_env()
