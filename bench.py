@@ -231,11 +231,17 @@ def _rotation(touched_bytes: int, device) -> int:
 
 
 class Decoder:
-    """Device-resident state for one workload: R rotating input sets."""
+    """Device-resident state for one workload: R rotating input sets.
 
-    def __init__(self, w: wl.Workload, device, mode: str, sets: int):
+    A step is the scatter of the new rows, the bias build (materialised mode)
+    and the attention: by default the bias build and attention_ext_kv_scatter
+    (the scatter fused into the attention call), or, with fused_step=False, the
+    three separate calls."""
+
+    def __init__(self, w: wl.Workload, device, mode: str, sets: int, fused_step: bool = True):
         from biased_gqa_attention_gb300 import extkv as ek
         self.ek, self.w, self.mode, self.device = ek, w, mode, device
+        self.fused_step = fused_step
         base = wl.make_inputs(w, device)
         self.base = base
         self.sets = []
@@ -266,19 +272,32 @@ class Decoder:
                                  fused=s["spec"] if self.mode == "fused" else None,
                                  workspace=self.workspace, status=self.status)
 
+    def attention_scatter(self, r):
+        s = self.sets[r]
+        self.ek.attention_ext_kv_scatter(s["y"], s["q"], s["k"], s["v"], s["k_new"], s["v_new"], s["write_idx"],
+                                         s["nonpad"], self.w.scale,
+                                         bias=s["bias"] if self.mode == "bias" else None,
+                                         fused=s["spec"] if self.mode == "fused" else None,
+                                         workspace=self.workspace, status=self.status)
+
     def step(self, r, ev=None):
-        self.scatter(r)
+        if not self.fused_step:
+            self.scatter(r)
         if self.mode == "bias":
             self.bias(r)
         if ev:
             ev[0].record()
-        self.attention(r)
+        if self.fused_step:
+            self.attention_scatter(r)
+        else:
+            self.attention(r)
         if ev:
             ev[1].record()
 
     def kernels_per_step(self):
-        # scatter, bias build, and what the attention call reported launching
-        return 1 + (1 if self.mode == "bias" else 0) + self.ek.extkv_last_launches()
+        # (scatter,) bias build, and what the attention call reported launching
+        # (which counts a scatter kernel it ran ahead of an unfused path)
+        return (0 if self.fused_step else 1) + (1 if self.mode == "bias" else 0) + self.ek.extkv_last_launches()
 
 
 def _events(n, external):
@@ -323,8 +342,11 @@ def run_ours(args, rank, local, world):
     amount, scale, unit = step_work(w, nonpad, spans, args.mode)
     prefill = w.S_q > 1
     attn_b, attn_f = attention_work(w, nonpad, spans, args.mode)
+    fused_step = not args.unfused_step
+    if fused_step:  # the attention call also moves the new rows (read + write, K and V)
+        attn_b += 2 * 2 * w.B * w.Hkv * w.S_q * w.D * (4 if w.dtype == torch.float32 else 2)
     R = _rotation(sb, device)
-    dec = Decoder(w, device, args.mode, R)
+    dec = Decoder(w, device, args.mode, R, fused_step=fused_step)
     stream = torch.cuda.Stream(device)
     K, W = args.steps, args.warmup
 
@@ -383,7 +405,9 @@ def run_ours(args, rank, local, world):
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": f"{R} rotating input sets, >2x L2 touched between reuses",
                    "timing": "CUDA graph of K steps, CUDA events on the launching stream",
-                   "step": "ext_kv_scatter + build_static_cache_bias + attention_ext_kv",
+                   "step": ("build_static_cache_bias + attention_ext_kv_scatter (the scatter fused into "
+                            "the attention call)" if fused_step else
+                            "ext_kv_scatter + build_static_cache_bias + attention_ext_kv"),
                    "step_algorithmic_bytes": sb},
         "gpu_launches": K * dec.kernels_per_step(),
         "roofline": roof,
@@ -584,6 +608,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=wl.C2.name, choices=sorted(wl.BY_NAME))
     ap.add_argument("--mode", choices=["bias", "fused"], default="bias")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--unfused-step", action="store_true",
+                    help="time the step as three calls (ext_kv_scatter, bias build, attention_ext_kv)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--clock-load-s", type=float, default=1.0)

@@ -117,6 +117,14 @@ struct DecodeParams {
   int4* info;  // per unit: {first CTA, number of slices, slot in the first CTA, 0}; slices 0: no live tile
   float* part;
   int32_t* status;
+  // fused scatter (k_new == nullptr: none): the new rows (B, Hkv, S_new, D) go
+  // to slots [write_idx[b], write_idx[b] + S_new) of the caches
+  __nv_bfloat16* kc_w;
+  __nv_bfloat16* vc_w;
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  const int64_t* write_idx;
+  int S_new;
 };
 
 // Allowed keys of one query position, as int32 bounds clipped to
@@ -304,7 +312,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeP
 // of batch b (Hkv units of cnt[b] items each), prefix_s[B] = T.  One warp.
 template <int MODE>
 __device__ __forceinline__ int64_t batch_tables(const DecodeParams& p, int lane, int32_t* prefix_s,
-                                                int32_t* np_s, Runs* runs_s) {
+                                                int32_t* np_s, Runs* runs_s, int32_t* wi_s) {
   int run = 0;
   for (int b0 = 0; b0 < p.B; b0 += 32) {
     const int b = b0 + lane;
@@ -312,6 +320,10 @@ __device__ __forceinline__ int64_t batch_tables(const DecodeParams& p, int lane,
     if (b < p.B) {
       const int64_t np64 = p.nonpad[b];
       np_s[b] = bad_nonpad(np64, p.max_seq) ? 0 : static_cast<int>(np64);
+      if (p.k_new) {  // first new slot of the fused scatter; -1: none or out of range (skipped)
+        const int64_t w = p.write_idx[b];
+        wi_s[b] = (w < 0 || w + p.S_new > p.max_seq) ? -1 : static_cast<int>(w);
+      }
       int cnt;
       if (p.plan) {
         cnt = p.count[b];
@@ -360,7 +372,8 @@ struct Smem {
   static constexpr int kBars = kTerm + SPW * 256;          // SPW stages + 2 Q slots
   static constexpr int kPrefix = kBars + (SPW + 2) * 8;    // int32 [kMaxB + 1]
   static constexpr int kNp = kPrefix + (kMaxB + 1) * 4 + 12;  // int32 [kMaxB]
-  static constexpr int kRuns = kNp + kMaxB * 4;            // Runs [kMaxB] (no plan)
+  static constexpr int kWi = kNp + kMaxB * 4;              // int32 [kMaxB]: write_idx (fused scatter)
+  static constexpr int kRuns = kWi + kMaxB * 4;            // Runs [kMaxB] (no plan)
   static constexpr int kWork = kRuns;                      // uint16 [kMaxWork] (plan)
   static constexpr int kEnd = kRuns + kMaxB * 16;
   static_assert(kMaxWork * 2 <= kMaxB * 16, "the work table shares the runs table");
@@ -385,6 +398,7 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
   uint64_t* qbars = bars + SPW;
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + S::kPrefix);
   int32_t* np_s = reinterpret_cast<int32_t*>(smem + S::kNp);
+  int32_t* wi_s = reinterpret_cast<int32_t*>(smem + S::kWi);
   Runs* runs_s = reinterpret_cast<Runs*>(smem + S::kRuns);
   uint16_t* work = reinterpret_cast<uint16_t*>(smem + S::kWork);
   const int lane = threadIdx.x;
@@ -403,7 +417,7 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
   // previous kernel in the stream wrote.
   ptx::grid_dependency_wait();
 
-  const int64_t T = batch_tables<MODE>(p, lane, prefix, np_s, runs_s);
+  const int64_t T = batch_tables<MODE>(p, lane, prefix, np_s, runs_s, wi_s);
   if (c == 0) {
     // units without a live tile (the merge kernel writes their zero rows)
     for (int b = lane; b < p.B; b += 32) {
@@ -414,7 +428,34 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
   }
   // Slice over min(G, T) CTAs: every slice holds at least one item.
   const int G = static_cast<int>(T < p.G ? T : static_cast<int64_t>(p.G));
-  if (c >= G) return;
+  // The fused scatter, this CTA's share (all CTAs together write every new
+  // row into the caches).  Loads of other CTAs may see a row before or after
+  // it is written; a tile that holds new rows is patched from k_new / v_new
+  // in shared memory below.
+  auto scatter_share = [&]() {
+    if (!p.k_new) return;
+    const int vpr = D / 8;  // 16-byte vectors per row
+    const int64_t total = static_cast<int64_t>(p.B) * p.Hkv * p.S_new * vpr;
+    for (int64_t i = static_cast<int64_t>(c) * 32 + lane; i < total; i += static_cast<int64_t>(gridDim.x) * 32) {
+      const int64_t row = i / vpr;  // over (b, kv head, s)
+      const int v = static_cast<int>(i % vpr);
+      const int sn = static_cast<int>(row % p.S_new);
+      const int64_t bh = row / p.S_new;
+      const int b = static_cast<int>(bh / p.Hkv);
+      const int64_t w = p.write_idx[b];
+      if (w < 0 || w + p.S_new > p.max_seq) {
+        if (sn == 0 && v == 0 && bh % p.Hkv == 0) report(p.status, EXTKV_DEV_BAD_WRITE_IDX);
+        continue;
+      }
+      const int64_t dst = (bh * p.max_seq + w + sn) * D + v * 8, src = row * D + v * 8;
+      *reinterpret_cast<uint4*>(p.kc_w + dst) = __ldg(reinterpret_cast<const uint4*>(p.k_new + src));
+      *reinterpret_cast<uint4*>(p.vc_w + dst) = __ldg(reinterpret_cast<const uint4*>(p.v_new + src));
+    }
+  };
+  if (c >= G) {
+    scatter_share();
+    return;
+  }
   const int64_t x0 = (static_cast<int64_t>(c) * T) / G, x1 = (static_cast<int64_t>(c + 1) * T) / G;
   const int n = static_cast<int>(x1 - x0);
 
@@ -498,6 +539,7 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
     }
   };
   fill(0);
+  scatter_share();  // this CTA's share, while its first loads are in flight
 
   // ---- consumer ----
   constexpr int kAcc = kKSteps >= 16 ? 4 : 2;  // independent QK^T accumulator chains
@@ -510,6 +552,7 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   Win32 w0{}, w1{};
   int np = 0;
+  int w_new = -1;  // first new slot of the current unit's batch (fused scatter), -1: none
   bool failed = false;
   uint32_t q_s = 0;
   Cursor cc = cursor_at(x0);
@@ -599,6 +642,7 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
         p.info[cc.b * p.Hkv + cc.kvh] = make_int4(c, c_last - c + 1, ub <= x0 ? 0 : 1, 0);
       }
       np = np_s[cc.b];
+      if (p.k_new) w_new = wi_s[cc.b];  // -1: the scatter skipped this batch, no patch
       if (MODE == kFused || MODE == kFusedExtra) {
         const int64_t qs = query_start(p.spec.q_start, cc.b, np, p.S_q);
         w0 = win32(p.spec, cc.b, qs + i0, np, p.max_seq);
@@ -626,6 +670,23 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
     const uint32_t k_s = ptx::smem_u32(kst), v_s = k_s + S::kTileBytes;
     const uint16_t* term = reinterpret_cast<const uint16_t*>(smem + S::kTerm + st * 256);
     const int key0 = tile_of(cc, k) * kTile;
+    if (w_new >= 0 && key0 < w_new + p.S_new && key0 + kTile > w_new) {
+      // new rows of this tile straight from k_new / v_new (what the cache
+      // holds after the scatter), into the 128-byte-swizzled stage layout
+      const int lo = max(key0, w_new), hi = min(key0 + kTile, w_new + p.S_new);
+      constexpr int vpr = D / 8;
+      const int64_t nb = static_cast<int64_t>(cc.b * p.Hkv + cc.kvh) * p.S_new;
+      for (int idx = lane; idx < (hi - lo) * vpr; idx += 32) {
+        const int key = lo + idx / vpr;
+        const int r = key - key0, ch = idx % vpr;
+        const int off = (ch >> 3) * (kTile * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+        const int64_t src = (nb + (key - w_new)) * D + ch * 8;
+        *reinterpret_cast<uint4*>(kst + off) = __ldg(reinterpret_cast<const uint4*>(p.k_new + src));
+        *reinterpret_cast<uint4*>(kst + S::kTileBytes + off) = __ldg(reinterpret_cast<const uint4*>(p.v_new + src));
+      }
+      ptx::fence_proxy_async_smem();  // these generic writes precede the stage's next TMA fill
+      __syncwarp();
+    }
 
     // S^T (16 keys x 8 rows) = K (16 x D) Q^T (D x 8), kAcc interleaved chains
     float sa[kAcc][4];
@@ -1018,6 +1079,12 @@ cudaError_t launch_d(const AttnArgs& a, const char** name) {
   prm.info = reinterpret_cast<int4*>(wsb + ws.info);
   prm.part = reinterpret_cast<float*>(wsb + ws.part);
   prm.status = a.status;
+  prm.kc_w = static_cast<__nv_bfloat16*>(a.kc_w);
+  prm.vc_w = static_cast<__nv_bfloat16*>(a.vc_w);
+  prm.k_new = static_cast<const __nv_bfloat16*>(a.k_new);
+  prm.v_new = static_cast<const __nv_bfloat16*>(a.v_new);
+  prm.write_idx = a.write_idx;
+  prm.S_new = static_cast<int>(a.S_new);
 
   cudaError_t e;
   switch (mode_of(a)) {
@@ -1027,7 +1094,7 @@ cudaError_t launch_d(const AttnArgs& a, const char** name) {
     default: e = launch_dm<D, kFusedExtra>(a, prm, kmap, vmap, qmap, tmap, max_tiles); break;
   }
   if (e != cudaSuccess) return e;
-  *name = "attn_decode_streamk_mma";
+  *name = prm.k_new ? "attn_decode_streamk_mma_scatter" : "attn_decode_streamk_mma";
   return cudaGetLastError();
 }
 

@@ -152,12 +152,25 @@ size_t attention_ext_kv_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64
   return need;
 }
 
-int attention_ext_kv(void* y, const void* q, const void* k_cache, const void* v_cache,
-                     const void* bias, const extkv_bias_spec* fused, const int64_t* nonpad,
-                     float scale, int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq,
-                     int64_t D, int dtype, void* workspace, size_t ws_bytes, int32_t* status,
-                     void* stream) {
-  g_error[0] = 0;
+}  // extern "C"
+
+namespace extkv {
+namespace {
+
+// A scatter to fuse into the attention call (ext_kv_scatter's arguments).
+struct ScatterIn {
+  void* k_cache;
+  void* v_cache;
+  const void* k_new;
+  const void* v_new;
+  const int64_t* write_idx;
+  int64_t S_new;
+};
+
+int attention_impl(void* y, const void* q, const void* k_cache, const void* v_cache, const void* bias,
+                   const extkv_bias_spec* fused, const int64_t* nonpad, float scale, int64_t B, int64_t Hq,
+                   int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t D, int dtype, void* workspace,
+                   size_t ws_bytes, int32_t* status, void* stream, const ScatterIn* sc) {
   if (!valid_dtype(dtype)) return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv: unknown dtype %d", dtype);
   if (B < 0 || S_q < 0 || Hq <= 0 || Hkv <= 0 || max_seq <= 0 || D <= 0)
     return fail(EXTKV_ERR_INVALID_ARG,
@@ -172,7 +185,12 @@ int attention_ext_kv(void* y, const void* q, const void* k_cache, const void* v_
                 (long long)D);
   if (bias && fused)
     return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv: pass either a materialised bias or a fused spec, not both");
-  if (B == 0 || S_q == 0) return EXTKV_OK;
+  if (B == 0 || S_q == 0) {
+    if (!sc) return EXTKV_OK;
+    cudaError_t e = launch_scatter(sc->k_cache, sc->v_cache, sc->k_new, sc->v_new, sc->write_idx, B, Hkv,
+                                   sc->S_new, max_seq, D, dtype, status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? EXTKV_OK : cuda_fail(e, "attention_ext_kv_scatter launch");
+  }
   if (!y || !q || !k_cache || !v_cache || !nonpad)
     return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv: null pointer");
   if (fused && ((fused->span_offsets == nullptr) != (fused->spans == nullptr)))
@@ -215,41 +233,104 @@ int attention_ext_kv(void* y, const void* q, const void* k_cache, const void* v_
   const char* name = "";
   cudaError_t e;
   g_launches = 0;
+  int extra_launches = 0;  // a scatter kernel launched ahead of an unfused path
+  // the decode kernel takes the scatter; the other paths get the scatter kernel first
+  auto launch_decode_with = [&](AttnArgs& aa, const ScatterIn* s, const char** nm) {
+    if (s) {
+      aa.kc_w = s->k_cache;
+      aa.vc_w = s->v_cache;
+      aa.k_new = s->k_new;
+      aa.v_new = s->v_new;
+      aa.write_idx = s->write_idx;
+      aa.S_new = s->S_new;
+    }
+    return launch_attn_decode(aa, nm);
+  };
+  auto scatter_first = [&](const AttnArgs& aa, const ScatterIn* s) -> cudaError_t {
+    if (!s) return cudaSuccess;
+    ++extra_launches;
+    return launch_scatter(s->k_cache, s->v_cache, s->k_new, s->v_new, s->write_idx, aa.B, aa.Hkv, s->S_new,
+                          aa.max_seq, aa.D, aa.dtype, aa.status, aa.stream);
+  };
   const size_t decode_ws = decode_workspace_bytes(B, Hq, Hkv, S_q, max_seq, D);
   // a materialised bias or an extra term needs the prefill kernel's column-mask table
   const size_t prefill_ws =
       (bias || (fused && fused->extra)) ? prefill_workspace_bytes(B, S_q, max_seq) : 0;
   switch (g_algo) {
     case EXTKV_ALGO_GENERIC:
+      if ((e = scatter_first(a, sc)) != cudaSuccess) break;
       e = launch_attn_generic(a, &name);
       break;
     case EXTKV_ALGO_DECODE:
       if (!decode_supported(a))
         return fail(EXTKV_ERR_UNSUPPORTED, "attention_ext_kv: the decode kernel cannot run this shape/type");
       if (int rc = check_workspace(a, decode_ws)) return rc;
-      e = launch_attn_decode(a, &name);
+      e = launch_decode_with(a, sc, &name);
       break;
     case EXTKV_ALGO_PREFILL:
       if (!prefill_supported(a))
         return fail(EXTKV_ERR_UNSUPPORTED, "attention_ext_kv: the prefill kernel cannot run this shape/type");
       if (int rc = check_workspace(a, prefill_ws)) return rc;
+      if ((e = scatter_first(a, sc)) != cudaSuccess) break;
       e = launch_attn_prefill(a, &name);
       break;
     default:
       if (decode_supported(a)) {
         if (int rc = check_workspace(a, decode_ws)) return rc;
-        e = launch_attn_decode(a, &name);
+        e = launch_decode_with(a, sc, &name);
       } else if (prefill_supported(a)) {
         if (int rc = check_workspace(a, prefill_ws)) return rc;
+        if ((e = scatter_first(a, sc)) != cudaSuccess) break;
         e = launch_attn_prefill(a, &name);
       } else {
+        if ((e = scatter_first(a, sc)) != cudaSuccess) break;
         e = launch_attn_generic(a, &name);
       }
   }
   if (e != cudaSuccess) return cuda_fail(e, "attention_ext_kv launch");
   g_last_kernel = name;
-  g_last_launches = g_launches;
+  g_last_launches = g_launches + extra_launches;
   return EXTKV_OK;
+}
+
+}  // namespace
+}  // namespace extkv
+
+extern "C" {
+
+int attention_ext_kv(void* y, const void* q, const void* k_cache, const void* v_cache,
+                     const void* bias, const extkv_bias_spec* fused, const int64_t* nonpad,
+                     float scale, int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq,
+                     int64_t D, int dtype, void* workspace, size_t ws_bytes, int32_t* status,
+                     void* stream) {
+  g_error[0] = 0;
+  return attention_impl(y, q, k_cache, v_cache, bias, fused, nonpad, scale, B, Hq, Hkv, S_q, max_seq, D, dtype,
+                        workspace, ws_bytes, status, stream, nullptr);
+}
+
+int attention_ext_kv_scatter(void* y, const void* q, void* k_cache, void* v_cache, const void* k_new,
+                             const void* v_new, const int64_t* write_idx, int64_t S_new, const void* bias,
+                             const extkv_bias_spec* fused, const int64_t* nonpad, float scale, int64_t B,
+                             int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t D, int dtype,
+                             void* workspace, size_t ws_bytes, int32_t* status, void* stream) {
+  g_error[0] = 0;
+  if (!valid_dtype(dtype))
+    return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv_scatter: unknown dtype %d", dtype);
+  if (S_new < 0 || S_new > max_seq)
+    return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv_scatter: S_new=%lld outside [0, max_seq=%lld]",
+                (long long)S_new, (long long)max_seq);
+  if (B > 0 && S_new > 0) {
+    if (!k_cache || !v_cache || !k_new || !v_new || !write_idx)
+      return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv_scatter: null pointer");
+    if (D <= 0 || (D * elem_size(dtype)) % 16)
+      return fail(EXTKV_ERR_UNSUPPORTED, "attention_ext_kv_scatter: D*sizeof(T) must be a multiple of 16 (D=%lld)",
+                  (long long)D);
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(write_idx, 8))
+      return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv_scatter: tensors must be 16-byte aligned");
+  }
+  const ScatterIn sc{k_cache, v_cache, k_new, v_new, write_idx, S_new};
+  return attention_impl(y, q, k_cache, v_cache, bias, fused, nonpad, scale, B, Hq, Hkv, S_q, max_seq, D, dtype,
+                        workspace, ws_bytes, status, stream, (B > 0 && S_new > 0) ? &sc : nullptr);
 }
 
 int extkv_clear_status(int32_t* status, void* stream) {

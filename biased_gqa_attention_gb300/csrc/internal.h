@@ -30,6 +30,13 @@ struct AttnArgs {
   void* workspace;
   size_t ws_bytes;
   cudaStream_t stream;
+  // fused scatter, taken by the decode kernel (k_new == nullptr: none)
+  void* kc_w;
+  void* vc_w;
+  const void* k_new;
+  const void* v_new;
+  const int64_t* write_idx;
+  int64_t S_new;
 };
 
 // Each launcher returns cudaSuccess or the launch error; `name` receives the

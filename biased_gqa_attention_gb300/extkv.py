@@ -23,8 +23,9 @@ ALGO_AUTO, ALGO_GENERIC, ALGO_DECODE, ALGO_PREFILL = 0, 1, 2, 3
 
 # Every symbol include/extkv.h declares.
 SYMBOLS = ("ext_kv_scatter", "build_static_cache_bias", "attention_ext_kv_workspace_size",
-           "attention_ext_kv", "extkv_clear_status", "extkv_read_status", "extkv_last_error",
-           "extkv_last_kernel", "extkv_last_launches", "extkv_set_algo", "attention_ext_kv_noalloc")
+           "attention_ext_kv", "attention_ext_kv_scatter", "extkv_clear_status", "extkv_read_status",
+           "extkv_last_error", "extkv_last_kernel", "extkv_last_launches", "extkv_set_algo",
+           "attention_ext_kv_noalloc")
 
 
 class ExtKVError(RuntimeError):
@@ -57,6 +58,9 @@ def load(path: str = LIB_PATH):
     lib.attention_ext_kv_workspace_size.restype = ctypes.c_size_t
     lib.attention_ext_kv.argtypes = [P, P, P, P, P, ctypes.POINTER(_BiasSpec), P, ctypes.c_float,
                                      I64, I64, I64, I64, I64, I64, I, P, ctypes.c_size_t, I32P, P]
+    lib.attention_ext_kv_scatter.argtypes = [P, P, P, P, P, P, P, I64, P, ctypes.POINTER(_BiasSpec), P,
+                                             ctypes.c_float, I64, I64, I64, I64, I64, I64, I, P,
+                                             ctypes.c_size_t, I32P, P]
     lib.attention_ext_kv_noalloc.argtypes = [P, P, P, P, P, ctypes.POINTER(_BiasSpec), P,
                                              ctypes.c_float, I64, I64, I64, I64, I64, I64, I, I32P, P]
     lib.extkv_clear_status.argtypes = [I32P, P]
@@ -190,6 +194,36 @@ def attention_ext_kv(y, q, k_cache, v_cache, nonpad, scale, bias=None, fused: Op
                                    None if c is None else ctypes.byref(c), _p(nonpad), float(scale),
                                    B, Hq, Hkv, S_q, max_seq, D, _dt(q), _p(workspace), ws, _p(status),
                                    _stream(stream)))
+
+
+def attention_ext_kv_scatter(y, q, k_cache, v_cache, k_new, v_new, write_idx, nonpad, scale, bias=None,
+                             fused: Optional[BiasSpec] = None, workspace=None, status=None, stream=None):
+    """ext_kv_scatter of (k_new, v_new) at write_idx, then attention_ext_kv over
+    the updated caches, in one call (fused into the decode kernel where it runs)."""
+    for t, n in ((y, "y"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (k_new, "k_new"),
+                 (v_new, "v_new")):
+        _need(t, n, dims=4, dtype=q.dtype)
+    _need(bias, "bias", dims=4, dtype=q.dtype)
+    _need(nonpad, "nonpad", dims=1, dtype=torch.int64)
+    _need(write_idx, "write_idx", dims=1, dtype=torch.int64)
+    B, Hq, S_q, D = q.shape
+    Hkv, max_seq = k_cache.shape[1], k_cache.shape[2]
+    S_new = k_new.shape[2]
+    if y.shape != q.shape or v_cache.shape != k_cache.shape or k_cache.shape[0] != B or \
+            k_cache.shape[3] != D or k_new.shape != v_new.shape or k_new.shape[:2] != (B, Hkv) or \
+            k_new.shape[3] != D or write_idx.shape[0] != B:
+        raise ValueError("inconsistent q / y / cache / new-row shapes")
+    c = None if fused is None else fused._c()
+    if workspace is None:
+        need = load().attention_ext_kv_workspace_size(B, Hq, Hkv, S_q, max_seq, D, _dt(q))
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().attention_ext_kv_scatter(_p(y), _p(q), _p(k_cache), _p(v_cache), _p(k_new), _p(v_new),
+                                           _p(write_idx), S_new, _p(bias),
+                                           None if c is None else ctypes.byref(c), _p(nonpad), float(scale),
+                                           B, Hq, Hkv, S_q, max_seq, D, _dt(q), _p(workspace), ws,
+                                           _p(status), _stream(stream)))
 
 
 def attention_ext_kv_noalloc(y, q, k_cache, v_cache, nonpad, scale, bias=None,

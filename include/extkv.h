@@ -172,6 +172,32 @@ int attention_ext_kv(void *y, const void *q, const void *k_cache, const void *v_
                      int32_t *status, void *stream);
 
 /*
+ * ext_kv_scatter followed by attention_ext_kv, in one call: the same results
+ * (the caches hold the new rows afterwards, bit for bit, and y is what
+ * attention_ext_kv gives over the updated caches).  The scatter is the step
+ * just before the attention in the pages' decode graph ("Skill: Attention
+ * Optimization", "In-place KV for ONNX Attention via TensorScatter (static
+ * cache)"); fusing it saves a launch and a pass over the new rows.
+ *   - k_new / v_new: (B, Hkv, S_new, D), written to slots
+ *     [write_idx[b], write_idx[b] + S_new) of k_cache / v_cache (which are
+ *     therefore not const here).  S_new == 0 is attention_ext_kv.
+ *   - Where the decode kernel runs (see attention_ext_kv), it writes the
+ *     rows itself and takes the tiles that hold them from k_new / v_new;
+ *     elsewhere the scatter kernel runs first, then the attention.
+ *     extkv_last_kernel() names the path ("..._scatter" when fused).
+ *   - A batch whose new rows would leave [0, max_seq) is not written and is
+ *     flagged EXTKV_DEV_BAD_WRITE_IDX; its attention reads the cache as it was.
+ *   - Other arguments, requirements and errors as for ext_kv_scatter and
+ *     attention_ext_kv; the workspace is attention_ext_kv_workspace_size(...).
+ */
+int attention_ext_kv_scatter(void *y, const void *q, void *k_cache, void *v_cache, const void *k_new,
+                             const void *v_new, const int64_t *write_idx, int64_t S_new,
+                             const void *bias, const extkv_bias_spec *fused, const int64_t *nonpad,
+                             float scale, int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q,
+                             int64_t max_seq, int64_t D, int dtype, void *workspace, size_t ws_bytes,
+                             int32_t *status, void *stream);
+
+/*
  * Size of the static scratch array behind attention_ext_kv_noalloc: 16 MiB of
  * device memory, held by every GPU that loads this library until exit.
  */
