@@ -59,6 +59,8 @@ def _load():
             lib.oracle_scatter.restype = I64
             lib.oracle_bias.argtypes = [P, I, I64, P, P, P, P, P, I64, I64, I64, I]
             lib.oracle_bias.restype = I64
+            lib.oracle_bias_from_mask.argtypes = [P, P, I64, I]
+            lib.oracle_bias_from_mask.restype = None
             lib.oracle_attention.argtypes = [P, P, P, P, P, P, ctypes.c_float, I64, I64, I64,
                                              I64, I64, I64, I, P, I64]
             lib.oracle_attention.restype = I64
@@ -144,6 +146,15 @@ def bias(nonpad, S_q, max_seq, dt, causal=True, window=0, spans=None, extra=None
     bad = _load().oracle_bias(_ptr(out), int(bool(causal)), int(window), _ptr(so), _ptr(sp),
                               _ptr(ex), _ptr(qs), _ptr(np_), B, S_q, max_seq, DTYPES[dt])
     return out, int(bad)
+
+
+def bias_from_mask(mask, dt):
+    """The additive bias of a boolean (B,1,S_q,max_seq) mask in type ``dt``
+    (raw bits): 0 where the mask is true, lowest(dt) where it is false."""
+    m = np.ascontiguousarray(np.asarray(mask).astype(np.uint8))
+    out = np.zeros(m.shape, _RAW[dt])
+    _load().oracle_bias_from_mask(_ptr(out), _ptr(m), int(m.size), DTYPES[dt])
+    return out
 
 
 def attention(q, k_cache, v_cache, bias_, nonpad, scale, rows=None):

@@ -168,6 +168,21 @@ int64_t oracle_bias(void *bias, int causal, int64_t window, const int64_t *span_
   return bad;
 }
 
+/* ---- a boolean attention mask as the additive bias ---------------------- */
+/*
+ * [ORT] section 6, "Additive-bias path", and the attention-mask skill ("Bool
+ * mask vs float additive bias"): a boolean mask is turned into an additive
+ * bias -- an attended slot (mask != 0) gets 0, a masked slot the sentinel,
+ * here lowest(T) as for every other masked slot of this path ([ORT] section
+ * 8).  n elements of (B,1,S_q,max_seq), element by element.
+ */
+void oracle_bias_from_mask(void *bias, const unsigned char *mask, int64_t n, int dt) {
+  for (int64_t i = 0; i < n; ++i) {
+    if (mask[i]) orc_store_zero(bias, i, dt);
+    else orc_store_lowest(bias, i, dt);
+  }
+}
+
 /* ---- steps 3-6: scores, bias, softmax, PV ----------------------------- */
 /*
  * One query row (b, h, i), written out as the plain definition:

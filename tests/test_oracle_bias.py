@@ -150,3 +150,58 @@ def test_out_of_range_nonpad_is_reported():
     b, bad = oracle.bias([5, 17, -1], S_q=1, max_seq=16, dt="f32")
     assert bad == 2
     assert allowed_mask(b[0, 0], "f32")[0, :5].all()
+
+
+# ---- a boolean attention mask turned into the additive bias ------------------
+# "ONNX Domain Attention (Opset 23/24) CUDA Patterns", section 6 ("Additive-bias
+# path", bool mask converted to bias) and the attention-mask skill ("Bool mask
+# vs float additive bias": both represent any pattern; the bool mask becomes a
+# float bias internally).  Pinned against independent paths: the spec builder
+# above, and the attention with and without a bias.
+
+def _causal_window_mask(nonpad, S_q, max_seq, window):
+    """Boolean mask from the closed form of the section-11 positions: query i of
+    batch b sits at max(nonpad - S_q, 0) + i and sees j in (p - window, p], j < nonpad."""
+    B = len(nonpad)
+    m = np.zeros((B, 1, S_q, max_seq), bool)
+    j = np.arange(max_seq)
+    for b, n in enumerate(nonpad):
+        qs = max(n - S_q, 0)
+        for i in range(S_q):
+            p = qs + i
+            m[b, 0, i] = (j <= p) & (j < n) & ((p - j < window) if window > 0 else True)
+    return m
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_bool_mask_bias_equals_the_spec_builder(dt):
+    nonpad, S_q, max_seq, W = [37, 5, 48], 6, 48, 9
+    mask = _causal_window_mask(nonpad, S_q, max_seq, W)
+    from_mask = oracle.bias_from_mask(mask, dt)
+    from_spec, bad = oracle.bias(nonpad, S_q=S_q, max_seq=max_seq, dt=dt, causal=True, window=W)
+    assert bad == 0
+    assert np.array_equal(from_mask, from_spec)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_bool_mask_all_true_is_no_bias_and_a_false_row_is_a_zero_row(dt):
+    rng = np.random.default_rng(5)
+    B, Hq, Hkv, S_q, max_seq, D = 2, 4, 2, 3, 24, 8
+
+    def rand(shape):  # fp32 values, or their bf16 bits (round to nearest even)
+        x = rng.standard_normal(shape).astype(np.float32)
+        if dt == "f32":
+            return x
+        u = x.view(np.uint32).astype(np.uint64)
+        return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+    q, k, v = rand((B, Hq, S_q, D)), rand((B, Hkv, max_seq, D)), rand((B, Hkv, max_seq, D))
+    nonpad = np.array([24, 17], np.int64)
+    mask = np.ones((B, 1, S_q, max_seq), bool)
+    y_all = oracle.attention(q, k, v, oracle.bias_from_mask(mask, dt), nonpad, 0.35)
+    y_none = oracle.attention(q, k, v, None, nonpad, 0.35)
+    assert np.array_equal(y_all, y_none)
+    mask[1, 0, 2, :] = False  # query row 2 of batch 1 attends nothing
+    y = oracle.attention(q, k, v, oracle.bias_from_mask(mask, dt), nonpad, 0.35)
+    assert np.all(y[1, :, 2] == 0.0)
+    assert np.array_equal(y[0], y_none[0])
