@@ -129,6 +129,23 @@ int build_static_cache_bias(void* bias, const extkv_bias_spec* spec, const int64
   return EXTKV_OK;
 }
 
+int build_bias_from_bool_mask(void* bias, const uint8_t* mask, int64_t B, int64_t S_q, int64_t max_seq, int dtype,
+                              void* stream) {
+  g_error[0] = 0;
+  if (!valid_dtype(dtype)) return fail(EXTKV_ERR_INVALID_ARG, "build_bias_from_bool_mask: unknown dtype %d", dtype);
+  if (B < 0 || S_q < 0 || max_seq <= 0)
+    return fail(EXTKV_ERR_INVALID_ARG, "build_bias_from_bool_mask: bad sizes B=%lld S_q=%lld max_seq=%lld",
+                (long long)B, (long long)S_q, (long long)max_seq);
+  const int64_t n = B * S_q * max_seq;
+  if (n == 0) return EXTKV_OK;
+  if (!bias || !mask) return fail(EXTKV_ERR_INVALID_ARG, "build_bias_from_bool_mask: null pointer");
+  if (!aligned(bias, 16) || !aligned(mask, 16))
+    return fail(EXTKV_ERR_INVALID_ARG, "build_bias_from_bool_mask: bias and mask must be 16-byte aligned");
+  cudaError_t e = launch_mask_bias(bias, mask, n, dtype, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "build_bias_from_bool_mask launch");
+  return EXTKV_OK;
+}
+
 size_t attention_ext_kv_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq,
                                        int64_t D, int dtype) {
   // The decode kernel keeps its plan and its split-unit partials there; the

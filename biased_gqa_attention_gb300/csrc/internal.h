@@ -48,6 +48,7 @@ cudaError_t launch_scatter(void* k_cache, void* v_cache, const void* k_new, cons
 cudaError_t launch_bias(void* bias, const extkv_bias_spec& spec, const int64_t* nonpad, int64_t B,
                         int64_t S_q, int64_t max_seq, int dtype, int32_t* status,
                         cudaStream_t stream);
+cudaError_t launch_mask_bias(void* bias, const uint8_t* mask, int64_t n, int dtype, cudaStream_t stream);
 cudaError_t launch_attn_generic(const AttnArgs& a, const char** name);
 
 // Fast paths: `supported` says whether the shape can run; launch returns the error.

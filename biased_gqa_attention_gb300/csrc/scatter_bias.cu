@@ -184,4 +184,55 @@ cudaError_t launch_bias(void* bias, const extkv_bias_spec& s, const int64_t* non
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// ---- a boolean attention mask as the additive bias ------------------------
+// "ONNX Domain Attention (Opset 23/24) CUDA Patterns", section 6 (additive-bias
+// path: a bool mask is converted to a bias) and the attention-mask skill ("Bool
+// mask vs float additive bias"): an attended slot (mask byte != 0) gets 0, a
+// masked slot lowest(T), the same sentinel the bias builder writes.  16 mask
+// bytes per step (one 16-byte load) become 16 elements (two or four 16-byte
+// stores); a ragged tail of fewer than 16 elements is done element by element.
+template <typename T>
+__global__ void __launch_bounds__(256) mask_bias_kernel(T* __restrict__ bias, const uint8_t* __restrict__ mask,
+                                                        int64_t n) {
+  ptx::grid_dependency_wait();
+  ptx::grid_launch_dependents();
+  const T low = Elem<T>::from_float(Elem<T>::lowest());
+  const T zero = Elem<T>::from_float(0.f);
+  const int64_t nv = n / 16;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < nv; v += stride) {
+    const uint4 m = __ldg(reinterpret_cast<const uint4*>(mask) + v);
+    const uint8_t* mb = reinterpret_cast<const uint8_t*>(&m);
+    constexpr int kPerVec = 16 / sizeof(T);  // elements per 16-byte store
+    uint4* out = reinterpret_cast<uint4*>(bias + v * 16);
+#pragma unroll
+    for (int q = 0; q < 16 / kPerVec; ++q) {
+      union {
+        uint4 u;
+        T e[kPerVec];
+      } w;
+#pragma unroll
+      for (int e = 0; e < kPerVec; ++e) w.e[e] = mb[q * kPerVec + e] ? zero : low;
+      out[q] = w.u;
+    }
+  }
+  for (int64_t i = nv * 16 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    bias[i] = mask[i] ? zero : low;
+}
+
+cudaError_t launch_mask_bias(void* bias, const uint8_t* mask, int64_t n, int dtype, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t want = (n / 16 + threads - 1) / threads;
+  const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(num_sms()) * 8)));
+  cudaLaunchConfig_t cfg = pdl_config(blocks, threads, stream);
+  cudaLaunchAttribute attr[1];
+  pdl_attr(cfg, attr);
+  cudaError_t e = dtype == EXTKV_F32
+                      ? cudaLaunchKernelEx(&cfg, mask_bias_kernel<float>, static_cast<float*>(bias), mask, n)
+                      : cudaLaunchKernelEx(&cfg, mask_bias_kernel<__nv_bfloat16>,
+                                           static_cast<__nv_bfloat16*>(bias), mask, n);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 }  // namespace extkv

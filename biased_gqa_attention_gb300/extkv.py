@@ -23,7 +23,8 @@ ALGO_AUTO, ALGO_GENERIC, ALGO_DECODE, ALGO_PREFILL = 0, 1, 2, 3
 
 # Every symbol include/extkv.h declares.
 SYMBOLS = ("ext_kv_scatter", "build_static_cache_bias", "attention_ext_kv_workspace_size",
-           "attention_ext_kv", "attention_ext_kv_scatter", "extkv_clear_status", "extkv_read_status",
+           "attention_ext_kv", "attention_ext_kv_scatter", "build_bias_from_bool_mask",
+           "extkv_clear_status", "extkv_read_status",
            "extkv_last_error", "extkv_last_kernel", "extkv_last_launches", "extkv_set_algo",
            "attention_ext_kv_noalloc")
 
@@ -54,6 +55,7 @@ def load(path: str = LIB_PATH):
     P, I64, I, I32P = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
     lib.ext_kv_scatter.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I, I32P, P]
     lib.build_static_cache_bias.argtypes = [P, ctypes.POINTER(_BiasSpec), P, I64, I64, I64, I, I32P, P]
+    lib.build_bias_from_bool_mask.argtypes = [P, P, I64, I64, I64, I, P]
     lib.attention_ext_kv_workspace_size.argtypes = [I64, I64, I64, I64, I64, I64, I]
     lib.attention_ext_kv_workspace_size.restype = ctypes.c_size_t
     lib.attention_ext_kv.argtypes = [P, P, P, P, P, ctypes.POINTER(_BiasSpec), P, ctypes.c_float,
@@ -194,6 +196,18 @@ def attention_ext_kv(y, q, k_cache, v_cache, nonpad, scale, bias=None, fused: Op
                                    None if c is None else ctypes.byref(c), _p(nonpad), float(scale),
                                    B, Hq, Hkv, S_q, max_seq, D, _dt(q), _p(workspace), ws, _p(status),
                                    _stream(stream)))
+
+
+def build_bias_from_bool_mask(bias, mask, stream=None):
+    """Writes the additive bias of a boolean (B,1,S_q,max_seq) mask into ``bias``
+    (same shape, float32 or bfloat16): 0 where the mask is true, the element
+    type's lowest finite value where it is false."""
+    _need(bias, "bias", dims=4)
+    _need(mask, "mask", dims=4, dtype=torch.bool)
+    if mask.shape != bias.shape or bias.shape[1] != 1:
+        raise ValueError("mask and bias must both be (B,1,S_q,max_seq)")
+    B, _, S_q, max_seq = bias.shape
+    _check(load().build_bias_from_bool_mask(_p(bias), _p(mask), B, S_q, max_seq, _dt(bias), _stream(stream)))
 
 
 def attention_ext_kv_scatter(y, q, k_cache, v_cache, k_new, v_new, write_idx, nonpad, scale, bias=None,

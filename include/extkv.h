@@ -124,6 +124,23 @@ int build_static_cache_bias(void *bias, const extkv_bias_spec *spec, const int64
                             int32_t *status, void *stream);
 
 /*
+ * A boolean attention mask as the additive bias that attention_ext_kv takes
+ * ("ONNX Domain Attention (Opset 23/24) CUDA Patterns", section 6: the bool
+ * mask is converted to an additive bias; the attention-mask skill, "Bool mask
+ * vs float additive bias": both represent any pattern).  mask: (B,1,S_q,max_seq)
+ * bytes, nonzero = attend; bias: (B,1,S_q,max_seq) of T, written 0 where the
+ * mask is set and lowest(T) (the sentinel of build_static_cache_bias) where it
+ * is not.  Bit-exact.  Both 16-byte aligned.  Slots at or beyond nonpad[b] stay
+ * masked by attention_ext_kv whatever the mask says; a mask that already
+ * applies causal masking must not be combined with a causal fused spec (the
+ * pages warn against applying causal twice).  A maskless causal layer
+ * (is_causal = 1 with nonpad, no mask) needs no bias at all: pass the fused
+ * spec {causal = 1, window = 0} to attention_ext_kv.
+ */
+int build_bias_from_bool_mask(void *bias, const uint8_t *mask, int64_t B, int64_t S_q, int64_t max_seq,
+                              int dtype, void *stream);
+
+/*
  * Bytes of device workspace attention_ext_kv needs for these sizes on the
  * current device: enough for whichever kernel runs, chosen automatically or
  * by extkv_set_algo.  The decode path keeps its live-tile plan and the
