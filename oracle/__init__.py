@@ -64,6 +64,9 @@ def _load():
             lib.oracle_attention.argtypes = [P, P, P, P, P, P, ctypes.c_float, I64, I64, I64,
                                              I64, I64, I64, I, P, I64]
             lib.oracle_attention.restype = I64
+            lib.oracle_attention_softcap.argtypes = [P, P, P, P, P, P, ctypes.c_float, ctypes.c_float, I64,
+                                                     I64, I64, I64, I64, I64, I, P, I64]
+            lib.oracle_attention_softcap.restype = I64
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = I
             _lib = lib
@@ -157,9 +160,10 @@ def bias_from_mask(mask, dt):
     return out
 
 
-def attention(q, k_cache, v_cache, bias_, nonpad, scale, rows=None):
+def attention(q, k_cache, v_cache, bias_, nonpad, scale, rows=None, softcap=0.0):
     """fp64 attention output.  q (B,Hq,S_q,D), caches (B,Hkv,max_seq,D),
-    ``bias_`` None or (B,1,S_q,max_seq), all in one element type.
+    ``bias_`` None or (B,1,S_q,max_seq), all in one element type.  ``softcap``
+    > 0 caps the scaled scores, cap * tanh(x / cap), before the bias.
 
     With ``rows`` (flat indices (b*Hq+h)*S_q+i) only those rows are computed
     and the result is (len(rows), D); otherwise it is (B,Hq,S_q,D).
@@ -175,8 +179,9 @@ def attention(q, k_cache, v_cache, bias_, nonpad, scale, rows=None):
     r = _c(rows, np.int64)
     n = B * Hq * S_q if r is None else r.shape[0]
     y = np.zeros((n, D), np.float64)
-    _load().oracle_attention(_ptr(y), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(b_), _ptr(np_),
-                             float(scale), B, Hq, Hkv, S_q, max_seq, D, DTYPES[dt], _ptr(r), n)
+    _load().oracle_attention_softcap(_ptr(y), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(b_), _ptr(np_),
+                                     float(scale), float(softcap), B, Hq, Hkv, S_q, max_seq, D, DTYPES[dt],
+                                     _ptr(r), n)
     return y.reshape(B, Hq, S_q, D) if r is None else y
 
 

@@ -194,15 +194,16 @@ void oracle_bias_from_mask(void *bias, const unsigned char *mask, int64_t n, int
  *              bias is above the sentinel; a finite very negative bias stays
  *              unmasked)
  *   U empty  -> y = 0                ([ORT] section 6, rows and whole batches)
- *   s_j      = scale * (q . k_j) + bias_j         ([ORT] section 4 op order,
- *                                                  softcap off)
+ *   s_j      = c(scale * (q . k_j)) + bias_j      ([ORT] section 4 op order:
+ *              c(x) = cap * tanh(x / cap) when the softcap cap > 0, else x;
+ *              the cap acts before the bias, so a masked slot stays masked)
  *   y        = sum_{j in U} exp(s_j - m) v_j / sum_{j in U} exp(s_j - m),
  *              m = max_{j in U} s_j  (max-subtracted softmax, [ORT] section 8)
  * Without a bias, U = { j < nonpad[b] } and bias_j = 0.
  * Returns 0, or 1 when nonpad[b] is outside [0,max_seq] (the row is zeroed).
  */
 static int orc_row(double *y, const void *q, const void *k_cache, const void *v_cache,
-                   const void *bias, const int64_t *nonpad, double scale, int64_t Hq,
+                   const void *bias, const int64_t *nonpad, double scale, double softcap, int64_t Hq,
                    int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t D, int dt, int64_t b,
                    int64_t h, int64_t i, double *s, unsigned char *in_u) {
   int64_t np = nonpad[b];
@@ -221,7 +222,9 @@ static int orc_row(double *y, const void *q, const void *k_cache, const void *v_
     double dot = 0.0;
     for (int64_t d = 0; d < D; ++d)
       dot += orc_load(q, q_off + d, dt) * orc_load(k_cache, (kv_base + j) * D + d, dt);
-    s[j] = scale * dot + bj;
+    double t = scale * dot;
+    if (softcap > 0.0) t = softcap * tanh(t / softcap);
+    s[j] = t + bj;
     if (!any || s[j] > m) m = s[j];
     any = 1;
   }
@@ -245,10 +248,10 @@ static int orc_row(double *y, const void *q, const void *k_cache, const void *v_
  * no preceding scatter.  Returns the number of rows whose batch had an
  * out-of-range nonpad.
  */
-int64_t oracle_attention(double *y, const void *q, const void *k_cache, const void *v_cache,
-                         const void *bias, const int64_t *nonpad, float scale, int64_t B,
-                         int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t D, int dt,
-                         const int64_t *rows, int64_t n_rows) {
+int64_t oracle_attention_softcap(double *y, const void *q, const void *k_cache, const void *v_cache,
+                                 const void *bias, const int64_t *nonpad, float scale, float softcap,
+                                 int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t D,
+                                 int dt, const int64_t *rows, int64_t n_rows) {
   int64_t total = rows ? n_rows : B * Hq * S_q;
   int64_t bad = 0;
 #pragma omp parallel reduction(+ : bad)
@@ -260,13 +263,22 @@ int64_t oracle_attention(double *y, const void *q, const void *k_cache, const vo
       int64_t r = rows ? rows[t] : t;
       int64_t i = r % S_q, bh = r / S_q;
       int64_t h = bh % Hq, b = bh / Hq;
-      bad += orc_row(y + t * D, q, k_cache, v_cache, bias, nonpad, (double)scale, Hq, Hkv, S_q,
-                     max_seq, D, dt, b, h, i, s, in_u);
+      bad += orc_row(y + t * D, q, k_cache, v_cache, bias, nonpad, (double)scale, (double)softcap, Hq, Hkv,
+                     S_q, max_seq, D, dt, b, h, i, s, in_u);
     }
     free(s);
     free(in_u);
   }
   return bad;
+}
+
+/* The attention without a softcap. */
+int64_t oracle_attention(double *y, const void *q, const void *k_cache, const void *v_cache,
+                         const void *bias, const int64_t *nonpad, float scale, int64_t B,
+                         int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t D, int dt,
+                         const int64_t *rows, int64_t n_rows) {
+  return oracle_attention_softcap(y, q, k_cache, v_cache, bias, nonpad, scale, 0.0f, B, Hq, Hkv, S_q, max_seq, D,
+                                  dt, rows, n_rows);
 }
 
 int oracle_num_threads(void) {

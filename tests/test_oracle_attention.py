@@ -256,3 +256,79 @@ def test_row_subset_matches_full_and_threads_do_not_change_bits():
     rows = np.array([0, 5, 17, 47, 23], np.int64)
     ys = oracle.attention(q, k, v, bias, nonpad, 0.3, rows=rows)
     assert ys.tobytes() == y.reshape(-1, 8)[rows].tobytes()
+
+
+# ---- softcap: cap * tanh(x / cap) on the scaled scores, before the bias -------
+# "ONNX Domain Attention (Opset 23/24) CUDA Patterns", section 4 (op order:
+# scale, softcap, + bias / mask, softmax).
+
+def _softcap_case(dt, seed=3):
+    rng = np.random.default_rng(seed)
+    B, Hq, Hkv, S_q, max_seq, D = 2, 4, 2, 3, 40, 16
+    q = _rand((B, Hq, S_q, D), dt, rng)
+    k = _rand((B, Hkv, max_seq, D), dt, rng)
+    v = _rand((B, Hkv, max_seq, D), dt, rng)
+    nonpad = np.array([40, 23], np.int64)
+    return q, k, v, nonpad, 1.0 / np.sqrt(D)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_softcap_large_cap_converges_to_no_cap_within_the_taylor_bound(dt):
+    """cap * tanh(x / cap) = x - x^3 / (3 cap^2) + ..., so with |x| <= X the
+    scores move by at most X^3 / (3 cap^2) and the output by less than
+    2 * max|v| * (exp(2 delta) - 1)."""
+    q, k, v, nonpad, scale = _softcap_case(dt)
+    b, _ = oracle.bias(nonpad, 3, 40, dt, causal=True, window=0)
+    cap = 200.0
+    qf, kf = oracle.to_f64(q), oracle.to_f64(k)
+    X = scale * np.abs(np.einsum("bhsd,bkjd->bhskj", qf, kf)).max()
+    delta = X ** 3 / (3 * cap ** 2)
+    y0 = oracle.attention(q, k, v, b, nonpad, scale)
+    y1 = oracle.attention(q, k, v, b, nonpad, scale, softcap=cap)
+    bound = 2 * np.abs(oracle.to_f64(v)).max() * (np.exp(2 * delta) - 1)
+    assert 0 < np.abs(y1 - y0).max() <= bound
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_softcap_before_the_bias_keeps_softmax_shift_invariance(dt):
+    """Adding one constant to every allowed bias entry of a row leaves the
+    output unchanged only if the cap acts before the bias (with the cap after
+    it, tanh would see the shifted scores)."""
+    q, k, v, nonpad, scale = _softcap_case(dt)
+    rng = np.random.default_rng(9)
+    ex = (np.round(np.clip(rng.standard_normal((2, 1, 3, 40)), -3, 3) * 4) / 4).astype(np.float32)  # exact in bf16, +1.5 too
+    extra = ex if dt == "f32" else (ex.view(np.uint32) >> 16).astype(np.uint16)
+    b, _ = oracle.bias(nonpad, 3, 40, dt, causal=True, window=0, extra=extra)
+    b2, _ = oracle.bias(nonpad, 3, 40, dt, causal=True, window=0,
+                        extra=(ex + 1.5) if dt == "f32" else ((ex + 1.5).view(np.uint32) >> 16).astype(np.uint16))
+    for cap in (1.0, 3.0):
+        y1 = oracle.attention(q, k, v, b, nonpad, scale, softcap=cap)
+        y2 = oracle.attention(q, k, v, b2, nonpad, scale, softcap=cap)
+        assert np.abs(y1 - y2).max() <= 1e-12
+    assert np.abs(oracle.attention(q, k, v, b, nonpad, scale, softcap=1.0) -
+                  oracle.attention(q, k, v, b, nonpad, scale)).max() > 1e-3  # the cap does act
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_softcap_single_key_and_poison_under_the_mask(dt):
+    """One unmasked key: y is its value row, whatever the cap.  A tiny cap with
+    NaN V rows under masked slots (the pages' guard case): the masked slots
+    stay out of the softmax, the output is finite and equals the output
+    without the poison."""
+    q, k, v, nonpad, scale = _softcap_case(dt)
+    b, _ = oracle.bias(nonpad, 3, 40, dt, causal=True, window=1)  # each row: its own key only
+    y = oracle.attention(q, k, v, b, nonpad, scale, softcap=0.5)
+    vf = oracle.to_f64(v)
+    for bb in range(2):
+        qs = max(int(nonpad[bb]) - 3, 0)
+        for h in range(4):
+            for i in range(3):
+                assert np.array_equal(y[bb, h, i], vf[bb, h // 2, qs + i])
+    bw, _ = oracle.bias(nonpad, 3, 40, dt, causal=True, window=8)
+    vp = v.copy()
+    nan = np.float32(np.nan) if dt == "f32" else np.uint16(0x7FC0)
+    for bb in range(2):  # every slot before the first row's window (query 0 at nonpad - 3)
+        vp[bb, :, :max(int(nonpad[bb]) - 3 - 8 + 1, 0)] = nan
+    y0 = oracle.attention(q, k, v, bw, nonpad, scale, softcap=0.05)
+    yp = oracle.attention(q, k, vp, bw, nonpad, scale, softcap=0.05)
+    assert np.isfinite(yp).all() and np.array_equal(y0, yp)

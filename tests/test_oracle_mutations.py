@@ -16,8 +16,11 @@ SRC = os.path.join(ROOT, "oracle", "extkv_oracle.c")
 
 MUTATIONS = {
     "gqa_head_map": ("int64_t kv = h / (Hq / Hkv);", "int64_t kv = h % Hkv;"),
-    "scale_dropped": ("s[j] = scale * dot + bj;", "s[j] = dot + bj;"),
-    "bias_dropped": ("s[j] = scale * dot + bj;", "s[j] = scale * dot;"),
+    "scale_dropped": ("double t = scale * dot;", "double t = dot;"),
+    "bias_dropped": ("s[j] = t + bj;", "s[j] = t;"),
+    "softcap_after_bias": ("if (softcap > 0.0) t = softcap * tanh(t / softcap);\n    s[j] = t + bj;",
+                           "s[j] = t + bj;\n    if (softcap > 0.0) s[j] = softcap * tanh(s[j] / softcap);"),
+    "softcap_unscaled": ("t = softcap * tanh(t / softcap);", "t = tanh(t / softcap);"),
     "sentinel_inclusive": ("in_u[j] = (unsigned char)(!bias || bj > lowest);",
                            "in_u[j] = (unsigned char)(!bias || bj >= lowest);"),
     "window_off_by_one": ("p - j < window", "p - j <= window"),
