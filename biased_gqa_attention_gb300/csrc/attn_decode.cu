@@ -108,6 +108,7 @@ struct DecodeParams {
   BiasSpec spec;
   const int64_t* nonpad;
   float scale;
+  float softcap;  // > 0: scores capped before the bias
   int B, Hq, Hkv, S_q, g, R, D;
   int max_seq, max_tiles;
   int G;     // CTAs of the decode grid
@@ -385,7 +386,9 @@ struct Cursor {
   int b, kvh, kk, cnt;
 };
 
-template <int D, int SPW, int MODE>
+// CAP: the scores are softcapped (a separate instantiation, so that the
+// uncapped kernel is compiled as if the cap did not exist).
+template <int D, int SPW, int MODE, bool CAP>
 __global__ void __launch_bounds__(32) attn_decode_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap tmap,
@@ -755,8 +758,18 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
         for (int e = 0; e < 4; ++e) live[e] = live[e] && bv[e] > lowest;
       }
     }
+    if constexpr (CAP) {
+      // softcap on the scaled score, before the bias ("ONNX Domain Attention
+      // (Opset 23/24) CUDA Patterns", section 4 op order)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) s[e] = live[e] ? fmaf(s[e], sl2, bv[e] * kLog2e) : -INFINITY;
+      for (int e = 0; e < 4; ++e) {
+        const float x = p.softcap * tanhf(s[e] * p.scale / p.softcap);
+        s[e] = live[e] ? (x + bv[e]) * kLog2e : -INFINITY;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[e] = live[e] ? fmaf(s[e], sl2, bv[e] * kLog2e) : -INFINITY;
+    }
 
     // Keys no row attends: zero their V rows (poison must not reach PV).
     const unsigned da = __ballot_sync(0xffffffffu, !live[0] && !live[1]);
@@ -939,7 +952,7 @@ int persistent_grid(int64_t items_max) {
   {
     std::lock_guard<std::mutex> g(mu);
     if (cached_dev != dev) {
-      auto kern = attn_decode_kernel<D, Cfg::SPW, kBias>;
+      auto kern = attn_decode_kernel<D, Cfg::SPW, kBias, false>;
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(S::bytes()));
       int o = 0;
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, 32, S::bytes()) != cudaSuccess || o <= 0) {
@@ -976,7 +989,7 @@ int mode_of(const AttnArgs& a) {
   return a.extra ? kFusedExtra : kFused;
 }
 
-template <int D, int MODE>
+template <int D, int MODE, bool CAP>
 cudaError_t launch_dm(const AttnArgs& a, const DecodeParams& prm, const CUtensorMap& kmap,
                       const CUtensorMap& vmap, const CUtensorMap& qmap, const CUtensorMap& tmap,
                       int64_t max_tiles) {
@@ -1001,7 +1014,7 @@ cudaError_t launch_dm(const AttnArgs& a, const DecodeParams& prm, const CUtensor
     e = cudaLaunchKernelEx(&cfg, pk, prm);
     if (e != cudaSuccess) return e;
   }
-  auto kern = attn_decode_kernel<D, Cfg::SPW, MODE>;
+  auto kern = attn_decode_kernel<D, Cfg::SPW, MODE, CAP>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(S::bytes()));
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(static_cast<unsigned>(prm.G));
@@ -1018,6 +1031,13 @@ cudaError_t launch_dm(const AttnArgs& a, const DecodeParams& prm, const CUtensor
   e = cudaLaunchKernelEx(&cfg, decode_merge_kernel<MODE>, prm);
   if (e == cudaSuccess) note_launches(prm.plan ? 3 : 2);
   return e;
+}
+
+template <int D, int MODE>
+cudaError_t launch_dmc(const AttnArgs& a, const DecodeParams& prm, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                       const CUtensorMap& qmap, const CUtensorMap& tmap, int64_t max_tiles) {
+  return a.softcap > 0.f ? launch_dm<D, MODE, true>(a, prm, kmap, vmap, qmap, tmap, max_tiles)
+                         : launch_dm<D, MODE, false>(a, prm, kmap, vmap, qmap, tmap, max_tiles);
 }
 
 template <int D>
@@ -1063,6 +1083,7 @@ cudaError_t launch_d(const AttnArgs& a, const char** name) {
   prm.spec = BiasSpec{a.causal, a.window, a.span_offsets, a.spans, a.extra, a.q_start};
   prm.nonpad = a.nonpad;
   prm.scale = a.scale;
+  prm.softcap = a.softcap;
   prm.B = static_cast<int>(a.B);
   prm.Hq = static_cast<int>(a.Hq);
   prm.Hkv = static_cast<int>(a.Hkv);
@@ -1088,10 +1109,10 @@ cudaError_t launch_d(const AttnArgs& a, const char** name) {
 
   cudaError_t e;
   switch (mode_of(a)) {
-    case kNone: e = launch_dm<D, kNone>(a, prm, kmap, vmap, qmap, tmap, max_tiles); break;
-    case kBias: e = launch_dm<D, kBias>(a, prm, kmap, vmap, qmap, tmap, max_tiles); break;
-    case kFused: e = launch_dm<D, kFused>(a, prm, kmap, vmap, qmap, tmap, max_tiles); break;
-    default: e = launch_dm<D, kFusedExtra>(a, prm, kmap, vmap, qmap, tmap, max_tiles); break;
+    case kNone: e = launch_dmc<D, kNone>(a, prm, kmap, vmap, qmap, tmap, max_tiles); break;
+    case kBias: e = launch_dmc<D, kBias>(a, prm, kmap, vmap, qmap, tmap, max_tiles); break;
+    case kFused: e = launch_dmc<D, kFused>(a, prm, kmap, vmap, qmap, tmap, max_tiles); break;
+    default: e = launch_dmc<D, kFusedExtra>(a, prm, kmap, vmap, qmap, tmap, max_tiles); break;
   }
   if (e != cudaSuccess) return e;
   *name = prm.k_new ? "attn_decode_streamk_mma_scatter" : "attn_decode_streamk_mma";

@@ -25,7 +25,7 @@ template <typename T, int DPL>
 __global__ void __launch_bounds__(32 * kWarps) attn_generic_kernel(
     T* __restrict__ y, const T* __restrict__ q, const T* __restrict__ k_cache,
     const T* __restrict__ v_cache, const T* __restrict__ bias, BiasSpec spec, int fused,
-    const int64_t* __restrict__ nonpad, float scale, int64_t Hq, int64_t Hkv, int64_t S_q,
+    const int64_t* __restrict__ nonpad, float scale, float softcap, int64_t Hq, int64_t Hkv, int64_t S_q,
     int64_t max_seq, int D, int64_t rows, int32_t* status) {
   using E = Elem<T>;
   const int lane = threadIdx.x & 31;
@@ -103,7 +103,8 @@ __global__ void __launch_bounds__(32 * kWarps) attn_generic_kernel(
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-        const float s = fmaf(scale, part, bb);
+        // softcap (if > 0) on the scaled score, before the bias (section 4 op order)
+        const float s = softcap > 0.f ? fmaf(softcap, tanhf(scale * part / softcap), bb) : fmaf(scale, part, bb);
         const float m_new = fmaxf(m, s);
         // Differences are formed before any scaling, so an extreme finite
         // score can never overflow to -inf and be mistaken for a mask.
@@ -134,7 +135,7 @@ void launch_dpl(const AttnArgs& a, int blocks, const BiasSpec& spec, int64_t row
   attn_generic_kernel<T, DPL><<<blocks, 32 * kWarps, 0, a.stream>>>(
       static_cast<T*>(a.y), static_cast<const T*>(a.q), static_cast<const T*>(a.k_cache),
       static_cast<const T*>(a.v_cache), static_cast<const T*>(a.bias), spec, a.fused, a.nonpad,
-      a.scale, a.Hq, a.Hkv, a.S_q, a.max_seq, static_cast<int>(a.D), rows, a.status);
+      a.scale, a.softcap, a.Hq, a.Hkv, a.S_q, a.max_seq, static_cast<int>(a.D), rows, a.status);
 }
 
 template <typename T>

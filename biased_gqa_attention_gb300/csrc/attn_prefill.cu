@@ -123,6 +123,8 @@ struct PrefillParams {
   const uint64_t* colmask;  // bias / extra-term modes: per (b, query tile, 64-key tile) live columns
   BiasSpec spec;
   float scale_log2;  // scale * log2(e)
+  float scale;
+  float softcap;     // > 0: scores capped to softcap * tanh(score / softcap) before the bias
   int B, Hq, Hkv, S_q, max_seq, n_pt, n_tiles;  // n_tiles: 64-key words per colmask row
   int32_t* status;
 };
@@ -362,6 +364,27 @@ __device__ __forceinline__ void half_scores(float (&t)[kBN], const uint32_t (&sa
   }
 }
 
+// The same with the softcap of the ORT page's section 4 op order: the scaled
+// score x = scale*s becomes cap*tanh(x/cap) before the term is added.
+template <int H, bool TERM, bool PARTIAL>
+__device__ __forceinline__ void half_scores_capped(float (&t)[kBN], const uint32_t (&sa)[32], const uint32_t (&sb)[32],
+                                                   const uint32_t (&tw)[32], uint64_t allowed, float scale, float cap,
+                                                   float lowest) {
+#pragma unroll
+  for (int c = 0; c < 64; ++c) {
+    const uint32_t sv = c < 32 ? sa[c] : sb[c - 32];
+    bool ok = true;
+    float b = 0.f;
+    if (TERM) {
+      b = __uint_as_float((c & 1) ? (tw[c >> 1] & 0xFFFF0000u) : (tw[c >> 1] << 16));
+      ok = b > lowest;
+    }
+    if (PARTIAL) ok = ok && ((allowed >> c) & 1);
+    const float x = cap * tanhf(__uint_as_float(sv) * scale / cap);
+    t[64 * H + c] = ok ? (x + b) * kLog2e : -INFINITY;
+  }
+}
+
 __device__ __forceinline__ float tile_max(const float (&t)[kBN]) {
   float acc[8];
 #pragma unroll
@@ -391,7 +414,9 @@ __device__ __forceinline__ void load_swizzled_row(uint32_t (&w)[32], const uint8
 
 // ---- the attention kernel ---------------------------------------------------------
 
-template <int D, int MODE>
+// CAP: the scores are softcapped (a separate instantiation, so that the
+// uncapped kernel is compiled as if the cap did not exist).
+template <int D, int MODE, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap tmap,
@@ -667,6 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- softmax and epilogue (one query row per thread) ----------------
     const uint32_t tl = tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
     const float sl2 = p.scale_log2;
+    constexpr bool capped = CAP;
     const float lowest = Elem<__nv_bfloat16>::lowest();
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
@@ -733,10 +759,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_ld32(ts + 32, sb);
         if (C::kTerm) load_swizzled_row(tw, tblk, row);
         ptx::tmem_wait_ld();
-        if (part0)
+        if constexpr (capped) {
+          if (part0)
+            half_scores_capped<0, C::kTerm, true>(t, sa, sb, tw, al0, p.scale, p.softcap, lowest);
+          else
+            half_scores_capped<0, C::kTerm, false>(t, sa, sb, tw, al0, p.scale, p.softcap, lowest);
+        } else if (part0) {
           half_scores<0, C::kTerm, true>(t, sa, sb, tw, al0, sl2, lowest);
-        else
+        } else {
           half_scores<0, C::kTerm, false>(t, sa, sb, tw, al0, sl2, lowest);
+        }
         ptx::tmem_ld32(ts + 64, sa);
         ptx::tmem_ld32(ts + 96, sb);
         if (C::kTerm) {
@@ -745,10 +777,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) ptx::mbar_arrive(&bar.t_empty[tb]);
         }
         ptx::tmem_wait_ld();
-        if (part1)
+        if constexpr (capped) {
+          if (part1)
+            half_scores_capped<1, C::kTerm, true>(t, sa, sb, tw, al1, p.scale, p.softcap, lowest);
+          else
+            half_scores_capped<1, C::kTerm, false>(t, sa, sb, tw, al1, p.scale, p.softcap, lowest);
+        } else if (part1) {
           half_scores<1, C::kTerm, true>(t, sa, sb, tw, al1, sl2, lowest);
-        else
+        } else {
           half_scores<1, C::kTerm, false>(t, sa, sb, tw, al1, sl2, lowest);
+        }
       }
       const float mt = tile_max(t);
       // lazy rescale: only when the running maximum grows by more than 2^8
@@ -870,13 +908,13 @@ int n_plan_chunks(int64_t max_seq) { return static_cast<int>((max_seq + kPlanKey
 // the plan's column-mask table: one 64-bit word per 64 keys
 int n_mask_words(int64_t max_seq) { return static_cast<int>((max_seq + 63) / 64); }
 
-template <int D, int MODE>
+template <int D, int MODE, bool CAP>
 cudaError_t launch_dm(const AttnArgs& a, const char** name) {
   using C = Cfg<D, MODE>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_prefill_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(attn_prefill_kernel<D, MODE, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     C::kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
@@ -917,6 +955,8 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
   prm.colmask = static_cast<const uint64_t*>(a.workspace);
   prm.spec = BiasSpec{a.causal, a.window, a.span_offsets, a.spans, a.extra, a.q_start};
   prm.scale_log2 = a.scale * kLog2e;
+  prm.scale = a.scale;
+  prm.softcap = a.softcap;
   prm.B = static_cast<int>(a.B);
   prm.Hq = static_cast<int>(a.Hq);
   prm.Hkv = static_cast<int>(a.Hkv);
@@ -958,18 +998,23 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_prefill_kernel<D, MODE>, qmap, kmap, vmap, tmap, prm);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_prefill_kernel<D, MODE, CAP>, qmap, kmap, vmap, tmap, prm);
   if (e != cudaSuccess) return e;
   *name = "attn_prefill_tcgen05";
   note_launches(C::kTerm ? 2 : 1);  // the plan kernel, then the attention kernel
   return cudaGetLastError();
 }
 
+template <int D, bool CAP>
+cudaError_t launch_dc(const AttnArgs& a, const char** name) {
+  if (a.bias) return launch_dm<D, kBias, CAP>(a, name);
+  if (a.fused) return a.extra ? launch_dm<D, kFusedExtra, CAP>(a, name) : launch_dm<D, kFused, CAP>(a, name);
+  return launch_dm<D, kNone, CAP>(a, name);
+}
+
 template <int D>
 cudaError_t launch_d(const AttnArgs& a, const char** name) {
-  if (a.bias) return launch_dm<D, kBias>(a, name);
-  if (a.fused) return a.extra ? launch_dm<D, kFusedExtra>(a, name) : launch_dm<D, kFused>(a, name);
-  return launch_dm<D, kNone>(a, name);
+  return a.softcap > 0.f ? launch_dc<D, true>(a, name) : launch_dc<D, false>(a, name);
 }
 
 }  // namespace

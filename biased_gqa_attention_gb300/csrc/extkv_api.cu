@@ -187,7 +187,7 @@ struct ScatterIn {
 int attention_impl(void* y, const void* q, const void* k_cache, const void* v_cache, const void* bias,
                    const extkv_bias_spec* fused, const int64_t* nonpad, float scale, int64_t B, int64_t Hq,
                    int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t D, int dtype, void* workspace,
-                   size_t ws_bytes, int32_t* status, void* stream, const ScatterIn* sc) {
+                   size_t ws_bytes, int32_t* status, void* stream, const ScatterIn* sc, float softcap = 0.f) {
   if (!valid_dtype(dtype)) return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv: unknown dtype %d", dtype);
   if (B < 0 || S_q < 0 || Hq <= 0 || Hkv <= 0 || max_seq <= 0 || D <= 0)
     return fail(EXTKV_ERR_INVALID_ARG,
@@ -235,6 +235,7 @@ int attention_impl(void* y, const void* q, const void* k_cache, const void* v_ca
   }
   a.nonpad = nonpad;
   a.scale = scale;
+  a.softcap = softcap;
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;
@@ -323,6 +324,18 @@ int attention_ext_kv(void* y, const void* q, const void* k_cache, const void* v_
   g_error[0] = 0;
   return attention_impl(y, q, k_cache, v_cache, bias, fused, nonpad, scale, B, Hq, Hkv, S_q, max_seq, D, dtype,
                         workspace, ws_bytes, status, stream, nullptr);
+}
+
+int attention_ext_kv_softcap(void* y, const void* q, const void* k_cache, const void* v_cache,
+                             const void* bias, const extkv_bias_spec* fused, const int64_t* nonpad,
+                             float scale, float softcap, int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q,
+                             int64_t max_seq, int64_t D, int dtype, void* workspace, size_t ws_bytes,
+                             int32_t* status, void* stream) {
+  g_error[0] = 0;
+  if (!(softcap >= 0.f) || softcap == INFINITY)
+    return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv_softcap: softcap must be finite and >= 0");
+  return attention_impl(y, q, k_cache, v_cache, bias, fused, nonpad, scale, B, Hq, Hkv, S_q, max_seq, D, dtype,
+                        workspace, ws_bytes, status, stream, nullptr, softcap);
 }
 
 int attention_ext_kv_scatter(void* y, const void* q, void* k_cache, void* v_cache, const void* k_new,

@@ -24,6 +24,7 @@ struct AttnArgs {
   int fused;              // evaluate the spec in registers
   const int64_t* nonpad;
   float scale;
+  float softcap;  // > 0: scores capped to softcap * tanh(score / softcap) before the bias
   int64_t B, Hq, Hkv, S_q, max_seq, D;
   int dtype;
   int32_t* status;

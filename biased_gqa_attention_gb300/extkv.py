@@ -23,7 +23,8 @@ ALGO_AUTO, ALGO_GENERIC, ALGO_DECODE, ALGO_PREFILL = 0, 1, 2, 3
 
 # Every symbol include/extkv.h declares.
 SYMBOLS = ("ext_kv_scatter", "build_static_cache_bias", "attention_ext_kv_workspace_size",
-           "attention_ext_kv", "attention_ext_kv_scatter", "build_bias_from_bool_mask",
+           "attention_ext_kv", "attention_ext_kv_scatter", "attention_ext_kv_softcap",
+           "build_bias_from_bool_mask",
            "extkv_clear_status", "extkv_read_status",
            "extkv_last_error", "extkv_last_kernel", "extkv_last_launches", "extkv_set_algo",
            "attention_ext_kv_noalloc")
@@ -56,6 +57,9 @@ def load(path: str = LIB_PATH):
     lib.ext_kv_scatter.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I, I32P, P]
     lib.build_static_cache_bias.argtypes = [P, ctypes.POINTER(_BiasSpec), P, I64, I64, I64, I, I32P, P]
     lib.build_bias_from_bool_mask.argtypes = [P, P, I64, I64, I64, I, P]
+    lib.attention_ext_kv_softcap.argtypes = [P, P, P, P, P, ctypes.POINTER(_BiasSpec), P, ctypes.c_float,
+                                             ctypes.c_float, I64, I64, I64, I64, I64, I64, I, P, ctypes.c_size_t,
+                                             I32P, P]
     lib.attention_ext_kv_workspace_size.argtypes = [I64, I64, I64, I64, I64, I64, I]
     lib.attention_ext_kv_workspace_size.restype = ctypes.c_size_t
     lib.attention_ext_kv.argtypes = [P, P, P, P, P, ctypes.POINTER(_BiasSpec), P, ctypes.c_float,
@@ -172,8 +176,10 @@ def new_workspace(q: torch.Tensor, k_cache: torch.Tensor) -> Optional[torch.Tens
 
 
 def attention_ext_kv(y, q, k_cache, v_cache, nonpad, scale, bias=None, fused: Optional[BiasSpec] = None,
-                     workspace=None, status=None, stream=None):
-    """Y = softmax(scale*QK^T + bias)V over the external cache; writes ``y`` (B,Hq,S_q,D).
+                     workspace=None, status=None, stream=None, softcap: float = 0.0):
+    """Y = softmax(cap(scale*QK^T) + bias)V over the external cache; writes ``y`` (B,Hq,S_q,D).
+    ``softcap`` > 0 caps the scaled scores to softcap*tanh(x/softcap) before the
+    bias (attention_ext_kv_softcap); 0 is plain attention_ext_kv.
 
     ``workspace`` (uint8 device tensor of attention_ext_kv_workspace_size bytes)
     is allocated here when not given."""
@@ -192,10 +198,13 @@ def attention_ext_kv(y, q, k_cache, v_cache, nonpad, scale, bias=None, fused: Op
         if need:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load().attention_ext_kv(_p(y), _p(q), _p(k_cache), _p(v_cache), _p(bias),
-                                   None if c is None else ctypes.byref(c), _p(nonpad), float(scale),
-                                   B, Hq, Hkv, S_q, max_seq, D, _dt(q), _p(workspace), ws, _p(status),
-                                   _stream(stream)))
+    args = (_p(y), _p(q), _p(k_cache), _p(v_cache), _p(bias), None if c is None else ctypes.byref(c), _p(nonpad),
+            float(scale))
+    tail = (B, Hq, Hkv, S_q, max_seq, D, _dt(q), _p(workspace), ws, _p(status), _stream(stream))
+    if softcap:
+        _check(load().attention_ext_kv_softcap(*args, float(softcap), *tail))
+    else:
+        _check(load().attention_ext_kv(*args, *tail))
 
 
 def build_bias_from_bool_mask(bias, mask, stream=None):

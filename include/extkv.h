@@ -189,6 +189,20 @@ int attention_ext_kv(void *y, const void *q, const void *k_cache, const void *v_
                      int32_t *status, void *stream);
 
 /*
+ * attention_ext_kv with a softcap ("ONNX Domain Attention (Opset 23/24) CUDA
+ * Patterns", section 4 op order): each scaled score x = scale * q.k becomes
+ * softcap * tanh(x / softcap) before the bias is added, so a masked slot stays
+ * masked (its V row never reaches the output).  softcap == 0 is
+ * attention_ext_kv; a negative, NaN or infinite softcap is
+ * EXTKV_ERR_INVALID_ARG.  Every path (decode, prefill, generic) takes it.
+ */
+int attention_ext_kv_softcap(void *y, const void *q, const void *k_cache, const void *v_cache,
+                             const void *bias, const extkv_bias_spec *fused, const int64_t *nonpad,
+                             float scale, float softcap, int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q,
+                             int64_t max_seq, int64_t D, int dtype, void *workspace, size_t ws_bytes,
+                             int32_t *status, void *stream);
+
+/*
  * ext_kv_scatter followed by attention_ext_kv, in one call: the same results
  * (the caches hold the new rows afterwards, bit for bit, and y is what
  * attention_ext_kv gives over the updated caches).  The scatter is the step

@@ -44,7 +44,7 @@ def run_gpu(inp: wl.Inputs, mode: str = "bias", algo: int = ek.ALGO_AUTO, scatte
 
 
 def oracle_path(inp: wl.Inputs, rows=None, mode: str = "bias", scatter: bool = True,
-                k_cache=None, v_cache=None):
+                k_cache=None, v_cache=None, softcap: float = 0.0):
     """The oracle on host copies of the same inputs: scatter, bias, attention.
     ``k_cache``/``v_cache`` optionally replace the workload's caches with numpy
     arrays the oracle produced earlier (never with GPU results)."""
@@ -61,7 +61,7 @@ def oracle_path(inp: wl.Inputs, rows=None, mode: str = "bias", scatter: bool = T
                             spans=spans, extra=extra)
     assert bad == 0
     y = oracle.attention(raw(inp.q), kc, vc, bias if mode != "none" else None, nonpad,
-                         np.float32(w.scale), rows=rows)
+                         np.float32(w.scale), rows=rows, softcap=softcap)
     return dict(k=kc, v=vc, bias=bias, y=y)
 
 
