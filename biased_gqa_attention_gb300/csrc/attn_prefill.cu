@@ -91,6 +91,7 @@ struct Cfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kQBytes;
   static constexpr int kOffT = kOffKV + kNU * kUnitBytes;
+  static_assert(kNU * kUnitBytes >= 4 * (D / 64) * 4096, "the epilogue stages 128 rows x D in the K/V ring");
   static constexpr int kOffBar = kOffT + kTermBufs * kTermBytes;
   static constexpr int kSmem = kOffBar + 512 + 1024;
   // tensor memory: S_0, S_1 at columns 0 and 128 (P_j, bf16, over the first 64
@@ -420,7 +421,7 @@ template <int D, int MODE, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap tmap,
-                        const PrefillParams p) {
+                        const __grid_constant__ CUtensorMap ymap, const PrefillParams p) {
   using C = Cfg<D, MODE>;
   constexpr bool kFusedMode = MODE == kFused || MODE == kFusedExtra;
   extern __shared__ uint8_t smem_raw[];
@@ -868,30 +869,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = false;
     ptx::tc_fence_after();
     const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-    __nv_bfloat16* yrow = p.y + ((static_cast<int64_t>(b) * p.Hq + h) * p.S_q + q0 + row) * D;
+    // The warp's 32 rows go through shared memory (the K/V ring is idle now:
+    // every MMA that read it has completed) in 32 x 64-column blocks with the
+    // 128-byte swizzle, and leave as one TMA store per block; rows beyond S_q
+    // fall outside the (D, S_q, B*Hq) view and are not written.
+    uint8_t* stage = sKV + (warp & 3) * (D / 64) * 4096;
 #pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t o[32];
+    for (int cb = 0; cb < D / 64; ++cb) {
+      uint32_t o[64];
       if (ok && T > 0) {
-        ptx::tmem_ld32(tl + C::kOCol + 32 * c, o);
+        ptx::tmem_ld32(tl + C::kOCol + 64 * cb, *reinterpret_cast<uint32_t(*)[32]>(o));
+        ptx::tmem_ld32(tl + C::kOCol + 64 * cb + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
         ptx::tmem_wait_ld();
       } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0;
+        for (int e = 0; e < 64; ++e) o[e] = 0;
       }
-      if (row_valid && ok) {
-        uint4* dst = reinterpret_cast<uint4*>(yrow + 32 * c);
+      uint8_t* blk = stage + cb * 4096 + lane * 128;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t w[4];
+      for (int q = 0; q < 8; ++q) {
+        uint32_t w[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w[e] = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 2 * e]) * inv,
-                                    __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
-          dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
+        for (int e = 0; e < 4; ++e)
+          w[e] = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 2 * e]) * inv, __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
+        *reinterpret_cast<uint4*>(blk + ((q ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
+    ptx::fence_proxy_async_smem();  // the staged rows, visible to the TMA store
+    __syncwarp();
+    if (ok && lane == 0 && q0 + 32 * (warp & 3) < p.S_q) {  // a box wholly past S_q writes nothing
+      for (int cb = 0; cb < D / 64; ++cb)
+        ptx::tma_store_3d(&ymap, stage + cb * 4096, cb * 64, q0 + 32 * (warp & 3), b * p.Hq + h);
+      ptx::bulk_commit_group();
+      ptx::bulk_wait_read_all();  // shared memory stays valid until the stores have read it
+    }
+    __syncwarp();
   }
   ptx::grid_launch_dependents();
   if (tid == 0 && *abort) report(p.status, EXTKV_DEV_TIMEOUT);
@@ -938,6 +950,14 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
     if (!make_tensor_map_bf16(&qmap, a.q, 3, q_dims, q_strides, q_box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
+  // output view (D, S_q, B*Hq): the epilogue's 32-row x 64-column stores
+  CUtensorMap ymap;
+  const uint64_t y_dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.S_q),
+                              static_cast<uint64_t>(a.B * a.Hq)};
+  const uint64_t y_strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(a.S_q) * D * 2};
+  const uint32_t y_box[3] = {64, 32, 1};
+  if (!make_tensor_map_bf16(&ymap, a.y, 3, y_dims, y_strides, y_box, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   std::memset(&tmap, 0, sizeof tmap);
   const void* term = MODE == kBias ? a.bias : (MODE == kFusedExtra ? a.extra : nullptr);
   if (term) {
@@ -998,7 +1018,7 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_prefill_kernel<D, MODE, CAP>, qmap, kmap, vmap, tmap, prm);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_prefill_kernel<D, MODE, CAP>, qmap, kmap, vmap, tmap, ymap, prm);
   if (e != cudaSuccess) return e;
   *name = "attn_prefill_tcgen05";
   note_launches(C::kTerm ? 2 : 1);  // the plan kernel, then the attention kernel
