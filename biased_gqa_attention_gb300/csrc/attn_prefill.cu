@@ -296,11 +296,13 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_bias_kernel(const _
   if (keys > 0) {
     // whole 16-byte pieces: max_seq % 8 == 0 keeps the rounded row inside the tensor
     const uint32_t row_bytes = static_cast<uint32_t>((keys + 7) / 8) * 16;
-    if (tid == 0) {
-      ptx::mbar_arrive_expect_tx(bar, row_bytes * rows);
-      const __nv_bfloat16* src = bias + (static_cast<int64_t>(b) * S_q + q0) * max_seq + k_begin;
-      for (int r = 0; r < rows; ++r)
-        ptx::bulk_load(rows_s + r * kPlanKeys, src + static_cast<int64_t>(r) * max_seq, row_bytes, bar);
+    // one row copy per thread, issued side by side (a copy costs its issuing
+    // thread a fixed time, so one thread issuing all rows would serialise them)
+    if (tid == 0) ptx::mbar_arrive_expect_tx(bar, row_bytes * rows);
+    __syncthreads();
+    if (tid < rows) {
+      const __nv_bfloat16* src = bias + (static_cast<int64_t>(b) * S_q + q0 + tid) * max_seq + k_begin;
+      ptx::bulk_load(rows_s + tid * kPlanKeys, src, row_bytes, bar);
     }
     ok = ptx::mbar_wait_bounded(bar, 0, kWaitPolls);
     if (!ok && tid == 0) report(status, EXTKV_DEV_TIMEOUT);
