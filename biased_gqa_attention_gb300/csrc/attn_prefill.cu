@@ -66,6 +66,7 @@ constexpr int kPlanKeys = 256;             // keys per plan block (8 per lane)
 constexpr int kPlanThreads = 256;
 constexpr uint32_t kWaitPolls = 1u << 22;  // bounded mbarrier waits
 constexpr int kMaxUnits = 8;
+constexpr int kMaxSplit = 8;               // key splits of a query tile (small grids)
 
 enum Mode { kNone = 0, kBias = 1, kFused = 2, kFusedExtra = 3 };
 
@@ -128,7 +129,17 @@ struct PrefillParams {
   float softcap;     // > 0: scores capped to softcap * tanh(score / softcap) before the bias
   int B, Hq, Hkv, S_q, max_seq, n_pt, n_tiles;  // n_tiles: 64-key words per colmask row
   int32_t* status;
+  // Key splits of a query tile (small grids): CTA split s takes its share of
+  // the tile's KV tiles and writes an fp32 partial row per query row,
+  // part[((b*Hq + h)*n_split + s)*S_q + i][kPartStride(D)] = O[D], max, sum
+  // (max in base-2 units; O and sum relative to it); a merge kernel combines
+  // them.  n_split == 1: the output rows are written directly.
+  int n_split;
+  float* part;
 };
+
+// floats per partial row: O, then max and sum, rounded to 16 bytes
+__host__ __device__ constexpr int part_stride(int D) { return D + 4; }
 
 // Bounded wait that also gives up once another role has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -435,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = &bar.abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.x, pt = blockIdx.y, b = blockIdx.z;
+  const int h = blockIdx.x / p.n_split, sp = blockIdx.x % p.n_split, pt = blockIdx.y, b = blockIdx.z;
   const int g = p.Hq / p.Hkv;
   const int hk = h / g;
   const int q0 = pt * kBM;
@@ -482,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int64_t np64 = p.nonpad[b];
   const bool bad = bad_nonpad(np64, p.max_seq);
-  if (bad && tid == 0 && h == 0 && pt == 0) report(p.status, EXTKV_DEV_BAD_NONPAD);
+  if (bad && tid == 0 && h == 0 && pt == 0 && sp == 0) report(p.status, EXTKV_DEV_BAD_NONPAD);
   const int np = bad ? 0 : static_cast<int>(np64);
   const int64_t qs = bad ? 0 : query_start(p.spec.q_start, b, np64, p.S_q);
   const uint64_t* cmrow = C::kTerm ? p.colmask + (static_cast<int64_t>(b) * p.n_pt + pt) * p.n_tiles : nullptr;
@@ -542,8 +553,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   const int rlo = bar.range_lo, rhi = bar.range_hi;
-  const int t_lo = rlo < rhi ? rlo / kBN : 0;
-  const int T = rlo < rhi ? (rhi + kBN - 1) / kBN - t_lo : 0;  // KV tiles
+  const int t_lo0 = rlo < rhi ? rlo / kBN : 0;
+  const int T0 = rlo < rhi ? (rhi + kBN - 1) / kBN - t_lo0 : 0;  // KV tiles of the query tile
+  // this split's whole tiles (the rows' masks are per key, so a tile range
+  // needs nothing else)
+  const int t_lo = t_lo0 + (T0 * sp) / p.n_split;
+  const int T = (T0 * (sp + 1)) / p.n_split - (T0 * sp) / p.n_split;
   const uint32_t tbase = bar.tmem_base;
 
   if (warp == 0) {
@@ -875,37 +890,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     // every MMA that read it has completed) in 32 x 64-column blocks with the
     // 128-byte swizzle, and leave as one TMA store per block; rows beyond S_q
     // fall outside the (D, S_q, B*Hq) view and are not written.
-    uint8_t* stage = sKV + (warp & 3) * (D / 64) * 4096;
+    if (p.n_split > 1) {
+      // a partial row of this split: unnormalised O, the running max and sum
+      float* prow = p.part + ((static_cast<int64_t>(b * p.Hq + h) * p.n_split + sp) * p.S_q + q0 + row) *
+                                 part_stride(D);
+      const bool live = ok && T > 0;
 #pragma unroll 1
-    for (int cb = 0; cb < D / 64; ++cb) {
-      uint32_t o[64];
-      if (ok && T > 0) {
-        ptx::tmem_ld32(tl + C::kOCol + 64 * cb, *reinterpret_cast<uint32_t(*)[32]>(o));
-        ptx::tmem_ld32(tl + C::kOCol + 64 * cb + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
-        ptx::tmem_wait_ld();
-      } else {
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (live) {
+          ptx::tmem_ld32(tl + C::kOCol + 32 * c, o);
+          ptx::tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int e = 0; e < 64; ++e) o[e] = 0;
+          for (int e = 0; e < 32; ++e) o[e] = 0;
+        }
+        if (row_valid) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(prow + 32 * c + 4 * q) =
+                make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]), __uint_as_float(o[4 * q + 2]),
+                            __uint_as_float(o[4 * q + 3]));
+        }
       }
-      uint8_t* blk = stage + cb * 4096 + lane * 128;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          w[e] = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 2 * e]) * inv, __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
-        *reinterpret_cast<uint4*>(blk + ((q ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      if (row_valid) {
+        prow[D] = live ? m_run : -INFINITY;
+        prow[D + 1] = live ? l_run : 0.f;
       }
+    } else {
+      uint8_t* stage = sKV + (warp & 3) * (D / 64) * 4096;
+#pragma unroll 1
+      for (int cb = 0; cb < D / 64; ++cb) {
+        uint32_t o[64];
+        if (ok && T > 0) {
+          ptx::tmem_ld32(tl + C::kOCol + 64 * cb, *reinterpret_cast<uint32_t(*)[32]>(o));
+          ptx::tmem_ld32(tl + C::kOCol + 64 * cb + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
+          ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) o[e] = 0;
+        }
+        uint8_t* blk = stage + cb * 4096 + lane * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 2 * e]) * inv, __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
+          *reinterpret_cast<uint4*>(blk + ((q ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      ptx::fence_proxy_async_smem();  // the staged rows, visible to the TMA store
+      __syncwarp();
+      if (ok && lane == 0 && q0 + 32 * (warp & 3) < p.S_q) {  // a box wholly past S_q writes nothing
+        for (int cb = 0; cb < D / 64; ++cb)
+          ptx::tma_store_3d(&ymap, stage + cb * 4096, cb * 64, q0 + 32 * (warp & 3), b * p.Hq + h);
+        ptx::bulk_commit_group();
+        ptx::bulk_wait_read_all();  // shared memory stays valid until the stores have read it
+      }
+      __syncwarp();
     }
-    ptx::fence_proxy_async_smem();  // the staged rows, visible to the TMA store
-    __syncwarp();
-    if (ok && lane == 0 && q0 + 32 * (warp & 3) < p.S_q) {  // a box wholly past S_q writes nothing
-      for (int cb = 0; cb < D / 64; ++cb)
-        ptx::tma_store_3d(&ymap, stage + cb * 4096, cb * 64, q0 + 32 * (warp & 3), b * p.Hq + h);
-      ptx::bulk_commit_group();
-      ptx::bulk_wait_read_all();  // shared memory stays valid until the stores have read it
-    }
-    __syncwarp();
   }
   ptx::grid_launch_dependents();
   if (tid == 0 && *abort) report(p.status, EXTKV_DEV_TIMEOUT);
@@ -915,12 +959,81 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) ptx::tmem_dealloc(tbase, C::kTmemCols);
 }
 
+// ---- merge of the key splits ----------------------------------------------------------
+
+// One warp per query row: weights 2^(max_s - M) of the splits (lane s holds
+// split s; n_split <= kMaxSplit), then the row's columns four per lane, summed in
+// split order (the result does not depend on timing).  A row whose splits
+// saw no unmasked key is an exact zero row.
+__global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillParams p, int D) {
+  ptx::grid_dependency_wait();
+  ptx::grid_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int ns = p.n_split, ps = part_stride(D);
+  const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.S_q;
+  const int64_t split_stride = static_cast<int64_t>(p.S_q) * ps;
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5); r < rows;
+       r += static_cast<int64_t>(gridDim.x) * 8) {
+    const int64_t bh = r / p.S_q, i = r % p.S_q;
+    const float* base = p.part + (bh * ns * p.S_q + i) * ps;
+    float m = -INFINITY, l = 0.f;
+    if (lane < ns) {
+      m = __ldcg(base + lane * split_stride + D);
+      l = __ldcg(base + lane * split_stride + D + 1);
+    }
+    float M = m;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float ref = M == -INFINITY ? 0.f : M;
+    const float w = (lane < ns && m != -INFINITY) ? ptx::ex2(m - ref) : 0.f;
+    float L = w * l;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    float wsv[kMaxSplit];
+#pragma unroll
+    for (int sg = 0; sg < kMaxSplit; ++sg) wsv[sg] = __shfl_sync(0xffffffffu, w, sg);
+    for (int d = 4 * lane; d < D; d += 128) {
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int sg = 0; sg < kMaxSplit; ++sg) {
+        const float ws = wsv[sg];
+        if (sg >= ns || ws == 0.f) continue;
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(base + sg * split_stride + d));
+        a.x = fmaf(v.x, ws, a.x);
+        a.y = fmaf(v.y, ws, a.y);
+        a.z = fmaf(v.z, ws, a.z);
+        a.w = fmaf(v.w, ws, a.w);
+      }
+      uint2 pk;
+      pk.x = ptx::pack_bf16x2(a.x * inv, a.y * inv);
+      pk.y = ptx::pack_bf16x2(a.z * inv, a.w * inv);
+      *reinterpret_cast<uint2*>(p.y + r * D + d) = pk;
+    }
+  }
+}
+
 // ---- host side ----------------------------------------------------------------------
 
 int n_query_tiles(int64_t S_q) { return static_cast<int>((S_q + kBM - 1) / kBM); }
 int n_plan_chunks(int64_t max_seq) { return static_cast<int>((max_seq + kPlanKeys - 1) / kPlanKeys); }
 // the plan's column-mask table: one 64-bit word per 64 keys
 int n_mask_words(int64_t max_seq) { return static_cast<int>((max_seq + 63) / 64); }
+
+// Key splits per query tile: a grid of fewer CTAs than half the SMs has its
+// query tiles' key ranges split so that about one CTA per SM works.
+int prefill_splits(int64_t B, int64_t Hq, int64_t S_q) {
+  const int64_t ctas = B * Hq * n_query_tiles(S_q);
+  const int sms = num_sms();
+  if (ctas <= 0 || ctas * 2 > sms) return 1;
+  return static_cast<int>(std::min<int64_t>(kMaxSplit, std::max<int64_t>(1, sms / ctas)));
+}
+
+// bytes of the column-mask table, rounded to 256 (the partials follow it)
+size_t colmask_bytes(int64_t B, int64_t S_q, int64_t max_seq) {
+  const size_t n = static_cast<size_t>(B) * n_query_tiles(S_q) * n_mask_words(max_seq) * sizeof(uint64_t);
+  return (n + 255) & ~size_t(255);
+}
 
 template <int D, int MODE, bool CAP>
 cudaError_t launch_dm(const AttnArgs& a, const char** name) {
@@ -987,6 +1100,8 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
   prm.n_pt = n_query_tiles(a.S_q);
   prm.n_tiles = n_mask_words(a.max_seq);
   prm.status = a.status;
+  prm.n_split = prefill_splits(a.B, a.Hq, a.S_q);
+  prm.part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + colmask_bytes(a.B, a.S_q, a.max_seq));
 
   if (MODE == kBias) {
     static std::once_flag plan_once;
@@ -1011,7 +1126,7 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
   }
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(prm.Hq, prm.n_pt, prm.B);
+  cfg.gridDim = dim3(prm.Hq * prm.n_split, prm.n_pt, prm.B);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = a.stream;
@@ -1022,8 +1137,17 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, attn_prefill_kernel<D, MODE, CAP>, qmap, kmap, vmap, tmap, ymap, prm);
   if (e != cudaSuccess) return e;
+  if (prm.n_split > 1) {
+    const int64_t rows = static_cast<int64_t>(prm.B) * prm.Hq * prm.S_q;
+    cfg.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>((rows + 7) / 8, int64_t(num_sms()) * 8)));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&cfg, prefill_merge_kernel, prm, D);
+    if (e != cudaSuccess) return e;
+  }
   *name = "attn_prefill_tcgen05";
-  note_launches(C::kTerm ? 2 : 1);  // the plan kernel, then the attention kernel
+  // the plan kernel, the attention kernel, the merge of the key splits
+  note_launches((C::kTerm ? 2 : 1) + (prm.n_split > 1 ? 1 : 0));
   return cudaGetLastError();
 }
 
@@ -1041,8 +1165,11 @@ cudaError_t launch_d(const AttnArgs& a, const char** name) {
 
 }  // namespace
 
-size_t prefill_workspace_bytes(int64_t B, int64_t S_q, int64_t max_seq) {
-  return static_cast<size_t>(B) * n_query_tiles(S_q) * n_mask_words(max_seq) * sizeof(uint64_t);
+size_t prefill_workspace_bytes(int64_t B, int64_t Hq, int64_t S_q, int64_t max_seq, int64_t D, bool term) {
+  const int ns = prefill_splits(B, Hq, S_q);
+  if (!term && ns == 1) return 0;
+  const size_t part = ns > 1 ? static_cast<size_t>(ns) * B * Hq * S_q * part_stride(static_cast<int>(D)) * 4 : 0;
+  return colmask_bytes(B, S_q, max_seq) + part;  // the partials follow the (maybe unused) mask table
 }
 
 bool prefill_supported(const AttnArgs& a) {

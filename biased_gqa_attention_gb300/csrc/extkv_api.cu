@@ -163,7 +163,7 @@ size_t attention_ext_kv_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64
   size_t need = 0;
   if (decode_supported(a)) need = decode_workspace_bytes(B, Hq, Hkv, S_q, max_seq, D);
   if (prefill_supported(a)) {
-    const size_t pf = prefill_workspace_bytes(B, S_q, max_seq);
+    const size_t pf = prefill_workspace_bytes(B, Hq, S_q, max_seq, D, true);
     need = pf > need ? pf : need;
   }
   return need;
@@ -272,8 +272,9 @@ int attention_impl(void* y, const void* q, const void* k_cache, const void* v_ca
   };
   const size_t decode_ws = decode_workspace_bytes(B, Hq, Hkv, S_q, max_seq, D);
   // a materialised bias or an extra term needs the prefill kernel's column-mask table
-  const size_t prefill_ws =
-      (bias || (fused && fused->extra)) ? prefill_workspace_bytes(B, S_q, max_seq) : 0;
+  // the column-mask table (a materialised bias or an extra term) and the
+  // partials of key splits (small grids)
+  const size_t prefill_ws = prefill_workspace_bytes(B, Hq, S_q, max_seq, D, bias || (fused && fused->extra));
   switch (g_algo) {
     case EXTKV_ALGO_GENERIC:
       if ((e = scatter_first(a, sc)) != cudaSuccess) break;

@@ -57,7 +57,7 @@ bool decode_supported(const AttnArgs& a);
 size_t decode_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t D);
 cudaError_t launch_attn_decode(const AttnArgs& a, const char** name);
 bool prefill_supported(const AttnArgs& a);
-size_t prefill_workspace_bytes(int64_t B, int64_t S_q, int64_t max_seq);
+size_t prefill_workspace_bytes(int64_t B, int64_t Hq, int64_t S_q, int64_t max_seq, int64_t D, bool term);
 cudaError_t launch_attn_prefill(const AttnArgs& a, const char** name);
 
 int num_sms();
