@@ -203,8 +203,8 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const __nv_b
   const int ch = blockIdx.x, pt = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   __shared__ uint32_t words[kPlanKeys / 32];
+  __shared__ int4 win_s[FUSED ? kBM : 1];  // per row: band [x, y) and span [z, w), clipped to [-1, max_seq + 1]
   if (tid < kPlanKeys / 32) words[tid] = 0;
-  __syncthreads();
   ptx::grid_launch_dependents();  // the attention kernel may start its prologue
   const int64_t np64 = nonpad[b];
   const bool bad = bad_nonpad(np64, max_seq);
@@ -212,6 +212,18 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const __nv_b
   const int64_t qs = bad ? 0 : query_start(spec.q_start, b, np64, S_q);
   const int q0 = pt * kBM;
   const int rows = min(kBM, S_q - q0);
+  if (FUSED) {
+    // each row's allowed intervals once per block (one thread per row)
+    auto clip = [&](int64_t v) { return static_cast<int>(v < -1 ? -1 : (v > max_seq + 1 ? max_seq + 1 : v)); };
+    for (int r = tid; r < rows; r += kPlanThreads) {
+      const RowWindow w = row_window(spec, b, qs + q0 + r, np);
+      int4 v = make_int4(clip(w.band_lo), clip(w.band_hi), clip(w.span_lo), clip(w.span_hi));
+      if (w.band_lo >= w.band_hi) v.x = v.y = 0;
+      if (w.span_lo >= w.span_hi) v.z = v.w = 0;
+      win_s[r] = v;
+    }
+  }
+  __syncthreads();
   const float lowest = Elem<__nv_bfloat16>::lowest();
   const int kl = ch * kPlanKeys + 8 * lane;  // this lane's 8 keys
   uint32_t acc = 0;
@@ -226,20 +238,12 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const __nv_b
       const int r = warp + (kPlanThreads / 32) * i;
       uint32_t m = r < rows ? valid : 0u;
       if (FUSED && m) {
-        const RowWindow w = row_window(spec, b, qs + q0 + r, np);
-        uint32_t a = 0;
-        if (w.band_lo < w.band_hi) {
-          const int64_t lo = w.band_lo - kl, hi = w.band_hi - kl;
-          const int l = lo < 0 ? 0 : (lo > 8 ? 8 : static_cast<int>(lo));
-          const int h = hi < 0 ? 0 : (hi > 8 ? 8 : static_cast<int>(hi));
-          if (l < h) a |= ((1u << h) - 1) & ~((1u << l) - 1);
-        }
-        if (w.span_lo < w.span_hi) {
-          const int64_t lo = w.span_lo - kl, hi = w.span_hi - kl;
-          const int l = lo < 0 ? 0 : (lo > 8 ? 8 : static_cast<int>(lo));
-          const int h = hi < 0 ? 0 : (hi > 8 ? 8 : static_cast<int>(hi));
-          if (l < h) a |= ((1u << h) - 1) & ~((1u << l) - 1);
-        }
+        // this lane's 8 keys [kl, kl + 8) against the row's two intervals
+        const int4 wv = win_s[r];
+        const int bl = min(max(wv.x - kl, 0), 8), bh = min(max(wv.y - kl, 0), 8);
+        const int sl = min(max(wv.z - kl, 0), 8), sh = min(max(wv.w - kl, 0), 8);
+        const uint32_t a = (bl < bh ? ((1u << bh) - 1) & ~((1u << bl) - 1) : 0u) |
+                           (sl < sh ? ((1u << sh) - 1) & ~((1u << sl) - 1) : 0u);
         m &= a;
       }
       want[i] = m;
