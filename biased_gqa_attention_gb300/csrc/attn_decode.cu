@@ -848,10 +848,14 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
 
 // ---- merge: split units' partials, and the zero rows of empty units -------------
 
+// Slices one unit can span: each holds at least one of the unit's live tiles,
+// and a unit has at most max_tiles of them.
+__host__ __device__ __forceinline__ int merge_slices(int G, int max_tiles) { return G < max_tiles ? G : max_tiles; }
+
 template <int MODE>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
   constexpr int kPre = 8;  // slices whose partial rows a thread loads before the weights are known
-  extern __shared__ float sm_raw[];  // [G][kRows] maxima, then [G][kRows] sums
+  extern __shared__ float sm_raw[];  // [NS][kRows] maxima, then [NS][kRows] sums
   const int tid = threadIdx.x;
   const int u = blockIdx.x;
   const int b = u / p.Hkv, kvh = u % p.Hkv;
@@ -868,7 +872,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   const int ns = info.y;
   if (ns == 1) return;  // written by the decode kernel
   float(*msh)[kRows] = reinterpret_cast<float(*)[kRows]>(sm_raw);
-  float(*lsh)[kRows] = reinterpret_cast<float(*)[kRows]>(sm_raw + static_cast<size_t>(p.G) * kRows);
+  float(*lsh)[kRows] = reinterpret_cast<float(*)[kRows]>(sm_raw + static_cast<size_t>(merge_slices(p.G, p.max_tiles)) * kRows);
   constexpr int PS = 2 * kRows;  // header floats of a partial
   const int stride = PS + kRows * D;
   // slice s of the unit: CTA info.x + s; the unit is the first unit of every
@@ -1024,7 +1028,7 @@ cudaError_t launch_dm(const AttnArgs& a, const DecodeParams& prm, const CUtensor
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.Hkv));
   cfg.blockDim = dim3(kMergeThreads);
-  cfg.dynamicSmemBytes = static_cast<size_t>(prm.G) * kRows * 4 * 2;
+  cfg.dynamicSmemBytes = static_cast<size_t>(merge_slices(prm.G, prm.max_tiles)) * kRows * 4 * 2;
   e = cudaFuncSetAttribute(decode_merge_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(cfg.dynamicSmemBytes));
   if (e != cudaSuccess) return e;
@@ -1138,10 +1142,12 @@ bool decode_supported(const AttnArgs& a) {
   const int64_t units = a.B * a.Hkv;
   if (a.B > kMaxB || units >= (1 << 20) || max_tiles > 65535) return false;
   if (a.B * a.Hq * a.S_q > 0x7fffffff || units * max_tiles > 0x7fffffff) return false;
-  // a slice must fit the plan's work table (the merge weights table holds G rows)
+  // a slice must fit the plan's work table (the merge weights table holds a
+  // row per slice of a unit)
   const int64_t G = grid_for(a.D, units * max_tiles);
   const int64_t slice = (units * max_tiles + G - 1) / G;
-  if (slice > kMaxWork || G * kRows * 8 > 200 * 1024) return false;
+  const int64_t ns = merge_slices(static_cast<int>(G), static_cast<int>(max_tiles));
+  if (slice > kMaxWork || ns * kRows * 8 > 200 * 1024) return false;
   return true;
 }
 

@@ -67,6 +67,9 @@ def _load():
             lib.oracle_attention_softcap.argtypes = [P, P, P, P, P, P, ctypes.c_float, ctypes.c_float, I64,
                                                      I64, I64, I64, I64, I64, I, P, I64]
             lib.oracle_attention_softcap.restype = I64
+            lib.oracle_attention_dv.argtypes = [P, P, P, P, P, P, ctypes.c_float, ctypes.c_float, I64,
+                                                I64, I64, I64, I64, I64, I64, I, P, I64]
+            lib.oracle_attention_dv.restype = I64
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = I
             _lib = lib
@@ -161,28 +164,32 @@ def bias_from_mask(mask, dt):
 
 
 def attention(q, k_cache, v_cache, bias_, nonpad, scale, rows=None, softcap=0.0):
-    """fp64 attention output.  q (B,Hq,S_q,D), caches (B,Hkv,max_seq,D),
-    ``bias_`` None or (B,1,S_q,max_seq), all in one element type.  ``softcap``
-    > 0 caps the scaled scores, cap * tanh(x / cap), before the bias.
+    """fp64 attention output.  q (B,Hq,S_q,Dk), k_cache (B,Hkv,max_seq,Dk),
+    v_cache (B,Hkv,max_seq,Dv) (Dv may differ from Dk), ``bias_`` None or
+    (B,1,S_q,max_seq), all in one element type.  ``softcap`` > 0 caps the
+    scaled scores, cap * tanh(x / cap), before the bias.
 
     With ``rows`` (flat indices (b*Hq+h)*S_q+i) only those rows are computed
-    and the result is (len(rows), D); otherwise it is (B,Hq,S_q,D).
+    and the result is (len(rows), Dv); otherwise it is (B,Hq,S_q,Dv).
     """
     dt = dtype_of(q)
     q, k_cache, v_cache = _raw(q, dt), _raw(k_cache, dt), _raw(v_cache, dt)
     b_ = None if bias_ is None else _raw(bias_, dt)
-    B, Hq, S_q, D = q.shape
+    B, Hq, S_q, Dk = q.shape
     Hkv, max_seq = k_cache.shape[1], k_cache.shape[2]
+    Dv = v_cache.shape[3]
     if Hq % Hkv:
         raise ValueError("Hq must be a multiple of Hkv")
+    if k_cache.shape[3] != Dk or v_cache.shape[:3] != k_cache.shape[:3]:
+        raise ValueError("cache shapes do not match q")
     np_ = _c(nonpad, np.int64)
     r = _c(rows, np.int64)
     n = B * Hq * S_q if r is None else r.shape[0]
-    y = np.zeros((n, D), np.float64)
-    _load().oracle_attention_softcap(_ptr(y), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(b_), _ptr(np_),
-                                     float(scale), float(softcap), B, Hq, Hkv, S_q, max_seq, D, DTYPES[dt],
-                                     _ptr(r), n)
-    return y.reshape(B, Hq, S_q, D) if r is None else y
+    y = np.zeros((n, Dv), np.float64)
+    _load().oracle_attention_dv(_ptr(y), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(b_), _ptr(np_),
+                                float(scale), float(softcap), B, Hq, Hkv, S_q, max_seq, Dk, Dv, DTYPES[dt],
+                                _ptr(r), n)
+    return y.reshape(B, Hq, S_q, Dv) if r is None else y
 
 
 # --- exact conversions between torch-free numpy arrays and element types ------

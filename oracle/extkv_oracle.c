@@ -200,17 +200,23 @@ void oracle_bias_from_mask(void *bias, const unsigned char *mask, int64_t n, int
  *   y        = sum_{j in U} exp(s_j - m) v_j / sum_{j in U} exp(s_j - m),
  *              m = max_{j in U} s_j  (max-subtracted softmax, [ORT] section 8)
  * Without a bias, U = { j < nonpad[b] } and bias_j = 0.
+ * q and k rows have Dk elements, v rows and y rows Dv: the query-key head
+ * size and the value head size may differ (the "ORT CUDA Attention Kernel
+ * Dispatch" section of the attention-optimization skill: a KV-shared layer
+ * borrowing K/V from a layer of another head size has head_size !=
+ * v_head_size); the scores use the Dk-long dot products, the output is a
+ * weighted sum of Dv-long value rows.
  * Returns 0, or 1 when nonpad[b] is outside [0,max_seq] (the row is zeroed).
  */
 static int orc_row(double *y, const void *q, const void *k_cache, const void *v_cache,
                    const void *bias, const int64_t *nonpad, double scale, double softcap, int64_t Hq,
-                   int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t D, int dt, int64_t b,
+                   int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t Dk, int64_t Dv, int dt, int64_t b,
                    int64_t h, int64_t i, double *s, unsigned char *in_u) {
   int64_t np = nonpad[b];
-  for (int64_t d = 0; d < D; ++d) y[d] = 0.0;
+  for (int64_t d = 0; d < Dv; ++d) y[d] = 0.0;
   if (np < 0 || np > max_seq) return 1;
   int64_t kv = h / (Hq / Hkv);
-  const int64_t q_off = ((b * Hq + h) * S_q + i) * D;
+  const int64_t q_off = ((b * Hq + h) * S_q + i) * Dk;
   const int64_t kv_base = (b * Hkv + kv) * max_seq;
   const double lowest = orc_lowest(dt);
   int any = 0;
@@ -220,8 +226,8 @@ static int orc_row(double *y, const void *q, const void *k_cache, const void *v_
     in_u[j] = (unsigned char)(!bias || bj > lowest);
     if (!in_u[j]) continue;
     double dot = 0.0;
-    for (int64_t d = 0; d < D; ++d)
-      dot += orc_load(q, q_off + d, dt) * orc_load(k_cache, (kv_base + j) * D + d, dt);
+    for (int64_t d = 0; d < Dk; ++d)
+      dot += orc_load(q, q_off + d, dt) * orc_load(k_cache, (kv_base + j) * Dk + d, dt);
     double t = scale * dot;
     if (softcap > 0.0) t = softcap * tanh(t / softcap);
     s[j] = t + bj;
@@ -234,24 +240,25 @@ static int orc_row(double *y, const void *q, const void *k_cache, const void *v_
     if (!in_u[j]) continue;
     double w = exp(s[j] - m);
     denom += w;
-    for (int64_t d = 0; d < D; ++d) y[d] += w * orc_load(v_cache, (kv_base + j) * D + d, dt);
+    for (int64_t d = 0; d < Dv; ++d) y[d] += w * orc_load(v_cache, (kv_base + j) * Dv + d, dt);
   }
-  for (int64_t d = 0; d < D; ++d) y[d] /= denom;
+  for (int64_t d = 0; d < Dv; ++d) y[d] /= denom;
   return 0;
 }
 
 /*
  * Attention over the external cache for all rows (rows == NULL, y is
- * (B,Hq,S_q,D)) or for the n_rows flat row indices r = (b*Hq + h)*S_q + i
- * listed in rows (y is (n_rows,D)).  bias is NULL or (B,1,S_q,max_seq).
- * A KV-shared layer ([PR] Design) is this same call on a borrowed cache with
- * no preceding scatter.  Returns the number of rows whose batch had an
- * out-of-range nonpad.
+ * (B,Hq,S_q,Dv)) or for the n_rows flat row indices r = (b*Hq + h)*S_q + i
+ * listed in rows (y is (n_rows,Dv)).  q is (B,Hq,S_q,Dk), the caches
+ * (B,Hkv,max_seq,Dk) and (B,Hkv,max_seq,Dv); bias is NULL or
+ * (B,1,S_q,max_seq).  A KV-shared layer ([PR] Design) is this same call on a
+ * borrowed cache with no preceding scatter.  Returns the number of rows whose
+ * batch had an out-of-range nonpad.
  */
-int64_t oracle_attention_softcap(double *y, const void *q, const void *k_cache, const void *v_cache,
-                                 const void *bias, const int64_t *nonpad, float scale, float softcap,
-                                 int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t D,
-                                 int dt, const int64_t *rows, int64_t n_rows) {
+int64_t oracle_attention_dv(double *y, const void *q, const void *k_cache, const void *v_cache, const void *bias,
+                            const int64_t *nonpad, float scale, float softcap, int64_t B, int64_t Hq, int64_t Hkv,
+                            int64_t S_q, int64_t max_seq, int64_t Dk, int64_t Dv, int dt, const int64_t *rows,
+                            int64_t n_rows) {
   int64_t total = rows ? n_rows : B * Hq * S_q;
   int64_t bad = 0;
 #pragma omp parallel reduction(+ : bad)
@@ -263,13 +270,22 @@ int64_t oracle_attention_softcap(double *y, const void *q, const void *k_cache, 
       int64_t r = rows ? rows[t] : t;
       int64_t i = r % S_q, bh = r / S_q;
       int64_t h = bh % Hq, b = bh / Hq;
-      bad += orc_row(y + t * D, q, k_cache, v_cache, bias, nonpad, (double)scale, (double)softcap, Hq, Hkv,
-                     S_q, max_seq, D, dt, b, h, i, s, in_u);
+      bad += orc_row(y + t * Dv, q, k_cache, v_cache, bias, nonpad, (double)scale, (double)softcap, Hq, Hkv,
+                     S_q, max_seq, Dk, Dv, dt, b, h, i, s, in_u);
     }
     free(s);
     free(in_u);
   }
   return bad;
+}
+
+/* One head size for queries, keys and values. */
+int64_t oracle_attention_softcap(double *y, const void *q, const void *k_cache, const void *v_cache,
+                                 const void *bias, const int64_t *nonpad, float scale, float softcap,
+                                 int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t D,
+                                 int dt, const int64_t *rows, int64_t n_rows) {
+  return oracle_attention_dv(y, q, k_cache, v_cache, bias, nonpad, scale, softcap, B, Hq, Hkv, S_q, max_seq, D, D,
+                             dt, rows, n_rows);
 }
 
 /* The attention without a softcap. */

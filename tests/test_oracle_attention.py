@@ -15,7 +15,12 @@ What fixes the result, independently of the oracle's own code:
     a decode step equals the last row of the matching prefill and a chunked
     prefill equals the one-shot prefill (section 11, bottom-right alignment);
     a KV-shared layer ("[GQA] Support KV-shared layers with empty K/V inputs",
-    Design) equals attention over the borrowed cache.
+    Design) equals attention over the borrowed cache;
+  * value rows of another head size (head_size != v_head_size, "Skill:
+    Attention Optimization", "ORT CUDA Attention Kernel Dispatch"): torch SDPA
+    on the same asymmetric shapes, and the output columns of a V split by
+    columns are the columns of the whole (each output column is the same
+    weighted sum over its own V column).
 """
 import math
 import os
@@ -332,3 +337,37 @@ def test_softcap_single_key_and_poison_under_the_mask(dt):
     y0 = oracle.attention(q, k, v, bw, nonpad, scale, softcap=0.05)
     yp = oracle.attention(q, k, vp, bw, nonpad, scale, softcap=0.05)
     assert np.isfinite(yp).all() and np.array_equal(y0, yp)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(16, 24), (24, 8)])
+def test_value_head_size_differs_matches_torch_sdpa_fp64(dt, dk, dv):
+    rng = np.random.default_rng(21)
+    B, Hq, Hkv, S_q, L = 2, 4, 2, 5, 23
+    nonpad = np.array([23, 11], np.int64)
+    q = _rand((B, Hq, S_q, dk), dt, rng)
+    k = _rand((B, Hkv, L, dk), dt, rng)
+    v = _rand((B, Hkv, L, dv), dt, rng)
+    bias, _ = oracle.bias(nonpad, S_q, L, dt, causal=True, window=7, spans=[[(15, 5)], []])
+    scale = np.float32(1.0 / math.sqrt(dk))
+    y = oracle.attention(q, k, v, bias, nonpad, scale)
+    assert y.shape == (B, Hq, S_q, dv)
+    ref, live = _sdpa(q, k, v, bias, nonpad, float(scale), dt)
+    assert live.any()
+    np.testing.assert_allclose(y[live], ref[live], rtol=0, atol=1e-12)
+    assert (y[~live] == 0).all()
+
+
+def test_value_columns_split_equals_whole():
+    rng = np.random.default_rng(8)
+    B, Hq, Hkv, S_q, L, dk, dv = 2, 4, 1, 3, 19, 8, 12
+    nonpad = np.array([19, 7], np.int64)
+    q = _rand((B, Hq, S_q, dk), "bf16", rng)
+    k = _rand((B, Hkv, L, dk), "bf16", rng)
+    v = _rand((B, Hkv, L, dv), "bf16", rng)
+    bias, _ = oracle.bias(nonpad, S_q, L, "bf16", causal=True, window=5)
+    scale = np.float32(0.3)
+    whole = oracle.attention(q, k, v, bias, nonpad, scale)
+    left = oracle.attention(q, k, np.ascontiguousarray(v[..., :5]), bias, nonpad, scale)
+    right = oracle.attention(q, k, np.ascontiguousarray(v[..., 5:]), bias, nonpad, scale)
+    assert np.array_equal(whole, np.concatenate([left, right], axis=-1))

@@ -29,8 +29,12 @@ MUTATIONS = {
     "v_reads_k": ("y[d] += w * orc_load(v_cache,", "y[d] += w * orc_load(k_cache,"),
     "span_end_inclusive": ("j >= lo && j < hi", "j >= lo && j <= hi"),
     "scatter_ignores_offset": ("* max_seq + (w + s)) * D + d;", "* max_seq + s) * D + d;"),
-    "query_row_reversed": ("const int64_t q_off = ((b * Hq + h) * S_q + i) * D;",
-                           "const int64_t q_off = ((b * Hq + h) * S_q + (S_q - 1 - i)) * D;"),
+    "query_row_reversed": ("const int64_t q_off = ((b * Hq + h) * S_q + i) * Dk;",
+                           "const int64_t q_off = ((b * Hq + h) * S_q + (S_q - 1 - i)) * Dk;"),
+    "v_rows_with_key_stride": ("orc_load(v_cache, (kv_base + j) * Dv + d, dt)",
+                               "orc_load(v_cache, (kv_base + j) * Dk + d, dt)"),
+    "k_rows_with_value_stride": ("orc_load(k_cache, (kv_base + j) * Dk + d, dt)",
+                                 "orc_load(k_cache, (kv_base + j) * Dv + d, dt)"),
     "causal_strict": ("int causal_ok = !causal || j <= p;", "int causal_ok = !causal || j < p;"),
     "padding_ignored_in_bias": ("if (j >= nonpad) return 0;", ""),
 }
