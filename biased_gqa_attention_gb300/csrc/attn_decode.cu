@@ -1135,6 +1135,7 @@ size_t decode_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, i
 bool decode_supported(const AttnArgs& a) {
   if (a.dtype != EXTKV_BF16) return false;
   if (a.D != 64 && a.D != 128 && a.D != 256 && a.D != 512) return false;
+  if (a.Dv != a.D) return false;  // one head size for keys and values
   if ((a.Hq / a.Hkv) * a.S_q > kRows) return false;
   // 16-byte rows for the bias / extra-term block copies
   if ((a.bias || (a.fused && a.extra)) && a.max_seq % 8) return false;

@@ -105,6 +105,7 @@ extern "C" int attention_ext_kv_noalloc(void* y, const void* q, const void* k_ca
   a.S_q = S_q;
   a.max_seq = max_seq;
   a.D = D;
+  a.Dv = D;
   a.dtype = dtype;
   a.status = status;
   a.stream = static_cast<cudaStream_t>(stream);

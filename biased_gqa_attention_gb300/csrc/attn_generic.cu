@@ -3,8 +3,11 @@
 // One warp per query row (b, h, i).  This is the path for fp32 inputs (the
 // tensor-core paths cannot multiply fp32 exactly) and for any supported shape
 // the specialised kernels do not take.  Lane l holds elements d = l + 32 t of
-// q and of its running output; a key's score is a warp-wide dot product, then
-// an online-softmax update (running max m, running sum l, rescaled output).
+// q (Dk of them) and of its running output (Dv); a key's score is a
+// warp-wide dot product, then an online-softmax update (running max m,
+// running sum l, rescaled output).  Dk and Dv may differ (head_size !=
+// v_head_size, "Skill: Attention Optimization", "ORT CUDA Attention Kernel
+// Dispatch").
 //
 // Semantics ("ONNX Domain Attention (Opset 23/24) CUDA Patterns"): section 4
 // op order scale*QK^T + bias -> softmax -> @V; section 6 masking (a key is
@@ -26,7 +29,7 @@ __global__ void __launch_bounds__(32 * kWarps) attn_generic_kernel(
     T* __restrict__ y, const T* __restrict__ q, const T* __restrict__ k_cache,
     const T* __restrict__ v_cache, const T* __restrict__ bias, BiasSpec spec, int fused,
     const int64_t* __restrict__ nonpad, float scale, float softcap, int64_t Hq, int64_t Hkv, int64_t S_q,
-    int64_t max_seq, int D, int64_t rows, int32_t* status) {
+    int64_t max_seq, int Dk, int Dv, int64_t rows, int32_t* status) {
   using E = Elem<T>;
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
@@ -41,21 +44,21 @@ __global__ void __launch_bounds__(32 * kWarps) attn_generic_kernel(
     const int64_t b = bh / Hq;
     const int64_t kvh = h / (Hq / Hkv);
     const int64_t np = nonpad[b];
-    T* yrow = y + row * D;
+    T* yrow = y + row * Dv;
     if (bad_nonpad(np, max_seq)) {
       if (lane == 0 && h == 0 && i == 0) report(status, EXTKV_DEV_BAD_NONPAD);
-      for (int d = lane; d < D; d += 32) yrow[d] = E::from_float(0.0f);
+      for (int d = lane; d < Dv; d += 32) yrow[d] = E::from_float(0.0f);
       continue;
     }
     float qr[DPL], acc[DPL];
 #pragma unroll
     for (int t = 0; t < DPL; ++t) {
       const int d = lane + 32 * t;
-      qr[t] = d < D ? E::load(q, row * D + d) : 0.0f;
+      qr[t] = d < Dk ? E::load(q, row * Dk + d) : 0.0f;
       acc[t] = 0.0f;
     }
-    const T* kbase = k_cache + (b * Hkv + kvh) * max_seq * D;
-    const T* vbase = v_cache + (b * Hkv + kvh) * max_seq * D;
+    const T* kbase = k_cache + (b * Hkv + kvh) * max_seq * Dk;
+    const T* vbase = v_cache + (b * Hkv + kvh) * max_seq * Dv;
     const T* brow = bias ? bias + (b * S_q + i) * max_seq : nullptr;
     const T* erow = extra ? extra + (b * S_q + i) * max_seq : nullptr;
 
@@ -93,13 +96,13 @@ __global__ void __launch_bounds__(32 * kWarps) attn_generic_kernel(
         mask &= mask - 1;
         const int64_t j = j0 + src;
         const float bb = __shfl_sync(0xffffffffu, bj, src);
-        const T* kr = kbase + j * D;
-        const T* vr = vbase + j * D;
+        const T* kr = kbase + j * Dk;
+        const T* vr = vbase + j * Dv;
         float part = 0.0f;
 #pragma unroll
         for (int t = 0; t < DPL; ++t) {
           const int d = lane + 32 * t;
-          if (d < D) part = fmaf(qr[t], E::load(kr, d), part);
+          if (d < Dk) part = fmaf(qr[t], E::load(kr, d), part);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
@@ -114,7 +117,7 @@ __global__ void __launch_bounds__(32 * kWarps) attn_generic_kernel(
 #pragma unroll
         for (int t = 0; t < DPL; ++t) {
           const int d = lane + 32 * t;
-          const float vv = d < D ? E::load(vr, d) : 0.0f;
+          const float vv = d < Dv ? E::load(vr, d) : 0.0f;
           acc[t] = fmaf(pj, vv, acc[t] * corr);
         }
         m = m_new;
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(32 * kWarps) attn_generic_kernel(
 #pragma unroll
     for (int t = 0; t < DPL; ++t) {
       const int d = lane + 32 * t;
-      if (d < D) yrow[d] = E::from_float(l > 0.0f ? acc[t] * inv : 0.0f);
+      if (d < Dv) yrow[d] = E::from_float(l > 0.0f ? acc[t] * inv : 0.0f);
     }
   }
 }
@@ -135,7 +138,8 @@ void launch_dpl(const AttnArgs& a, int blocks, const BiasSpec& spec, int64_t row
   attn_generic_kernel<T, DPL><<<blocks, 32 * kWarps, 0, a.stream>>>(
       static_cast<T*>(a.y), static_cast<const T*>(a.q), static_cast<const T*>(a.k_cache),
       static_cast<const T*>(a.v_cache), static_cast<const T*>(a.bias), spec, a.fused, a.nonpad,
-      a.scale, a.softcap, a.Hq, a.Hkv, a.S_q, a.max_seq, static_cast<int>(a.D), rows, a.status);
+      a.scale, a.softcap, a.Hq, a.Hkv, a.S_q, a.max_seq, static_cast<int>(a.D), static_cast<int>(a.Dv), rows,
+      a.status);
 }
 
 template <typename T>
@@ -144,7 +148,7 @@ cudaError_t launch_typed(const AttnArgs& a) {
   const int64_t want = (rows + kWarps - 1) / kWarps;
   const int blocks = static_cast<int>(std::min<int64_t>(want, int64_t(num_sms()) * 16));
   BiasSpec spec{a.causal, a.window, a.span_offsets, a.spans, a.extra, a.q_start};
-  const int64_t dpl = (a.D + 31) / 32;  // elements per lane, D <= 512
+  const int64_t dpl = (std::max(a.D, a.Dv) + 31) / 32;  // elements per lane, Dk, Dv <= 512
   if (dpl <= 1) launch_dpl<T, 1>(a, blocks, spec, rows);
   else if (dpl <= 2) launch_dpl<T, 2>(a, blocks, spec, rows);
   else if (dpl <= 4) launch_dpl<T, 4>(a, blocks, spec, rows);

@@ -146,10 +146,11 @@ int build_bias_from_bool_mask(void* bias, const uint8_t* mask, int64_t B, int64_
   return EXTKV_OK;
 }
 
-size_t attention_ext_kv_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq,
-                                       int64_t D, int dtype) {
+size_t attention_ext_kv_workspace_size_dv(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq,
+                                          int64_t Dk, int64_t Dv, int dtype) {
   // The decode kernel keeps its plan and its split-unit partials there; the
-  // prefill kernel keeps the live key ranges of a materialised bias.
+  // prefill kernel keeps the live key ranges of a materialised bias and the
+  // partials of key splits.
   if (dtype != EXTKV_BF16 || B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || S_q <= 0 || max_seq <= 0) return 0;
   AttnArgs a{};
   a.dtype = dtype;
@@ -158,15 +159,21 @@ size_t attention_ext_kv_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64
   a.Hkv = Hkv;
   a.S_q = S_q;
   a.max_seq = max_seq;
-  a.D = D;
+  a.D = Dk;
+  a.Dv = Dv;
   // enough for whichever kernel runs, automatic or chosen by extkv_set_algo
   size_t need = 0;
-  if (decode_supported(a)) need = decode_workspace_bytes(B, Hq, Hkv, S_q, max_seq, D);
+  if (decode_supported(a)) need = decode_workspace_bytes(B, Hq, Hkv, S_q, max_seq, Dk);
   if (prefill_supported(a)) {
-    const size_t pf = prefill_workspace_bytes(B, Hq, S_q, max_seq, D, true);
+    const size_t pf = prefill_workspace_bytes(B, Hq, S_q, max_seq, Dk, Dv, true);
     need = pf > need ? pf : need;
   }
   return need;
+}
+
+size_t attention_ext_kv_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq,
+                                       int64_t D, int dtype) {
+  return attention_ext_kv_workspace_size_dv(B, Hq, Hkv, S_q, max_seq, D, D, dtype);
 }
 
 }  // extern "C"
@@ -186,7 +193,7 @@ struct ScatterIn {
 
 int attention_impl(void* y, const void* q, const void* k_cache, const void* v_cache, const void* bias,
                    const extkv_bias_spec* fused, const int64_t* nonpad, float scale, int64_t B, int64_t Hq,
-                   int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t D, int dtype, void* workspace,
+                   int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t D, int64_t Dv, int dtype, void* workspace,
                    size_t ws_bytes, int32_t* status, void* stream, const ScatterIn* sc, float softcap = 0.f) {
   if (!valid_dtype(dtype)) return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv: unknown dtype %d", dtype);
   if (B < 0 || S_q < 0 || Hq <= 0 || Hkv <= 0 || max_seq <= 0 || D <= 0)
@@ -200,6 +207,11 @@ int attention_impl(void* y, const void* q, const void* k_cache, const void* v_ca
   if (D % 8 || D > 512)
     return fail(EXTKV_ERR_UNSUPPORTED, "attention_ext_kv: D=%lld unsupported (need D %% 8 == 0, D <= 512)",
                 (long long)D);
+  if (Dv <= 0 || Dv % 8 || Dv > 512)
+    return fail(EXTKV_ERR_UNSUPPORTED, "attention_ext_kv: Dv=%lld unsupported (need Dv %% 8 == 0, 0 < Dv <= 512)",
+                (long long)Dv);
+  if (sc && Dv != D)
+    return fail(EXTKV_ERR_UNSUPPORTED, "attention_ext_kv_scatter: one head size for keys and values");
   if (bias && fused)
     return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv: pass either a materialised bias or a fused spec, not both");
   if (B == 0 || S_q == 0) {
@@ -242,6 +254,7 @@ int attention_impl(void* y, const void* q, const void* k_cache, const void* v_ca
   a.S_q = S_q;
   a.max_seq = max_seq;
   a.D = D;
+  a.Dv = Dv;
   a.dtype = dtype;
   a.status = status;
   a.workspace = workspace;
@@ -274,7 +287,7 @@ int attention_impl(void* y, const void* q, const void* k_cache, const void* v_ca
   // a materialised bias or an extra term needs the prefill kernel's column-mask table
   // the column-mask table (a materialised bias or an extra term) and the
   // partials of key splits (small grids)
-  const size_t prefill_ws = prefill_workspace_bytes(B, Hq, S_q, max_seq, D, bias || (fused && fused->extra));
+  const size_t prefill_ws = prefill_workspace_bytes(B, Hq, S_q, max_seq, D, Dv, bias || (fused && fused->extra));
   switch (g_algo) {
     case EXTKV_ALGO_GENERIC:
       if ((e = scatter_first(a, sc)) != cudaSuccess) break;
@@ -323,7 +336,7 @@ int attention_ext_kv(void* y, const void* q, const void* k_cache, const void* v_
                      int64_t D, int dtype, void* workspace, size_t ws_bytes, int32_t* status,
                      void* stream) {
   g_error[0] = 0;
-  return attention_impl(y, q, k_cache, v_cache, bias, fused, nonpad, scale, B, Hq, Hkv, S_q, max_seq, D, dtype,
+  return attention_impl(y, q, k_cache, v_cache, bias, fused, nonpad, scale, B, Hq, Hkv, S_q, max_seq, D, D, dtype,
                         workspace, ws_bytes, status, stream, nullptr);
 }
 
@@ -335,7 +348,18 @@ int attention_ext_kv_softcap(void* y, const void* q, const void* k_cache, const 
   g_error[0] = 0;
   if (!(softcap >= 0.f) || softcap == INFINITY)
     return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv_softcap: softcap must be finite and >= 0");
-  return attention_impl(y, q, k_cache, v_cache, bias, fused, nonpad, scale, B, Hq, Hkv, S_q, max_seq, D, dtype,
+  return attention_impl(y, q, k_cache, v_cache, bias, fused, nonpad, scale, B, Hq, Hkv, S_q, max_seq, D, D, dtype,
+                        workspace, ws_bytes, status, stream, nullptr, softcap);
+}
+
+int attention_ext_kv_dv(void* y, const void* q, const void* k_cache, const void* v_cache, const void* bias,
+                        const extkv_bias_spec* fused, const int64_t* nonpad, float scale, float softcap, int64_t B,
+                        int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t Dk, int64_t Dv, int dtype,
+                        void* workspace, size_t ws_bytes, int32_t* status, void* stream) {
+  g_error[0] = 0;
+  if (!(softcap >= 0.f) || softcap == INFINITY)
+    return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv_dv: softcap must be finite and >= 0");
+  return attention_impl(y, q, k_cache, v_cache, bias, fused, nonpad, scale, B, Hq, Hkv, S_q, max_seq, Dk, Dv, dtype,
                         workspace, ws_bytes, status, stream, nullptr, softcap);
 }
 
@@ -360,7 +384,7 @@ int attention_ext_kv_scatter(void* y, const void* q, void* k_cache, void* v_cach
       return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv_scatter: tensors must be 16-byte aligned");
   }
   const ScatterIn sc{k_cache, v_cache, k_new, v_new, write_idx, S_new};
-  return attention_impl(y, q, k_cache, v_cache, bias, fused, nonpad, scale, B, Hq, Hkv, S_q, max_seq, D, dtype,
+  return attention_impl(y, q, k_cache, v_cache, bias, fused, nonpad, scale, B, Hq, Hkv, S_q, max_seq, D, D, dtype,
                         workspace, ws_bytes, status, stream, (B > 0 && S_new > 0) ? &sc : nullptr);
 }
 

@@ -25,7 +25,8 @@ struct AttnArgs {
   const int64_t* nonpad;
   float scale;
   float softcap;  // > 0: scores capped to softcap * tanh(score / softcap) before the bias
-  int64_t B, Hq, Hkv, S_q, max_seq, D;
+  int64_t B, Hq, Hkv, S_q, max_seq, D;  // D: head size of q and k
+  int64_t Dv;                            // head size of v and y (== D unless asymmetric)
   int dtype;
   int32_t* status;
   void* workspace;
@@ -57,7 +58,9 @@ bool decode_supported(const AttnArgs& a);
 size_t decode_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t D);
 cudaError_t launch_attn_decode(const AttnArgs& a, const char** name);
 bool prefill_supported(const AttnArgs& a);
-size_t prefill_workspace_bytes(int64_t B, int64_t Hq, int64_t S_q, int64_t max_seq, int64_t D, bool term);
+// Dk, Dv: the key and value head sizes (the partial rows of key splits hold Dv columns)
+size_t prefill_workspace_bytes(int64_t B, int64_t Hq, int64_t S_q, int64_t max_seq, int64_t Dk, int64_t Dv,
+                               bool term);
 cudaError_t launch_attn_prefill(const AttnArgs& a, const char** name);
 
 int num_sms();

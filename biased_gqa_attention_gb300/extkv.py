@@ -24,7 +24,7 @@ ALGO_AUTO, ALGO_GENERIC, ALGO_DECODE, ALGO_PREFILL = 0, 1, 2, 3
 # Every symbol include/extkv.h declares.
 SYMBOLS = ("ext_kv_scatter", "build_static_cache_bias", "attention_ext_kv_workspace_size",
            "attention_ext_kv", "attention_ext_kv_scatter", "attention_ext_kv_softcap",
-           "build_bias_from_bool_mask",
+           "build_bias_from_bool_mask", "attention_ext_kv_dv", "attention_ext_kv_workspace_size_dv",
            "extkv_clear_status", "extkv_read_status",
            "extkv_last_error", "extkv_last_kernel", "extkv_last_launches", "extkv_set_algo",
            "attention_ext_kv_noalloc")
@@ -62,6 +62,11 @@ def load(path: str = LIB_PATH):
                                              I32P, P]
     lib.attention_ext_kv_workspace_size.argtypes = [I64, I64, I64, I64, I64, I64, I]
     lib.attention_ext_kv_workspace_size.restype = ctypes.c_size_t
+    lib.attention_ext_kv_workspace_size_dv.argtypes = [I64, I64, I64, I64, I64, I64, I64, I]
+    lib.attention_ext_kv_workspace_size_dv.restype = ctypes.c_size_t
+    lib.attention_ext_kv_dv.argtypes = [P, P, P, P, P, ctypes.POINTER(_BiasSpec), P, ctypes.c_float,
+                                        ctypes.c_float, I64, I64, I64, I64, I64, I64, I64, I, P, ctypes.c_size_t,
+                                        I32P, P]
     lib.attention_ext_kv.argtypes = [P, P, P, P, P, ctypes.POINTER(_BiasSpec), P, ctypes.c_float,
                                      I64, I64, I64, I64, I64, I64, I, P, ctypes.c_size_t, I32P, P]
     lib.attention_ext_kv_scatter.argtypes = [P, P, P, P, P, P, P, I64, P, ctypes.POINTER(_BiasSpec), P,
@@ -162,24 +167,31 @@ def build_static_cache_bias(bias, spec: BiasSpec, nonpad, status=None, stream=No
                                           _dt(bias), _p(status), _stream(stream)))
 
 
-def attention_ext_kv_workspace_size(B, Hq, Hkv, S_q, max_seq, D, dtype) -> int:
-    """Bytes of device workspace attention_ext_kv needs (queries the current device)."""
-    return int(load().attention_ext_kv_workspace_size(B, Hq, Hkv, S_q, max_seq, D,
-                                                      EXTKV_F32 if dtype == torch.float32 else EXTKV_BF16))
+def attention_ext_kv_workspace_size(B, Hq, Hkv, S_q, max_seq, D, dtype, Dv=None) -> int:
+    """Bytes of device workspace attention_ext_kv needs (queries the current device);
+    ``Dv``: the value head size when it differs from D."""
+    dt = EXTKV_F32 if dtype == torch.float32 else EXTKV_BF16
+    if Dv is None or Dv == D:
+        return int(load().attention_ext_kv_workspace_size(B, Hq, Hkv, S_q, max_seq, D, dt))
+    return int(load().attention_ext_kv_workspace_size_dv(B, Hq, Hkv, S_q, max_seq, D, Dv, dt))
 
 
-def new_workspace(q: torch.Tensor, k_cache: torch.Tensor) -> Optional[torch.Tensor]:
+def new_workspace(q: torch.Tensor, k_cache: torch.Tensor, v_cache: Optional[torch.Tensor] = None
+                  ) -> Optional[torch.Tensor]:
     """A workspace sized for attention over these q / cache shapes (None if none is needed)."""
     B, Hq, S_q, D = q.shape
-    n = attention_ext_kv_workspace_size(B, Hq, k_cache.shape[1], S_q, k_cache.shape[2], D, q.dtype)
+    Dv = D if v_cache is None else v_cache.shape[3]
+    n = attention_ext_kv_workspace_size(B, Hq, k_cache.shape[1], S_q, k_cache.shape[2], D, q.dtype, Dv)
     return torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
 
 
 def attention_ext_kv(y, q, k_cache, v_cache, nonpad, scale, bias=None, fused: Optional[BiasSpec] = None,
                      workspace=None, status=None, stream=None, softcap: float = 0.0):
-    """Y = softmax(cap(scale*QK^T) + bias)V over the external cache; writes ``y`` (B,Hq,S_q,D).
+    """Y = softmax(cap(scale*QK^T) + bias)V over the external cache; writes ``y`` (B,Hq,S_q,Dv).
     ``softcap`` > 0 caps the scaled scores to softcap*tanh(x/softcap) before the
-    bias (attention_ext_kv_softcap); 0 is plain attention_ext_kv.
+    bias (attention_ext_kv_softcap); 0 is plain attention_ext_kv.  A v_cache
+    whose head size Dv differs from q's and k_cache's Dk goes through
+    attention_ext_kv_dv.
 
     ``workspace`` (uint8 device tensor of attention_ext_kv_workspace_size bytes)
     is allocated here when not given."""
@@ -189,17 +201,22 @@ def attention_ext_kv(y, q, k_cache, v_cache, nonpad, scale, bias=None, fused: Op
     _need(nonpad, "nonpad", dims=1, dtype=torch.int64)
     B, Hq, S_q, D = q.shape
     Hkv, max_seq = k_cache.shape[1], k_cache.shape[2]
-    if y.shape != q.shape or v_cache.shape != k_cache.shape or k_cache.shape[0] != B or \
+    Dv = v_cache.shape[3]
+    if y.shape != (B, Hq, S_q, Dv) or v_cache.shape[:3] != k_cache.shape[:3] or k_cache.shape[0] != B or \
             k_cache.shape[3] != D:
         raise ValueError("inconsistent q / y / cache shapes")
     c = None if fused is None else fused._c()
     if workspace is None:
-        need = load().attention_ext_kv_workspace_size(B, Hq, Hkv, S_q, max_seq, D, _dt(q))
+        need = attention_ext_kv_workspace_size(B, Hq, Hkv, S_q, max_seq, D, q.dtype, Dv)
         if need:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     args = (_p(y), _p(q), _p(k_cache), _p(v_cache), _p(bias), None if c is None else ctypes.byref(c), _p(nonpad),
             float(scale))
+    if Dv != D:
+        _check(load().attention_ext_kv_dv(*args, float(softcap), B, Hq, Hkv, S_q, max_seq, D, Dv, _dt(q),
+                                          _p(workspace), ws, _p(status), _stream(stream)))
+        return
     tail = (B, Hq, Hkv, S_q, max_seq, D, _dt(q), _p(workspace), ws, _p(status), _stream(stream))
     if softcap:
         _check(load().attention_ext_kv_softcap(*args, float(softcap), *tail))

@@ -53,6 +53,7 @@ class Workload:
     extra: bool = False          # dense additive term on allowed slots
     garbage_sigma: float = 1.0   # N(0, sigma^2) beyond nonpad
     kv_shared: bool = False      # a second call attends the borrowed cache
+    Dv: Optional[int] = None     # value head size when it differs from D (the q/k head size)
     description: str = ""
 
     @property
@@ -62,6 +63,10 @@ class Workload:
     @property
     def scale(self) -> float:
         return 1.0 / math.sqrt(self.D)
+
+    @property
+    def dv(self) -> int:
+        return self.D if self.Dv is None else self.Dv
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -178,14 +183,14 @@ def make_inputs(w: Workload, device="cpu", poison: bool = False) -> Inputs:
             x.mul_(sigma)
         return x.to(w.dtype)
 
-    B, Hq, Hkv, D, S_q, L = w.B, w.Hq, w.Hkv, w.D, w.S_q, w.max_seq
+    B, Hq, Hkv, D, S_q, L, Dv = w.B, w.Hq, w.Hkv, w.D, w.S_q, w.max_seq, w.dv
     q = draw((B, Hq, S_q, D))
     k_new = draw((B, Hkv, S_q, D))
-    v_new = draw((B, Hkv, S_q, D))
+    v_new = draw((B, Hkv, S_q, Dv))
     k_cache = draw((B, Hkv, L, D))
-    v_cache = draw((B, Hkv, L, D))
+    v_cache = draw((B, Hkv, L, Dv))
     gk = draw((B, Hkv, L, D), w.garbage_sigma)
-    gv = draw((B, Hkv, L, D), w.garbage_sigma)
+    gv = draw((B, Hkv, L, Dv), w.garbage_sigma)
     beyond = (torch.arange(L, device=device)[None, :] >= nonpad.to(device)[:, None])  # (B,L)
     sel = beyond[:, None, :, None]
     if poison:

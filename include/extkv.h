@@ -203,6 +203,30 @@ int attention_ext_kv_softcap(void *y, const void *q, const void *k_cache, const 
                              int32_t *status, void *stream);
 
 /*
+ * attention_ext_kv_softcap with value rows of another head size: q is
+ * (B,Hq,S_q,Dk), k_cache (B,Hkv,max_seq,Dk), v_cache (B,Hkv,max_seq,Dv) and
+ * y (B,Hq,S_q,Dv) ("Skill: Attention Optimization", "ORT CUDA Attention
+ * Kernel Dispatch": head_size != v_head_size, the case of a KV-shared layer
+ * borrowing the cache of a layer with another head size; the scores use the
+ * Dk-long dot products and each output row is a weighted sum of Dv-long
+ * value rows).  Dk == Dv is attention_ext_kv_softcap.  Both head sizes are
+ * multiples of 8 in [8, 512]; everything else as attention_ext_kv_softcap.
+ * The workspace is attention_ext_kv_workspace_size_dv(...) bytes.  Dk == Dv
+ * == 512 and Dk != Dv (each of 128, 256, 512) run on the tensor cores for a
+ * prefill chunk; other asymmetric shapes and decode steps with Dk != Dv run on
+ * the exact fp32 SIMT kernel.
+ */
+int attention_ext_kv_dv(void *y, const void *q, const void *k_cache, const void *v_cache, const void *bias,
+                        const extkv_bias_spec *fused, const int64_t *nonpad, float scale, float softcap,
+                        int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t Dk,
+                        int64_t Dv, int dtype, void *workspace, size_t ws_bytes, int32_t *status,
+                        void *stream);
+
+/* Workspace bytes for attention_ext_kv_dv (attention_ext_kv_workspace_size with Dk, Dv). */
+size_t attention_ext_kv_workspace_size_dv(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq,
+                                          int64_t Dk, int64_t Dv, int dtype);
+
+/*
  * ext_kv_scatter followed by attention_ext_kv, in one call: the same results
  * (the caches hold the new rows afterwards, bit for bit, and y is what
  * attention_ext_kv gives over the updated caches).  The scatter is the step

@@ -20,9 +20,12 @@ def spec_of(inp: wl.Inputs) -> ek.BiasSpec:
 
 
 def run_gpu(inp: wl.Inputs, mode: str = "bias", algo: int = ek.ALGO_AUTO, scatter: bool = True,
-            k_cache=None, v_cache=None):
-    """mode: 'bias' (materialised), 'fused' (in-register spec) or 'none'."""
+            k_cache=None, v_cache=None, softcap: float = 0.0):
+    """mode: 'bias' (materialised), 'fused' (in-register spec) or 'none'.  A
+    workload whose value head size differs from D attends its caches as they
+    are (no scatter: the new rows of K and V have different sizes)."""
     w = inp.w
+    assert not (scatter and w.dv != w.D), "no scatter with two head sizes"
     k = (inp.k_cache if k_cache is None else k_cache).clone()
     v = (inp.v_cache if v_cache is None else v_cache).clone()
     st = ek.new_status()
@@ -33,10 +36,10 @@ def run_gpu(inp: wl.Inputs, mode: str = "bias", algo: int = ek.ALGO_AUTO, scatte
     if mode == "bias":
         bias = torch.empty((w.B, 1, w.S_q, w.max_seq), dtype=w.dtype, device=inp.q.device)
         ek.build_static_cache_bias(bias, spec, inp.nonpad, status=st)
-    y = torch.empty_like(inp.q)
+    y = torch.empty((w.B, w.Hq, w.S_q, w.dv), dtype=w.dtype, device=inp.q.device)
     with ek.use_algo(algo):
         ek.attention_ext_kv(y, inp.q, k, v, inp.nonpad, w.scale, bias=bias,
-                            fused=spec if mode == "fused" else None, status=st)
+                            fused=spec if mode == "fused" else None, status=st, softcap=softcap)
         kernel = ek.extkv_last_kernel()
     code = ek.extkv_read_status(st)
     assert code == ek.EXTKV_OK, ek.extkv_last_error()
