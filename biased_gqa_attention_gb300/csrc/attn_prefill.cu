@@ -22,7 +22,7 @@ size_t prefill_workspace_bytes(int64_t B, int64_t Hq, int64_t S_q, int64_t max_s
   const int ns = prefill_splits(B, Hq * n_vc, S_q);
   if (!term && ns == 1) return 0;
   const size_t part = ns > 1 ? static_cast<size_t>(ns) * B * Hq * S_q * part_stride(static_cast<int>(Dv)) * 4 : 0;
-  return colmask_bytes(B, S_q, max_seq) + part;  // the partials follow the (maybe unused) mask table
+  return term_tables_bytes(B, S_q, max_seq) + part;  // the partials follow the (maybe unused) term tables
 }
 
 bool prefill_supported(const AttnArgs& a) {

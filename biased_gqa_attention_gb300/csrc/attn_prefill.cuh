@@ -141,6 +141,11 @@ struct PrefillParams {
   const __nv_bfloat16* q;
   const int64_t* nonpad;
   const uint64_t* colmask;  // bias / extra-term modes: per (b, query tile, 64-key tile) live columns
+  // materialised bias: per (b, query tile, row, 128-key tile) the row's live keys (16 bytes), and per
+  // (b, query tile, 128-key tile) whether the bias holds values other than 0 and the sentinel there
+  const uint8_t* rowmask;
+  const uint8_t* impure;
+  int rm_stride, n_kt;
   BiasSpec spec;
   float scale_log2;  // scale * log2(e)
   float scale;
@@ -311,18 +316,26 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const __nv_b
 
 // The same table for a materialised bias: each block stages its 128 x 256
 // bias block in shared memory with one bulk copy per row (all in flight at
-// once), then every thread ORs 16 rows of its 8 keys.
+// once), then every thread ORs 16 rows of its 8 keys.  It also writes, per
+// query row and 128-key tile, the bits of the keys the row may attend
+// (rowmask: 16 bytes per row and tile, rm_stride bytes per row), and per
+// (query tile, 128-key tile) whether the bias holds a value other than 0 and
+// the masked sentinel inside the live keys (impure).  Where it does not, the
+// attention kernel needs only the bits: adding a bias of 0 changes no score.
 constexpr int kPlanSmem = kBM * kPlanKeys * 2 + 64;
 
 __global__ void __launch_bounds__(kPlanThreads) prefill_plan_bias_kernel(const __nv_bfloat16* __restrict__ bias,
                                                                         const int64_t* __restrict__ nonpad,
                                                                         uint64_t* __restrict__ colmask, int S_q,
                                                                         int max_seq, int n_pt, int n_words,
+                                                                        uint8_t* __restrict__ rowmask, int rm_stride,
+                                                                        uint8_t* __restrict__ impure, int n_kt,
                                                                         int32_t* status) {
   extern __shared__ __align__(128) uint8_t plan_smem[];
   uint16_t* rows_s = reinterpret_cast<uint16_t*>(plan_smem);
   uint64_t* bar = reinterpret_cast<uint64_t*>(plan_smem + kBM * kPlanKeys * 2);
   __shared__ uint32_t words[kPlanKeys / 32];
+  __shared__ int impure_s[kPlanKeys / kBN];
   const int ch = blockIdx.x, pt = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   ptx::grid_launch_dependents();  // the attention kernel may start its prologue
@@ -333,12 +346,18 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_bias_kernel(const _
   const int q0 = pt * kBM;
   const int rows = min(kBM, S_q - q0);
   if (tid < kPlanKeys / 32) words[tid] = 0;
+  if (tid < kPlanKeys / kBN) impure_s[tid] = 0;
   if (tid == 0) {
     ptx::mbar_init(bar, 1);
     ptx::fence_mbar_init();
   }
   __syncthreads();
   bool ok = true;
+  const int kl = 8 * lane;  // this thread's 8 keys of the chunk
+  // this thread's byte of every row's key bits (none past the last 128-key tile)
+  const bool own_byte = k_begin + kl < n_kt * kBN;
+  uint8_t* rm = rowmask + (static_cast<int64_t>(b) * n_pt + pt) * kBM * rm_stride + (k_begin + kl) / 8;
+  uint32_t mrow[kBM / (kPlanThreads / 32) / 4] = {0, 0, 0, 0};  // this thread's byte of its 16 rows
   if (keys > 0) {
     // whole 16-byte pieces: max_seq % 8 == 0 keeps the rounded row inside the tensor
     const uint32_t row_bytes = static_cast<uint32_t>((keys + 7) / 8) * 16;
@@ -352,25 +371,52 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_bias_kernel(const _
     }
     ok = ptx::mbar_wait_bounded(bar, 0, kWaitPolls);
     if (!ok && tid == 0) report(status, EXTKV_DEV_TIMEOUT);
-    const int kl = 8 * lane;  // this thread's 8 keys of the chunk
     const uint32_t valid = keys - kl >= 8 ? 0xFFu : (keys - kl > 0 ? ((1u << (keys - kl)) - 1) : 0u);
     const float lowest = Elem<__nv_bfloat16>::lowest();
     uint32_t acc = 0;
-    if (ok && valid) {
-      for (int r = warp; r < rows; r += kPlanThreads / 32) {
+    // magnitude bits of the valid keys' values, per 32-bit word of two keys
+    uint32_t vmask[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      vmask[q] = (((valid >> (2 * q)) & 1) ? 0x7FFFu : 0u) | (((valid >> (2 * q + 1)) & 1) ? 0x7FFF0000u : 0u);
+    uint32_t nz = ok ? 0u : 1u;  // a failed copy leaves the tiles to the general path
+    const __nv_bfloat162 lowest2 = __bfloat162bfloat162(__float2bfloat16_rn(lowest));
+#pragma unroll
+    for (int i = 0; i < kBM / (kPlanThreads / 32); ++i) {
+      const int r = warp + (kPlanThreads / 32) * i;
+      uint32_t m = 0;
+      if (ok && valid && r < rows) {
         const uint4 v = *reinterpret_cast<const uint4*>(rows_s + r * kPlanKeys + kl);
         const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          if (__uint_as_float(w4[q] << 16) > lowest) acc |= 1u << (2 * q);
-          if (__uint_as_float(w4[q] & 0xFFFF0000u) > lowest) acc |= 2u << (2 * q);
+          // 0xFFFF in each half whose value is above the sentinel (false for NaN)
+          const uint32_t live = __hgt2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w4[q]), lowest2);
+          m |= ((live & 1u) | ((live >> 15) & 2u)) << (2 * q);
+          // a live value other than +-0 needs the bias itself
+          nz |= w4[q] & vmask[q] & live;
         }
+        m &= valid;
       }
-      acc &= valid;
+      acc |= m;
+      mrow[i >> 2] |= m << (8 * (i & 3));
     }
     if (acc) atomicOr(&words[lane >> 2], acc << (8 * (lane & 3)));
+    if (nz) impure_s[lane / (kBN / 8)] = 1;
   }
   __syncthreads();
+  // the row bits, where the attention kernel reads them: tiles that hold a
+  // live key and whose bias is 0 or the sentinel throughout
+  if (keys > 0 && own_byte && !impure_s[lane / (kBN / 8)]) {
+#pragma unroll
+    for (int i = 0; i < kBM / (kPlanThreads / 32); ++i)
+      rm[static_cast<int64_t>(warp + (kPlanThreads / 32) * i) * rm_stride] =
+          static_cast<uint8_t>(mrow[i >> 2] >> (8 * (i & 3)));
+  }
+  if (tid < kPlanKeys / kBN) {
+    const int kt = ch * (kPlanKeys / kBN) + tid;
+    if (kt < n_kt) impure[(static_cast<int64_t>(b) * n_pt + pt) * n_kt + kt] = static_cast<uint8_t>(impure_s[tid]);
+  }
   if (tid < kPlanKeys / 64) {
     const int t = ch * (kPlanKeys / 64) + tid;
     if (t < n_words)
@@ -536,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int np = bad ? 0 : static_cast<int>(np64);
   const int64_t qs = bad ? 0 : query_start(p.spec.q_start, b, np64, p.S_q);
   const uint64_t* cmrow = C::kTerm ? p.colmask + (static_cast<int64_t>(b) * p.n_pt + pt) * p.n_tiles : nullptr;
+  const int64_t imp0 = MODE == kBias ? (static_cast<int64_t>(b) * p.n_pt + pt) * p.n_kt : 0;
 
   // softmax threads: this thread's query row and its allowed key intervals
   const bool is_sm = warp >= 2;
@@ -606,9 +653,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int unit = b * p.Hkv + hk;
       int issued = 0, t_issued = 0;
       bool ok = true;
+      // term blocks of the tiles that need one, buffers taken in that order;
+      // the flag of the next tile is loaded one call ahead (calls come in tile order)
+      bool imp_next = MODE != kBias || (T > 0 && p.impure[imp0 + t_lo] != 0);
       auto load_term = [&](int j) -> bool {
-        const int tb = j % C::kTB;
-        if (j >= C::kTB && !wait_or_abort(&bar.t_empty[tb], ((j / C::kTB) - 1) & 1, abort)) return false;
+        const bool imp = imp_next;
+        if (MODE == kBias && j + 1 < T) imp_next = p.impure[imp0 + t_lo + j + 1] != 0;
+        if (!imp) return true;  // the row bits suffice
+        const int tb = t_issued % C::kTB;
+        if (t_issued >= C::kTB && !wait_or_abort(&bar.t_empty[tb], ((t_issued / C::kTB) - 1) & 1, abort))
+          return false;
         uint8_t* dst = sT + tb * C::kTermBytes;
         ptx::mbar_arrive_expect_tx(&bar.t_full[tb], C::kTermBytes);
         ptx::tma_load_2d(dst, &tmap, &bar.t_full[tb], (t_lo + j) * kBN, b * p.S_q + q0);
@@ -767,6 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float lowest = Elem<__nv_bfloat16>::lowest();
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
+    int t_seen = 0;  // term blocks consumed
     if (!C::kQSmem && T > 0) {
       // this row of Q into tensor memory (rows past the chunk: zeros)
       const uint4* qrow =
@@ -788,8 +843,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bar.q_full);
     }
+    // whether the bias of a tile holds only 0 and the sentinel: loaded one tile ahead
+    bool pure_next = MODE == kBias && T > 0 && p.impure[imp0 + t_lo] == 0;
     for (int j = 0; j < T; ++j) {
       const int tile = t_lo + j, key0 = tile * kBN;
+      const bool pure = pure_next;
+      if (MODE == kBias && j + 1 < T) pure_next = p.impure[imp0 + tile + 1] == 0;
       // keys of the tile no row of the CTA attends (their V rows are zeroed)
       uint64_t dead0, dead1;
       if (C::kTerm) {
@@ -799,9 +858,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         dead0 = ~bit_range(rlo - key0, rhi - key0);
         dead1 = ~bit_range(rlo - key0 - 64, rhi - key0 - 64);
       }
-      // this row's allowed keys before the term test
+      // this row's allowed keys before the term test; a tile whose bias
+      // holds only 0 and the sentinel needs the plan's bits of the row alone
       uint64_t al0, al1;
-      if (kFusedMode) {
+      if (pure) {
+        const uint4 rb = *reinterpret_cast<const uint4*>(
+            p.rowmask + ((static_cast<int64_t>(b) * p.n_pt + pt) * kBM + row) * p.rm_stride + tile * 16);
+        al0 = rb.x | (static_cast<uint64_t>(rb.y) << 32);
+        al1 = rb.z | (static_cast<uint64_t>(rb.w) << 32);
+      } else if (kFusedMode) {
         al0 = bit_range(a1 - key0, b1 - key0) | bit_range(a2 - key0, b2 - key0);
         al1 = bit_range(a1 - key0 - 64, b1 - key0 - 64) | bit_range(a2 - key0 - 64, b2 - key0 - 64);
       } else {
@@ -817,14 +882,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const uint32_t ts = tl + (j & 1) * kBN;
       float t[kBN];
-      {
-        const int tb = j % C::kTB;
+      if (pure) {
+        // bits only: the fused path's scores (a bias of 0 adds nothing)
+        uint32_t sa[32], sb[32], tw[32];
+        ptx::tmem_ld32(ts, sa);
+        ptx::tmem_ld32(ts + 32, sb);
+        ptx::tmem_wait_ld();
+        if constexpr (capped) {
+          if (part0) half_scores_capped<0, false, true>(t, sa, sb, tw, al0, p.scale, p.softcap, lowest);
+          else half_scores_capped<0, false, false>(t, sa, sb, tw, al0, p.scale, p.softcap, lowest);
+        } else if (part0) {
+          half_scores<0, false, true>(t, sa, sb, tw, al0, sl2, lowest);
+        } else {
+          half_scores<0, false, false>(t, sa, sb, tw, al0, sl2, lowest);
+        }
+        ptx::tmem_ld32(ts + 64, sa);
+        ptx::tmem_ld32(ts + 96, sb);
+        ptx::tmem_wait_ld();
+        if constexpr (capped) {
+          if (part1) half_scores_capped<1, false, true>(t, sa, sb, tw, al1, p.scale, p.softcap, lowest);
+          else half_scores_capped<1, false, false>(t, sa, sb, tw, al1, p.scale, p.softcap, lowest);
+        } else if (part1) {
+          half_scores<1, false, true>(t, sa, sb, tw, al1, sl2, lowest);
+        } else {
+          half_scores<1, false, false>(t, sa, sb, tw, al1, sl2, lowest);
+        }
+      } else {
+        // term blocks arrive in the order of the tiles that need one
+        const int tb = t_seen % C::kTB;
         const uint8_t* tblk = sT + tb * C::kTermBytes;
         if (C::kTerm &&
-            !__all_sync(0xffffffffu, wait_or_abort(&bar.t_full[tb], (j / C::kTB) & 1, abort))) {
+            !__all_sync(0xffffffffu, wait_or_abort(&bar.t_full[tb], (t_seen / C::kTB) & 1, abort))) {
           ok = false;
           break;
         }
+        if (C::kTerm) ++t_seen;
         uint32_t sa[32], sb[32], tw[32];
         ptx::tmem_ld32(ts, sa);
         ptx::tmem_ld32(ts + 32, sb);
@@ -1084,10 +1176,25 @@ int prefill_splits(int64_t B, int64_t Hq, int64_t S_q) {
   return static_cast<int>(std::min<int64_t>(kMaxSplit, std::max<int64_t>(1, sms / ctas)));
 }
 
-// bytes of the column-mask table, rounded to 256 (the partials follow it)
+// bytes of the column-mask table, rounded to 256
 size_t colmask_bytes(int64_t B, int64_t S_q, int64_t max_seq) {
   const size_t n = static_cast<size_t>(B) * n_query_tiles(S_q) * n_mask_words(max_seq) * sizeof(uint64_t);
   return (n + 255) & ~size_t(255);
+}
+
+// 128-key tiles of the cache, and the row bits of a materialised bias: 16
+// bytes per (b, query tile, row, 128-key tile); then one byte per (b, query
+// tile, 128-key tile) saying whether the tile needs the bias values
+int n_key_tiles(int64_t max_seq) { return static_cast<int>((max_seq + kBN - 1) / kBN); }
+size_t rowmask_bytes(int64_t B, int64_t S_q, int64_t max_seq) {
+  return static_cast<size_t>(B) * n_query_tiles(S_q) * kBM * n_key_tiles(max_seq) * 16;
+}
+size_t impure_bytes(int64_t B, int64_t S_q, int64_t max_seq) {
+  return (static_cast<size_t>(B) * n_query_tiles(S_q) * n_key_tiles(max_seq) + 255) & ~size_t(255);
+}
+// the tables of a bias or extra term (the partials of key splits follow them)
+size_t term_tables_bytes(int64_t B, int64_t S_q, int64_t max_seq) {
+  return colmask_bytes(B, S_q, max_seq) + rowmask_bytes(B, S_q, max_seq) + impure_bytes(B, S_q, max_seq);
 }
 
 // Columns of Y one CTA produces: the whole value head size up to 256, else
@@ -1150,7 +1257,14 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
   prm.y = static_cast<__nv_bfloat16*>(a.y);
   prm.q = static_cast<const __nv_bfloat16*>(a.q);
   prm.nonpad = a.nonpad;
-  prm.colmask = static_cast<const uint64_t*>(a.workspace);
+  uint8_t* wsb = static_cast<uint8_t*>(a.workspace);
+  const size_t off_rowmask = colmask_bytes(a.B, a.S_q, a.max_seq);
+  const size_t off_impure = off_rowmask + rowmask_bytes(a.B, a.S_q, a.max_seq);
+  prm.colmask = reinterpret_cast<const uint64_t*>(wsb);
+  prm.rowmask = wsb + off_rowmask;
+  prm.impure = wsb + off_impure;
+  prm.n_kt = n_key_tiles(a.max_seq);
+  prm.rm_stride = prm.n_kt * 16;
   prm.spec = BiasSpec{a.causal, a.window, a.span_offsets, a.spans, a.extra, a.q_start};
   prm.scale_log2 = a.scale * kLog2e;
   prm.scale = a.scale;
@@ -1166,7 +1280,7 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
   prm.n_vc = static_cast<int>(Dvf / DV);
   prm.status = a.status;
   prm.n_split = prefill_splits(a.B, a.Hq * prm.n_vc, a.S_q);
-  prm.part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + colmask_bytes(a.B, a.S_q, a.max_seq));
+  prm.part = reinterpret_cast<float*>(wsb + term_tables_bytes(a.B, a.S_q, a.max_seq));
 
   if (MODE == kBias) {
     static std::once_flag plan_once;
@@ -1179,7 +1293,8 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
     prefill_plan_bias_kernel<<<dim3(n_plan_chunks(a.max_seq), prm.n_pt, prm.B), kPlanThreads, kPlanSmem,
                                a.stream>>>(static_cast<const __nv_bfloat16*>(term), a.nonpad,
                                            static_cast<uint64_t*>(a.workspace), prm.S_q, prm.max_seq,
-                                           prm.n_pt, prm.n_tiles, a.status);
+                                           prm.n_pt, prm.n_tiles, wsb + off_rowmask, prm.rm_stride,
+                                           wsb + off_impure, prm.n_kt, a.status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   } else if (MODE == kFusedExtra) {

@@ -151,3 +151,39 @@ def test_prefill_full_c3_sampled_rows_in_every_mode():
         assert g["kernel"] == PRE
         o = oracle_path(inp, rows=rows, mode=mode)
         assert max_err(g["y"], o["y"], rows) <= TOL[w.dtype]
+
+
+def test_prefill_bias_with_mask_only_and_dense_tiles_interleaved():
+    """A materialised bias whose 128-key tiles alternate between values 0 /
+    sentinel only (the kernel reads the plan's row bits) and other values (it
+    reads the bias): the term blocks of the dense tiles must pair with the
+    right tiles.  Also a NaN and a -0.0 inside mask-only tiles (NaN is masked,
+    -0.0 adds nothing), and a finite very negative value that stays unmasked.
+    The bias is built by the oracle and edited on the host."""
+    from helpers import from_raw, raw
+    import oracle
+    w = wl.Workload("pf_mixed_tiles", 208, B=2, Hq=4, Hkv=2, D=128, S_q=200, max_seq=1280,
+                    dtype=torch.bfloat16, causal=True, window=700, nonpad_range=(900, 1280))
+    inp = wl.make_inputs(w, "cuda")
+    nonpad = raw(inp.nonpad)
+    bias, bad = oracle.bias(nonpad, w.S_q, w.max_seq, "bf16", causal=True, window=w.window)
+    assert bad == 0
+    b16 = bias.copy()
+    rng = np.random.default_rng(5)
+    lowest = 0xFF7F
+    for t in (1, 3, 6):  # dense tiles: random values on the allowed slots
+        blk = b16[:, :, :, t * 128:(t + 1) * 128]
+        live = blk != lowest
+        vals = (rng.standard_normal(blk.shape) * 2).astype(np.float32)
+        bits = ((vals.view(np.uint32) + 0x7FFF + ((vals.view(np.uint32) >> 16) & 1)) >> 16).astype(np.uint16)
+        blk[live] = bits[live]
+    b16[0, 0, 150, 2 * 128 + 5] = 0x7FC1   # NaN in a mask-only tile
+    b16[1, 0, 10, 4 * 128 + 9] = 0x8000    # -0.0
+    b16[1, 0, 199, 5 * 128 + 77] = 0xFF70  # about -3.2e38: finite, not masked
+    y = torch.empty_like(inp.q)
+    with ek.use_algo(ek.ALGO_PREFILL):
+        ek.attention_ext_kv(y, inp.q, inp.k_cache, inp.v_cache, inp.nonpad, w.scale,
+                            bias=from_raw(b16, torch.bfloat16).cuda())
+        assert ek.extkv_last_kernel() == PRE
+    ref = oracle.attention(raw(inp.q), raw(inp.k_cache), raw(inp.v_cache), b16, nonpad, np.float32(w.scale))
+    assert max_err(y, ref) <= TOL[w.dtype]
