@@ -293,14 +293,18 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const __nv_b
       }
     }
     asm volatile("" ::: "memory");  // every row's load is issued before any is consumed
+    const __nv_bfloat162 lowest2 = __bfloat162bfloat162(__float2bfloat16_rn(lowest));
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
       const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      uint32_t m = 0;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        if (__uint_as_float(w4[q] << 16) > lowest) acc |= (1u << (2 * q)) & want[i];
-        if (__uint_as_float(w4[q] & 0xFFFF0000u) > lowest) acc |= (2u << (2 * q)) & want[i];
+        // 0xFFFF in each half whose value is above the sentinel (false for NaN)
+        const uint32_t live = __hgt2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w4[q]), lowest2);
+        m |= ((live & 1u) | ((live >> 15) & 2u)) << (2 * q);
       }
+      acc |= m & want[i];
     }
   }
   // lanes 4i .. 4i+3 share word i (32 keys)
