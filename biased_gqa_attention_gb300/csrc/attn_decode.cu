@@ -854,7 +854,7 @@ __host__ __device__ __forceinline__ int merge_slices(int G, int max_tiles) { ret
 
 template <int MODE>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
-  constexpr int kPre = 8;  // slices whose partial rows a thread loads before the weights are known
+  constexpr int kPre = 16;  // slices whose partial rows a thread loads before the weights are known
   extern __shared__ float sm_raw[];  // [NS][kRows] maxima, then [NS][kRows] sums
   const int tid = threadIdx.x;
   const int u = blockIdx.x;
