@@ -76,3 +76,36 @@ def test_c1_prefill_then_decode_fp32():
     o2 = oracle_path(dec, mode="bias", k_cache=o1["k"], v_cache=o1["v"])
     assert _bits_equal(g2["k"], o2["k"]) and _bits_equal(g2["bias"], o2["bias"])
     assert max_err(g2["y"], o2["y"]) <= 1e-5
+
+
+@pytest.mark.parametrize("S_q", [1, 2])
+def test_decode_bias_mask_only_and_valued_batches(S_q):
+    """Decode with a materialised bias whose batches differ: mask-only rows
+    (0 and the sentinel) and rows carrying other values (finite, a very
+    negative finite value that stays unmasked, a NaN that masks, a -0.0 that
+    adds nothing).  The bias is built by the oracle and edited on the host."""
+    from helpers import from_raw
+    import oracle
+    w = wl.Workload("dec_mixed_bias", 209, B=5, Hq=8, Hkv=4, D=128, S_q=S_q, max_seq=1024,
+                    dtype=torch.bfloat16, causal=True, window=300, nonpad_range=(200, 1024))
+    inp = wl.make_inputs(w, "cuda")
+    nonpad = raw(inp.nonpad)
+    bias, bad = oracle.bias(nonpad, w.S_q, w.max_seq, "bf16", causal=True, window=w.window)
+    assert bad == 0
+    b16 = bias.copy()
+    lowest = 0xFF7F
+    rng = np.random.default_rng(9)
+    live1 = np.nonzero(b16[1, 0, 0] != lowest)[0]
+    vals = (rng.standard_normal(live1.size) * 2).astype(np.float32).view(np.uint32)
+    b16[1, 0, 0, live1] = ((vals + 0x7FFF + ((vals >> 16) & 1)) >> 16).astype(np.uint16)  # valued row
+    live2 = np.nonzero(b16[2, 0, -1] != lowest)[0]
+    b16[2, 0, -1, live2[len(live2) // 2]] = 0x7FC1      # NaN: masked
+    live3 = np.nonzero(b16[3, 0, -1] != lowest)[0]
+    b16[3, 0, -1, live3[0]] = 0x8000                    # -0.0
+    b16[4, 0, 0, live1[-1] if live1[-1] < nonpad[4] else 0] = 0xFF70  # about -3.2e38, not masked
+    bias_t = from_raw(b16, torch.bfloat16).cuda()
+    y = torch.empty_like(inp.q)
+    ek.attention_ext_kv(y, inp.q, inp.k_cache, inp.v_cache, inp.nonpad, w.scale, bias=bias_t)
+    assert ek.extkv_last_kernel().startswith("attn_decode")
+    ref = oracle.attention(raw(inp.q), raw(inp.k_cache), raw(inp.v_cache), b16, nonpad, np.float32(w.scale))
+    assert max_err(y, ref) <= TOL[w.dtype]
