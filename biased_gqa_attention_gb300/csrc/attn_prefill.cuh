@@ -68,7 +68,7 @@ namespace {
 
 constexpr int kBM = 128;                   // query rows per CTA (M, tensor-memory lanes)
 constexpr int kBN = 128;                   // keys per KV tile (N of S = Q K^T)
-constexpr int kThreads = 192;              // producer, MMA, 4 softmax warps
+constexpr int kMaxThreads = 320;           // producer, MMA, 4 or 8 softmax warps
 constexpr int kPlanKeys = 256;             // keys per plan block (8 per lane)
 constexpr int kPlanThreads = 256;
 constexpr uint32_t kWaitPolls = 1u << 22;  // bounded mbarrier waits
@@ -88,6 +88,12 @@ enum Mode { kNone = 0, kBias = 1, kFused = 2, kFusedExtra = 3 };
 template <int DK, int DV, int MODE>
 struct Cfg {
   static constexpr bool kTerm = MODE == kBias || MODE == kFusedExtra;  // a 128 x 128 block per tile
+  // Softmax warps: with DV <= 128 a tile's tensor work (~1.2 k cycles) is
+  // shorter than one thread's softmax of a 128-key row, so two warps share
+  // each tensor-memory lane quadrant, one per 64-key half of the tile.
+  static constexpr bool kSplit = DV <= 128 && DK <= 128;
+  static constexpr int kSoftWarps = kSplit ? 8 : 4;
+  static constexpr int kThreads = 64 + 32 * kSoftWarps;
   // Q as a shared-memory A operand where tensor memory has no room for it
   static constexpr bool kQSmem = 256 + DV + DK / 2 > 512;
   static constexpr int kKP = DK > 128 ? DK / 128 : 1;  // load units of a K tile
@@ -101,7 +107,8 @@ struct Cfg {
   static constexpr int kTermBytes = kTerm ? kBM * kBN * 2 : 0;
   static constexpr int kTermBufs = kTerm ? (kQSmem ? 1 : 2) : 0;
   static constexpr int kTB = kTermBufs > 0 ? kTermBufs : 1;  // divisor for buffer indexing
-  static constexpr int kBudget = 232448 - 1024 - 512;  // opt-in maximum, alignment, barriers
+  static constexpr int kXchBytes = kSplit ? 2 * 2 * kBM * 4 : 0;  // [tile parity][half][row] floats
+  static constexpr int kBudget = 232448 - 1024 - 512 - kXchBytes;  // opt-in maximum, alignment, barriers, exchange
   static constexpr int kFit = (kBudget - kQBytes - kTermBufs * kTermBytes) / kUnitBytes;
   static constexpr int kNU = kFit > kMaxUnits ? kMaxUnits : kFit;
   static constexpr int kOffQ = 0;
@@ -109,7 +116,8 @@ struct Cfg {
   static constexpr int kOffT = kOffKV + kNU * kUnitBytes;
   static_assert(kNU * kUnitBytes >= 4 * (DV / 64) * 4096, "the epilogue stages 128 rows x DV in the K/V ring");
   static constexpr int kOffBar = kOffT + kTermBufs * kTermBytes;
-  static constexpr int kSmem = kOffBar + 512 + 1024;
+  static constexpr int kOffXch = kOffBar + 512;
+  static constexpr int kSmem = kOffXch + kXchBytes + 1024;
   // tensor memory: S_0, S_1 at columns 0 and 128 (P_j, bf16, over the first 64
   // columns of S_j), O at 256, Q (when held there) after O
   static constexpr uint32_t kOCol = 256;
@@ -128,6 +136,7 @@ struct Bars {
   uint64_t u_full[kMaxUnits], u_empty[kMaxUnits];
   uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t v_ready[2];  // V_j has landed (MMA thread): dead V rows may be zeroed
+  uint64_t xch[4][2];   // split softmax: both warps of lane quadrant q wrote slot [parity]
   uint64_t t_full[2], t_empty[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -170,6 +179,17 @@ __host__ __device__ constexpr int part_stride(int D) { return D + 4; }
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
   for (uint32_t i = 0; i < kWaitPolls; ++i) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((i & 127u) == 127u && *abort) return false;
+  }
+  *abort = 1;
+  return false;
+}
+
+// Bounded wait polling with test_wait (no suspension): for short hand-offs
+// between warps that are usually already complete.
+__device__ __forceinline__ bool spin_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    if (ptx::mbar_test_wait(bar, parity)) return true;
     if ((i & 127u) == 127u && *abort) return false;
   }
   *abort = 1;
@@ -434,8 +454,8 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_bias_kernel(const _
 // Scores of 64 keys (half H of a tile) in base 2: t = scale*log2(e)*s
 // (+ log2(e)*term), -inf where the key is masked: outside the row's allowed
 // keys (PARTIAL halves only; `allowed` bit c) or, with a term, term <= lowest.
-template <int H, bool TERM, bool PARTIAL>
-__device__ __forceinline__ void half_scores(float (&t)[kBN], const uint32_t (&sa)[32], const uint32_t (&sb)[32],
+template <int H, bool TERM, bool PARTIAL, int N>
+__device__ __forceinline__ void half_scores(float (&t)[N], const uint32_t (&sa)[32], const uint32_t (&sb)[32],
                                             const uint32_t (&tw)[32], uint64_t allowed, float sl2, float lowest) {
   const uint64_t sl2x2 = ptx::f2(sl2, sl2);
   const uint64_t l2e = ptx::f2(kLog2e, kLog2e);
@@ -465,8 +485,8 @@ __device__ __forceinline__ void half_scores(float (&t)[kBN], const uint32_t (&sa
 
 // The same with the softcap of the ORT page's section 4 op order: the scaled
 // score x = scale*s becomes cap*tanh(x/cap) before the term is added.
-template <int H, bool TERM, bool PARTIAL>
-__device__ __forceinline__ void half_scores_capped(float (&t)[kBN], const uint32_t (&sa)[32], const uint32_t (&sb)[32],
+template <int H, bool TERM, bool PARTIAL, int N>
+__device__ __forceinline__ void half_scores_capped(float (&t)[N], const uint32_t (&sa)[32], const uint32_t (&sb)[32],
                                                    const uint32_t (&tw)[32], uint64_t allowed, float scale, float cap,
                                                    float lowest) {
 #pragma unroll
@@ -498,6 +518,20 @@ __device__ __forceinline__ float tile_max(const float (&t)[kBN]) {
   return ptx::max3(ptx::max3(acc[0], acc[1], acc[2]), ptx::max3(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7]));
 }
 
+// The maximum of 64 values (one half of a tile).
+__device__ __forceinline__ float half_max(const float (&t)[64]) {
+  float acc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    // the 8 values t[k + 8m], m = 0 .. 7
+    acc[k] = ptx::max3(t[k], t[k + 8], t[k + 16]);
+    acc[k] = ptx::max3(acc[k], t[k + 24], t[k + 32]);
+    acc[k] = ptx::max3(acc[k], t[k + 40], t[k + 48]);
+    acc[k] = fmaxf(acc[k], t[k + 56]);
+  }
+  return ptx::max3(ptx::max3(acc[0], acc[1], acc[2]), ptx::max3(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7]));
+}
+
 // The 128-byte row `row` of a 64-key block stored with the 128-byte swizzle.
 __device__ __forceinline__ void load_swizzled_row(uint32_t (&w)[32], const uint8_t* blk, int row) {
   const uint8_t* r = blk + row * 128;
@@ -516,7 +550,7 @@ __device__ __forceinline__ void load_swizzled_row(uint32_t (&w)[32], const uint8
 // CAP: the scores are softcapped (a separate instantiation, so that the
 // uncapped kernel is compiled as if the cap did not exist).
 template <int DK, int DV, int MODE, bool CAP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap tmap,
                         const __grid_constant__ CUtensorMap ymap, const PrefillParams p) {
@@ -540,18 +574,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = pt * kBM;
 
   if (tid == 0) {
-    ptx::mbar_init(&bar.q_full, C::kQSmem ? 1 : 4 * 32);
+    ptx::mbar_init(&bar.q_full, C::kQSmem ? 1 : C::kSoftWarps * 32);
     for (int s = 0; s < C::kNU; ++s) {
       ptx::mbar_init(&bar.u_full[s], 1);
       ptx::mbar_init(&bar.u_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&bar.s_full[s], 1);
-      ptx::mbar_init(&bar.p_full[s], 4 * 32);
+      ptx::mbar_init(&bar.p_full[s], C::kSoftWarps * 32);
       ptx::mbar_init(&bar.pv_done[s], 1);
       ptx::mbar_init(&bar.v_ready[s], 1);
+      for (int q = 0; q < 4; ++q) ptx::mbar_init(&bar.xch[q][s], 64);
       ptx::mbar_init(&bar.t_full[s], 1);
-      ptx::mbar_init(&bar.t_empty[s], 4);
+      ptx::mbar_init(&bar.t_empty[s], C::kSoftWarps);
     }
     ptx::mbar_init(&bar.drain, 1);
     bar.range_lo = INT_MAX;
@@ -820,6 +855,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- softmax and epilogue (one query row per thread) ----------------
     const uint32_t tl = tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    // split softmax: warps 2-5 score keys 0-63 of each tile, warps 6-9 keys
+    // 64-127 of the same rows; each pair meets once per tile for the maximum
+    const int hh = C::kSplit ? (warp - 2) >> 2 : 0;
+    const int quad = warp & 3;
+    float* xch = reinterpret_cast<float*>(sm + C::kOffXch);  // [parity][half][row]
     const float sl2 = p.scale_log2;
     constexpr bool capped = CAP;
     const float lowest = Elem<__nv_bfloat16>::lowest();
@@ -832,6 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           reinterpret_cast<const uint4*>(p.q + ((static_cast<int64_t>(b) * p.Hq + h) * p.S_q + q0 + row) * DK);
 #pragma unroll
       for (int c = 0; c < DK / 64; ++c) {
+        if (C::kSplit && (c & 1) != hh) continue;  // the pair shares the chunks
         uint32_t r[32];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -885,123 +926,221 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_after();
       const uint32_t ts = tl + (j & 1) * kBN;
-      float t[kBN];
-      if (pure) {
-        // bits only: the fused path's scores (a bias of 0 adds nothing)
-        uint32_t sa[32], sb[32], tw[32];
-        ptx::tmem_ld32(ts, sa);
-        ptx::tmem_ld32(ts + 32, sb);
-        ptx::tmem_wait_ld();
-        if constexpr (capped) {
-          if (part0) half_scores_capped<0, false, true>(t, sa, sb, tw, al0, p.scale, p.softcap, lowest);
-          else half_scores_capped<0, false, false>(t, sa, sb, tw, al0, p.scale, p.softcap, lowest);
-        } else if (part0) {
-          half_scores<0, false, true>(t, sa, sb, tw, al0, sl2, lowest);
-        } else {
-          half_scores<0, false, false>(t, sa, sb, tw, al0, sl2, lowest);
+      if constexpr (C::kSplit) {
+        // this warp's half of the tile: keys 64 hh .. 64 hh + 63
+        const uint64_t al = hh ? al1 : al0;
+        const bool part = hh ? part1 : part0;
+        const bool termed = C::kTerm && !pure;
+        float t[64];
+        {
+          uint32_t sa[32], sb[32], tw[32];
+          ptx::tmem_ld32(ts + 64 * hh, sa);
+          ptx::tmem_ld32(ts + 64 * hh + 32, sb);
+          if (termed) {
+            // term blocks arrive in the order of the tiles that need one
+            const int tb = t_seen % C::kTB;
+            if (!__all_sync(0xffffffffu, wait_or_abort(&bar.t_full[tb], (t_seen / C::kTB) & 1, abort))) {
+              ok = false;
+              break;
+            }
+            ++t_seen;
+            load_swizzled_row(tw, sT + tb * C::kTermBytes + hh * (C::kTermBytes / 2), row);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bar.t_empty[tb]);
+          }
+          ptx::tmem_wait_ld();
+          if constexpr (capped) {
+            if (termed) {
+              if (part) half_scores_capped<0, true, true>(t, sa, sb, tw, al, p.scale, p.softcap, lowest);
+              else half_scores_capped<0, true, false>(t, sa, sb, tw, al, p.scale, p.softcap, lowest);
+            } else if (part) {
+              half_scores_capped<0, false, true>(t, sa, sb, tw, al, p.scale, p.softcap, lowest);
+            } else {
+              half_scores_capped<0, false, false>(t, sa, sb, tw, al, p.scale, p.softcap, lowest);
+            }
+          } else if (termed) {
+            if (part) half_scores<0, true, true>(t, sa, sb, tw, al, sl2, lowest);
+            else half_scores<0, true, false>(t, sa, sb, tw, al, sl2, lowest);
+          } else if (part) {
+            half_scores<0, false, true>(t, sa, sb, tw, al, sl2, lowest);
+          } else {
+            half_scores<0, false, false>(t, sa, sb, tw, al, sl2, lowest);
+          }
         }
-        ptx::tmem_ld32(ts + 64, sa);
-        ptx::tmem_ld32(ts + 96, sb);
-        ptx::tmem_wait_ld();
-        if constexpr (capped) {
-          if (part1) half_scores_capped<1, false, true>(t, sa, sb, tw, al1, p.scale, p.softcap, lowest);
-          else half_scores_capped<1, false, false>(t, sa, sb, tw, al1, p.scale, p.softcap, lowest);
-        } else if (part1) {
-          half_scores<1, false, true>(t, sa, sb, tw, al1, sl2, lowest);
-        } else {
-          half_scores<1, false, false>(t, sa, sb, tw, al1, sl2, lowest);
-        }
-      } else {
-        // term blocks arrive in the order of the tiles that need one
-        const int tb = t_seen % C::kTB;
-        const uint8_t* tblk = sT + tb * C::kTermBytes;
-        if (C::kTerm &&
-            !__all_sync(0xffffffffu, wait_or_abort(&bar.t_full[tb], (t_seen / C::kTB) & 1, abort))) {
-          ok = false;
-          break;
-        }
-        if (C::kTerm) ++t_seen;
-        uint32_t sa[32], sb[32], tw[32];
-        ptx::tmem_ld32(ts, sa);
-        ptx::tmem_ld32(ts + 32, sb);
-        if (C::kTerm) load_swizzled_row(tw, tblk, row);
-        ptx::tmem_wait_ld();
-        if constexpr (capped) {
-          if (part0)
-            half_scores_capped<0, C::kTerm, true>(t, sa, sb, tw, al0, p.scale, p.softcap, lowest);
-          else
-            half_scores_capped<0, C::kTerm, false>(t, sa, sb, tw, al0, p.scale, p.softcap, lowest);
-        } else if (part0) {
-          half_scores<0, C::kTerm, true>(t, sa, sb, tw, al0, sl2, lowest);
-        } else {
-          half_scores<0, C::kTerm, false>(t, sa, sb, tw, al0, sl2, lowest);
-        }
-        ptx::tmem_ld32(ts + 64, sa);
-        ptx::tmem_ld32(ts + 96, sb);
-        if (C::kTerm) {
-          load_swizzled_row(tw, tblk + C::kTermBytes / 2, row);
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&bar.t_empty[tb]);
-        }
-        ptx::tmem_wait_ld();
-        if constexpr (capped) {
-          if (part1)
-            half_scores_capped<1, C::kTerm, true>(t, sa, sb, tw, al1, p.scale, p.softcap, lowest);
-          else
-            half_scores_capped<1, C::kTerm, false>(t, sa, sb, tw, al1, p.scale, p.softcap, lowest);
-        } else if (part1) {
-          half_scores<1, C::kTerm, true>(t, sa, sb, tw, al1, sl2, lowest);
-        } else {
-          half_scores<1, C::kTerm, false>(t, sa, sb, tw, al1, sl2, lowest);
-        }
-      }
-      const float mt = tile_max(t);
-      // lazy rescale: only when the running maximum grows by more than 2^8
-      const float m_new = fmaxf(m_run, mt);
-      const bool grow = m_new > m_run + 8.f;  // false while the row has no unmasked key
-      const bool rescale_o = grow && m_run != -INFINITY;
-      const float factor = rescale_o ? ptx::ex2(m_run - m_new) : 1.f;
-      if (__any_sync(0xffffffffu, rescale_o)) {
-        // the output accumulator holds P_{j-1} V_{j-1} once that product completes
-        if (!__all_sync(0xffffffffu, wait_or_abort(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort))) {
+        // the tile's maximum: both halves' maxima through shared memory, the
+        // pair's 64 threads meeting on the quadrant's barrier of this parity.
+        // The meeting also orders the pair's tensor-memory accesses: P of keys
+        // 64-127 goes over S columns 32-63, which the other warp has read by
+        // the time it arrives.
+        float* xm = xch + (j & 1) * 2 * kBM;
+        xm[hh * kBM + row] = half_max(t);
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&bar.xch[quad][j & 1]);
+        if (!__all_sync(0xffffffffu, spin_or_abort(&bar.xch[quad][j & 1], (j >> 1) & 1, abort))) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
+        const float mt = fmaxf(xm[row], xm[kBM + row]);  // the same in both warps
+        const float m_new = fmaxf(m_run, mt);
+        const bool grow = m_new > m_run + 8.f;
+        const bool rescale_o = grow && m_run != -INFINITY;
+        const float factor = rescale_o ? ptx::ex2(m_run - m_new) : 1.f;
+        if (__any_sync(0xffffffffu, rescale_o)) {
+          // this warp's half of the output columns, once P_{j-1} V_{j-1} completed
+          if (!__all_sync(0xffffffffu, wait_or_abort(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort))) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < DV / 32; ++c) {
-          uint32_t o[32];
-          ptx::tmem_ld32(tl + C::kOCol + 32 * c, o);
-          ptx::tmem_wait_ld();
+          for (int c = hh * (DV / 64); c < (hh + 1) * (DV / 64); ++c) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tl + C::kOCol + 32 * c, o);
+            ptx::tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
-          ptx::tmem_st32(tl + C::kOCol + 32 * c, o);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+            ptx::tmem_st32(tl + C::kOCol + 32 * c, o);
+          }
+          ptx::tmem_wait_st();
         }
-        ptx::tmem_wait_st();
-      }
-      if (grow) {
-        l_run *= factor;
-        m_run = m_new;
-      }
-      const float m_use = m_run == -INFINITY ? 0.f : m_run;
-      const uint64_t nm = ptx::f2(-m_use, -m_use);
-      uint64_t ls[4] = {0, 0, 0, 0};
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
+        if (grow) {
+          l_run *= factor;
+          m_run = m_new;
+        }
+        const float m_use = m_run == -INFINITY ? 0.f : m_run;
+        const uint64_t nm = ptx::f2(-m_use, -m_use);
+        uint64_t ls[4] = {0, 0, 0, 0};
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const uint64_t d = ptx::add2(ptx::f2(t[64 * hh + 2 * c], t[64 * hh + 2 * c + 1]), nm);
+          const uint64_t d = ptx::add2(ptx::f2(t[2 * c], t[2 * c + 1]), nm);
           const float e0 = ptx::ex2(ptx::f2_lo(d)), e1 = ptx::ex2(ptx::f2_hi(d));
           ls[c & 3] = ptx::add2(ls[c & 3], ptx::f2(e0, e1));
           pk[c] = ptx::pack_bf16x2(e0, e1);
         }
-        // P_j over the first half of S_j: QK_{j+2}, the next writer of this
-        // buffer, is issued after P_j V_j and the tensor pipe runs in order
-        ptx::tmem_st32(ts + 32 * hh, pk);
+        ptx::tmem_st32(ts + 32 * hh, pk);  // this half's P over S_j's first half
+        const uint64_t lsum = ptx::add2(ptx::add2(ls[0], ls[1]), ptx::add2(ls[2], ls[3]));
+        l_run += ptx::f2_lo(lsum) + ptx::f2_hi(lsum);  // this half's share of the row sum
+      } else {
+        float t[kBN];
+        if (pure) {
+          // bits only: the fused path's scores (a bias of 0 adds nothing)
+          uint32_t sa[32], sb[32], tw[32];
+          ptx::tmem_ld32(ts, sa);
+          ptx::tmem_ld32(ts + 32, sb);
+          ptx::tmem_wait_ld();
+          if constexpr (capped) {
+            if (part0) half_scores_capped<0, false, true>(t, sa, sb, tw, al0, p.scale, p.softcap, lowest);
+            else half_scores_capped<0, false, false>(t, sa, sb, tw, al0, p.scale, p.softcap, lowest);
+          } else if (part0) {
+            half_scores<0, false, true>(t, sa, sb, tw, al0, sl2, lowest);
+          } else {
+            half_scores<0, false, false>(t, sa, sb, tw, al0, sl2, lowest);
+          }
+          ptx::tmem_ld32(ts + 64, sa);
+          ptx::tmem_ld32(ts + 96, sb);
+          ptx::tmem_wait_ld();
+          if constexpr (capped) {
+            if (part1) half_scores_capped<1, false, true>(t, sa, sb, tw, al1, p.scale, p.softcap, lowest);
+            else half_scores_capped<1, false, false>(t, sa, sb, tw, al1, p.scale, p.softcap, lowest);
+          } else if (part1) {
+            half_scores<1, false, true>(t, sa, sb, tw, al1, sl2, lowest);
+          } else {
+            half_scores<1, false, false>(t, sa, sb, tw, al1, sl2, lowest);
+          }
+        } else {
+          // term blocks arrive in the order of the tiles that need one
+          const int tb = t_seen % C::kTB;
+          const uint8_t* tblk = sT + tb * C::kTermBytes;
+          if (C::kTerm &&
+              !__all_sync(0xffffffffu, wait_or_abort(&bar.t_full[tb], (t_seen / C::kTB) & 1, abort))) {
+            ok = false;
+            break;
+          }
+          if (C::kTerm) ++t_seen;
+          uint32_t sa[32], sb[32], tw[32];
+          ptx::tmem_ld32(ts, sa);
+          ptx::tmem_ld32(ts + 32, sb);
+          if (C::kTerm) load_swizzled_row(tw, tblk, row);
+          ptx::tmem_wait_ld();
+          if constexpr (capped) {
+            if (part0)
+              half_scores_capped<0, C::kTerm, true>(t, sa, sb, tw, al0, p.scale, p.softcap, lowest);
+            else
+              half_scores_capped<0, C::kTerm, false>(t, sa, sb, tw, al0, p.scale, p.softcap, lowest);
+          } else if (part0) {
+            half_scores<0, C::kTerm, true>(t, sa, sb, tw, al0, sl2, lowest);
+          } else {
+            half_scores<0, C::kTerm, false>(t, sa, sb, tw, al0, sl2, lowest);
+          }
+          ptx::tmem_ld32(ts + 64, sa);
+          ptx::tmem_ld32(ts + 96, sb);
+          if (C::kTerm) {
+            load_swizzled_row(tw, tblk + C::kTermBytes / 2, row);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bar.t_empty[tb]);
+          }
+          ptx::tmem_wait_ld();
+          if constexpr (capped) {
+            if (part1)
+              half_scores_capped<1, C::kTerm, true>(t, sa, sb, tw, al1, p.scale, p.softcap, lowest);
+            else
+              half_scores_capped<1, C::kTerm, false>(t, sa, sb, tw, al1, p.scale, p.softcap, lowest);
+          } else if (part1) {
+            half_scores<1, C::kTerm, true>(t, sa, sb, tw, al1, sl2, lowest);
+          } else {
+            half_scores<1, C::kTerm, false>(t, sa, sb, tw, al1, sl2, lowest);
+          }
+        }
+        const float mt = tile_max(t);
+        // lazy rescale: only when the running maximum grows by more than 2^8
+        const float m_new = fmaxf(m_run, mt);
+        const bool grow = m_new > m_run + 8.f;  // false while the row has no unmasked key
+        const bool rescale_o = grow && m_run != -INFINITY;
+        const float factor = rescale_o ? ptx::ex2(m_run - m_new) : 1.f;
+        if (__any_sync(0xffffffffu, rescale_o)) {
+          // the output accumulator holds P_{j-1} V_{j-1} once that product completes
+          if (!__all_sync(0xffffffffu, wait_or_abort(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort))) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+  #pragma unroll 1
+          for (int c = 0; c < DV / 32; ++c) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tl + C::kOCol + 32 * c, o);
+            ptx::tmem_wait_ld();
+  #pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+            ptx::tmem_st32(tl + C::kOCol + 32 * c, o);
+          }
+          ptx::tmem_wait_st();
+        }
+        if (grow) {
+          l_run *= factor;
+          m_run = m_new;
+        }
+        const float m_use = m_run == -INFINITY ? 0.f : m_run;
+        const uint64_t nm = ptx::f2(-m_use, -m_use);
+        uint64_t ls[4] = {0, 0, 0, 0};
+  #pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t pk[32];
+  #pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const uint64_t d = ptx::add2(ptx::f2(t[64 * hh + 2 * c], t[64 * hh + 2 * c + 1]), nm);
+            const float e0 = ptx::ex2(ptx::f2_lo(d)), e1 = ptx::ex2(ptx::f2_hi(d));
+            ls[c & 3] = ptx::add2(ls[c & 3], ptx::f2(e0, e1));
+            pk[c] = ptx::pack_bf16x2(e0, e1);
+          }
+          // P_j over the first half of S_j: QK_{j+2}, the next writer of this
+          // buffer, is issued after P_j V_j and the tensor pipe runs in order
+          ptx::tmem_st32(ts + 32 * hh, pk);
+        }
+        const uint64_t lsum = ptx::add2(ptx::add2(ls[0], ls[1]), ptx::add2(ls[2], ls[3]));
+        l_run += ptx::f2_lo(lsum) + ptx::f2_hi(lsum);
       }
-      const uint64_t lsum = ptx::add2(ptx::add2(ls[0], ls[1]), ptx::add2(ls[2], ls[3]));
-      l_run += ptx::f2_lo(lsum) + ptx::f2_hi(lsum);
       if (dead0 | dead1) {
         // zero the V rows of dead keys once V_j has landed (the MMA thread,
         // which consumes the units in order, says so: a parity wait on the
@@ -1015,7 +1154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int slot = (v_unit<kKP, kVP>(j, T) + part) % C::kNU;
           uint8_t* vt = sKV + slot * C::kUnitBytes;
           constexpr int kLines = C::kVKeys * (DV / 64) * 8;  // 16-byte pieces of the unit
-          for (int w = tid - 64; w < kLines; w += 128) {
+          for (int w = tid - 64; w < kLines; w += 32 * C::kSoftWarps) {
             const int kl = w / ((DV / 64) * 8), rem = w % ((DV / 64) * 8);
             const int key = part * C::kVKeys + kl;
             const uint64_t dm = key < 64 ? dead0 : dead1;
@@ -1035,7 +1174,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         !__all_sync(0xffffffffu, wait_or_abort(&bar.pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort)))
       ok = false;
     ptx::tc_fence_after();
+    if constexpr (C::kSplit) {
+      // the row's sum: both halves' shares, added in the same order in both warps
+      float* xl = xch + (T & 1) * 2 * kBM;
+      xl[hh * kBM + row] = l_run;
+      ptx::mbar_arrive(&bar.xch[quad][T & 1]);
+      if (!__all_sync(0xffffffffu, spin_or_abort(&bar.xch[quad][T & 1], (T >> 1) & 1, abort))) ok = false;
+      l_run = xl[row] + xl[kBM + row];
+    }
     const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    // output columns of this warp: all of them, or its half with the split softmax
+    constexpr int kNB = DV / 64;  // 64-column blocks
+    const int c32_lo = C::kSplit ? hh * (DV / 64) : 0, c32_hi = C::kSplit ? (hh + 1) * (DV / 64) : DV / 32;
+    const int cb_lo = C::kSplit ? (kNB >= 2 ? hh * (kNB / 2) : (hh ? kNB : 0)) : 0;
+    const int cb_hi = C::kSplit ? (kNB >= 2 ? (hh + 1) * (kNB / 2) : kNB) : kNB;
     // The warp's 32 rows go through shared memory (the K/V ring is idle now:
     // every MMA that read it has completed) in 32 x 64-column blocks with the
     // 128-byte swizzle, and leave as one TMA store per block; rows beyond S_q
@@ -1047,7 +1199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  part_stride(p.Dv);
       const bool live = ok && T > 0;
 #pragma unroll 1
-      for (int c = 0; c < DV / 32; ++c) {
+      for (int c = c32_lo; c < c32_hi; ++c) {
         uint32_t o[32];
         if (live) {
           ptx::tmem_ld32(tl + C::kOCol + 32 * c, o);
@@ -1064,14 +1216,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             __uint_as_float(o[4 * q + 3]));
         }
       }
-      if (row_valid && vc == 0) {
+      if (row_valid && vc == 0 && hh == 0) {
         prow[p.Dv] = live ? m_run : -INFINITY;
         prow[p.Dv + 1] = live ? l_run : 0.f;
       }
     } else {
-      uint8_t* stage = sKV + (warp & 3) * (DV / 64) * 4096;
+      uint8_t* stage = sKV + quad * kNB * 4096;
 #pragma unroll 1
-      for (int cb = 0; cb < DV / 64; ++cb) {
+      for (int cb = cb_lo; cb < cb_hi; ++cb) {
         uint32_t o[64];
         if (ok && T > 0) {
           ptx::tmem_ld32(tl + C::kOCol + 64 * cb, *reinterpret_cast<uint32_t(*)[32]>(o));
@@ -1094,7 +1246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::fence_proxy_async_smem();  // the staged rows, visible to the TMA store
       __syncwarp();
       if (ok && lane == 0 && q0 + 32 * (warp & 3) < p.S_q) {  // a box wholly past S_q writes nothing
-        for (int cb = 0; cb < DV / 64; ++cb)
+        for (int cb = cb_lo; cb < cb_hi; ++cb)
           ptx::tma_store_3d(&ymap, stage + cb * 4096, vc * DV + cb * 64, q0 + 32 * (warp & 3), b * p.Hq + h);
         ptx::bulk_commit_group();
         ptx::bulk_wait_read_all();  // shared memory stays valid until the stores have read it
@@ -1311,7 +1463,7 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(prm.Hq * prm.n_vc * prm.n_split, prm.n_pt, prm.B);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = a.stream;
   cudaLaunchAttribute attr[1];
