@@ -17,7 +17,7 @@
 // head_size != v_head_size); a value head size of 512 is covered by two CTAs
 // that share the scores' work and write 256 columns each, because S_0, S_1
 // and O must fit the 512 tensor-memory columns.
-// The CTA is warp-specialised (192 threads):
+// The CTA is warp-specialised (192 threads; 320 with the split softmax):
 //   warp 0   TMA producer: K_0, K_1, V_0, K_2, V_1, ... through a ring of
 //            shared-memory slots (one request per load unit via a permuted
 //            4-D view that lands the 128-byte-swizzled per-64-column layout),
@@ -35,6 +35,9 @@
 //            also copy the Q tile into tensor memory at the start.
 //            Epilogue: O / l from tensor memory to Y (bf16), zero rows where no
 //            key is unmasked.
+//   warps 2-9  (head sizes up to 128) the same with two warps per query row,
+//            one per 64-key half of each tile; the pair exchanges its half
+//            maxima once per tile and its sums at the end.
 // Tensor memory: S_0, S_1 (128 columns each), O (DV columns), Q (DK/2
 // columns) when held there.
 //
