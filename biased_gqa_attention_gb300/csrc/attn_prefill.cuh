@@ -341,15 +341,17 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const __nv_b
   }
 }
 
-// The same table for a materialised bias: each block stages its 128 x 256
-// bias block in shared memory with one bulk copy per row (all in flight at
-// once), then every thread ORs 16 rows of its 8 keys.  It also writes, per
-// query row and 128-key tile, the bits of the keys the row may attend
-// (rowmask: 16 bytes per row and tile, rm_stride bytes per row), and per
-// (query tile, 128-key tile) whether the bias holds a value other than 0 and
-// the masked sentinel inside the live keys (impure).  Where it does not, the
-// attention kernel needs only the bits: adding a bias of 0 changes no score.
-constexpr int kPlanSmem = kBM * kPlanKeys * 2 + 64;
+// The same table for a materialised bias: each block stages the 128 x 128
+// bias block of one key tile in shared memory (32 KB, so seven blocks fit an
+// SM and a whole query tile's row of blocks is in flight at once) with one
+// bulk copy per row, all in flight together, then thread (g, k) ORs rows
+// g, g + 16, ... of keys 8k .. 8k + 7.  It also writes, per query row and
+// 128-key tile, the bits of the keys the row may attend (rowmask: 16 bytes
+// per row and tile, rm_stride bytes per row), and per (query tile, 128-key
+// tile) whether the bias holds a value other than 0 and the sentinel inside
+// the live keys (impure).  Where it does not, the attention kernel needs only
+// the bits: adding a bias of 0 changes no score.
+constexpr int kPlanSmem = kBM * kBN * 2 + 64;
 
 __global__ void __launch_bounds__(kPlanThreads) prefill_plan_bias_kernel(const __nv_bfloat16* __restrict__ bias,
                                                                         const int64_t* __restrict__ nonpad,
@@ -358,33 +360,31 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_bias_kernel(const _
                                                                         uint8_t* __restrict__ rowmask, int rm_stride,
                                                                         uint8_t* __restrict__ impure, int n_kt,
                                                                         int32_t* status) {
+  constexpr int kGroups = kPlanThreads / (kBN / 8);  // row groups (16): thread = (group, 8-key column)
   extern __shared__ __align__(128) uint8_t plan_smem[];
   uint16_t* rows_s = reinterpret_cast<uint16_t*>(plan_smem);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(plan_smem + kBM * kPlanKeys * 2);
-  __shared__ uint32_t words[kPlanKeys / 32];
-  __shared__ int impure_s[kPlanKeys / kBN];
-  const int ch = blockIdx.x, pt = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(plan_smem + kBM * kBN * 2);
+  __shared__ uint32_t words[kBN / 32];
+  __shared__ int impure_s;
+  const int kt = blockIdx.x, pt = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, kc = tid % (kBN / 8), grp = tid / (kBN / 8);
   ptx::grid_launch_dependents();  // the attention kernel may start its prologue
   const int64_t np64 = nonpad[b];
   const int np = bad_nonpad(np64, max_seq) ? 0 : static_cast<int>(np64);
-  const int k_begin = ch * kPlanKeys;
-  const int keys = min(kPlanKeys, np - k_begin);  // <= 0: nothing live in this chunk
+  const int k_begin = kt * kBN;
+  const int keys = min(kBN, np - k_begin);  // <= 0: nothing live in this tile
   const int q0 = pt * kBM;
   const int rows = min(kBM, S_q - q0);
-  if (tid < kPlanKeys / 32) words[tid] = 0;
-  if (tid < kPlanKeys / kBN) impure_s[tid] = 0;
+  if (tid < kBN / 32) words[tid] = 0;
   if (tid == 0) {
+    impure_s = 0;
     ptx::mbar_init(bar, 1);
     ptx::fence_mbar_init();
   }
   __syncthreads();
-  bool ok = true;
-  const int kl = 8 * lane;  // this thread's 8 keys of the chunk
-  // this thread's byte of every row's key bits (none past the last 128-key tile)
-  const bool own_byte = k_begin + kl < n_kt * kBN;
-  uint8_t* rm = rowmask + (static_cast<int64_t>(b) * n_pt + pt) * kBM * rm_stride + (k_begin + kl) / 8;
-  uint32_t mrow[kBM / (kPlanThreads / 32) / 4] = {0, 0, 0, 0};  // this thread's byte of its 16 rows
+  const int kl = 8 * kc;  // this thread's 8 keys of the tile
+  uint8_t* rm = rowmask + (static_cast<int64_t>(b) * n_pt + pt) * kBM * rm_stride + kt * 16 + kc;
+  uint32_t mrow[kBM / kGroups / 4] = {0, 0};  // this thread's byte of its 8 rows
   if (keys > 0) {
     // whole 16-byte pieces: max_seq % 8 == 0 keeps the rounded row inside the tensor
     const uint32_t row_bytes = static_cast<uint32_t>((keys + 7) / 8) * 16;
@@ -394,26 +394,25 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_bias_kernel(const _
     __syncthreads();
     if (tid < rows) {
       const __nv_bfloat16* src = bias + (static_cast<int64_t>(b) * S_q + q0 + tid) * max_seq + k_begin;
-      ptx::bulk_load(rows_s + tid * kPlanKeys, src, row_bytes, bar);
+      ptx::bulk_load(rows_s + tid * kBN, src, row_bytes, bar);
     }
-    ok = ptx::mbar_wait_bounded(bar, 0, kWaitPolls);
+    const bool ok = ptx::mbar_wait_bounded(bar, 0, kWaitPolls);
     if (!ok && tid == 0) report(status, EXTKV_DEV_TIMEOUT);
     const uint32_t valid = keys - kl >= 8 ? 0xFFu : (keys - kl > 0 ? ((1u << (keys - kl)) - 1) : 0u);
     const float lowest = Elem<__nv_bfloat16>::lowest();
-    uint32_t acc = 0;
+    const __nv_bfloat162 lowest2 = __bfloat162bfloat162(__float2bfloat16_rn(lowest));
     // magnitude bits of the valid keys' values, per 32-bit word of two keys
     uint32_t vmask[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q)
       vmask[q] = (((valid >> (2 * q)) & 1) ? 0x7FFFu : 0u) | (((valid >> (2 * q + 1)) & 1) ? 0x7FFF0000u : 0u);
-    uint32_t nz = ok ? 0u : 1u;  // a failed copy leaves the tiles to the general path
-    const __nv_bfloat162 lowest2 = __bfloat162bfloat162(__float2bfloat16_rn(lowest));
+    uint32_t acc = 0, nz = ok ? 0u : 1u;  // a failed copy leaves the tile to the general path
 #pragma unroll
-    for (int i = 0; i < kBM / (kPlanThreads / 32); ++i) {
-      const int r = warp + (kPlanThreads / 32) * i;
+    for (int i = 0; i < kBM / kGroups; ++i) {
+      const int r = grp + kGroups * i;
       uint32_t m = 0;
       if (ok && valid && r < rows) {
-        const uint4 v = *reinterpret_cast<const uint4*>(rows_s + r * kPlanKeys + kl);
+        const uint4 v = *reinterpret_cast<const uint4*>(rows_s + r * kBN + kl);
         const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -428,24 +427,20 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_bias_kernel(const _
       acc |= m;
       mrow[i >> 2] |= m << (8 * (i & 3));
     }
-    if (acc) atomicOr(&words[lane >> 2], acc << (8 * (lane & 3)));
-    if (nz) impure_s[lane / (kBN / 8)] = 1;
+    if (acc) atomicOr(&words[kc >> 2], acc << (8 * (kc & 3)));
+    if (nz) impure_s = 1;
   }
   __syncthreads();
   // the row bits, where the attention kernel reads them: tiles that hold a
   // live key and whose bias is 0 or the sentinel throughout
-  if (keys > 0 && own_byte && !impure_s[lane / (kBN / 8)]) {
+  if (keys > 0 && !impure_s) {
 #pragma unroll
-    for (int i = 0; i < kBM / (kPlanThreads / 32); ++i)
-      rm[static_cast<int64_t>(warp + (kPlanThreads / 32) * i) * rm_stride] =
-          static_cast<uint8_t>(mrow[i >> 2] >> (8 * (i & 3)));
+    for (int i = 0; i < kBM / kGroups; ++i)
+      rm[static_cast<int64_t>(grp + kGroups * i) * rm_stride] = static_cast<uint8_t>(mrow[i >> 2] >> (8 * (i & 3)));
   }
-  if (tid < kPlanKeys / kBN) {
-    const int kt = ch * (kPlanKeys / kBN) + tid;
-    if (kt < n_kt) impure[(static_cast<int64_t>(b) * n_pt + pt) * n_kt + kt] = static_cast<uint8_t>(impure_s[tid]);
-  }
-  if (tid < kPlanKeys / 64) {
-    const int t = ch * (kPlanKeys / 64) + tid;
+  if (tid == 0) impure[(static_cast<int64_t>(b) * n_pt + pt) * n_kt + kt] = static_cast<uint8_t>(impure_s);
+  if (tid < kBN / 64) {
+    const int t = kt * (kBN / 64) + tid;
     if (t < n_words)
       colmask[(static_cast<int64_t>(b) * n_pt + pt) * n_words + t] =
           static_cast<uint64_t>(words[2 * tid]) | (static_cast<uint64_t>(words[2 * tid + 1]) << 32);
@@ -1449,7 +1444,7 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
                                       kPlanSmem);
     });
     if (plan_err != cudaSuccess) return plan_err;
-    prefill_plan_bias_kernel<<<dim3(n_plan_chunks(a.max_seq), prm.n_pt, prm.B), kPlanThreads, kPlanSmem,
+    prefill_plan_bias_kernel<<<dim3(prm.n_kt, prm.n_pt, prm.B), kPlanThreads, kPlanSmem,
                                a.stream>>>(static_cast<const __nv_bfloat16*>(term), a.nonpad,
                                            static_cast<uint64_t*>(a.workspace), prm.S_q, prm.max_seq,
                                            prm.n_pt, prm.n_tiles, wsb + off_rowmask, prm.rm_stride,
