@@ -28,8 +28,8 @@
 //     P^T moved into the B-operand layout with movmatrix; O^T += V^T P^T.
 //     A unit wholly inside the slice is written directly; a unit split
 //     across slices leaves an fp32 (max, sum, output) partial.
-//   Merge kernel (one CTA per unit): combines a split unit's partials, and
-//     writes the zero rows of units without a live tile.
+//   Merge kernel (one CTA per unit and group of output columns): combines a
+//     split unit's partials, and writes the zero rows of units without a live tile.
 //
 // Masking and zero rows follow section 6 of the ORT page: a key is masked iff
 // j >= nonpad[b] or bias <= lowest(T); masked scores become -inf by
@@ -848,31 +848,37 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
 
 // ---- merge: split units' partials, and the zero rows of empty units -------------
 
-// Slices one unit can span: each holds at least one of the unit's live tiles,
-// and a unit has at most max_tiles of them.
-__host__ __device__ __forceinline__ int merge_slices(int G, int max_tiles) { return G < max_tiles ? G : max_tiles; }
-
+// One CTA per (unit, group of output columns): thread (r, c) holds row r's
+// float4 c of the group.  Each thread loads, for up to kPre slices at once,
+// the slice's maximum and sum for its row and its partial float4, then forms
+// the weights 2^(max_s - M) in registers; slices are summed in slice order,
+// so the result does not depend on timing.
 template <int MODE>
-__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
-  constexpr int kPre = 16;  // slices whose partial rows a thread loads before the weights are known
-  extern __shared__ float sm_raw[];  // [NS][kRows] maxima, then [NS][kRows] sums
-  const int tid = threadIdx.x;
-  const int u = blockIdx.x;
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p, int n_cg) {
+  constexpr int kPre = 16;  // slices whose loads are in flight together
+  const int u = blockIdx.x / n_cg, cg = blockIdx.x % n_cg;
   const int b = u / p.Hkv, kvh = u % p.Hkv;
   const int D = p.D, R = p.R;
+  const int cols = D / 4 / n_cg;  // float4 per row in this group
+  const int i = threadIdx.x;
+  const int r = i / cols, d4 = (cg * cols + i % cols) * 4;
   ptx::grid_dependency_wait();
   const int4 info = p.info[u];
   const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + static_cast<int64_t>(kvh) * p.g) * p.S_q;
-  if (info.y == 0) {
-    // no live tile: every row of the unit is an exact zero row
-    uint4* dst = reinterpret_cast<uint4*>(p.y + row0 * D);
-    for (int i = tid; i < R * D / 8; i += kMergeThreads) dst[i] = make_uint4(0, 0, 0, 0);
+  if (i >= R * cols) return;
+  auto store = [&](const float4& acc) {
+    __nv_bfloat16* yr = p.y + (row0 + r) * D + d4;
+    uint2 pk;
+    pk.x = ptx::pack_bf16x2(acc.x, acc.y);
+    pk.y = ptx::pack_bf16x2(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(yr) = pk;
+  };
+  if (info.y == 0) {  // no live tile: an exact zero row
+    store(make_float4(0.f, 0.f, 0.f, 0.f));
     return;
   }
   const int ns = info.y;
   if (ns == 1) return;  // written by the decode kernel
-  float(*msh)[kRows] = reinterpret_cast<float(*)[kRows]>(sm_raw);
-  float(*lsh)[kRows] = reinterpret_cast<float(*)[kRows]>(sm_raw + static_cast<size_t>(merge_slices(p.G, p.max_tiles)) * kRows);
   constexpr int PS = 2 * kRows;  // header floats of a partial
   const int stride = PS + kRows * D;
   // slice s of the unit: CTA info.x + s; the unit is the first unit of every
@@ -881,65 +887,57 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
     const int slot = sg == 0 ? info.z : 0;
     return p.part + (static_cast<int64_t>(info.x + sg) * 2 + slot) * stride;
   };
-  for (int i = tid; i < ns * R; i += kMergeThreads) {
-    const float* pp = part_of(i / R);
-    msh[i / R][i % R] = __ldcg(pp + i % R);
-    lsh[i / R][i % R] = __ldcg(pp + kRows + i % R);
-  }
-  // this thread's output elements: (r, d4) = i; loads of the first kPre slices in flight
-  const int per_row = D / 4;
-  const int i0 = tid;
-  const bool has = i0 < R * per_row;
-  const int r = has ? i0 / per_row : 0, d4 = has ? (i0 % per_row) * 4 : 0;
-  float4 pre[kPre];
+  float M = -INFINITY, L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < ns; s0 += kPre) {
+    float m[kPre], l[kPre];
+    float4 o[kPre];
 #pragma unroll
-  for (int sg = 0; sg < kPre; ++sg)
-    if (has && sg < ns) pre[sg] = __ldcg(reinterpret_cast<const float4*>(part_of(sg) + PS + r * D + d4));
-  __syncthreads();
-  if (tid < R) {
-    float M = -INFINITY;
-    for (int sg = 0; sg < ns; ++sg) M = fmaxf(M, msh[sg][tid]);
-    const float ref = M == -INFINITY ? 0.f : M;
-    float L = 0.f;
-    for (int sg = 0; sg < ns; ++sg) {
-      const float w = ptx::ex2(msh[sg][tid] - ref);
-      msh[sg][tid] = w;
-      L += w * lsh[sg][tid];
+    for (int k = 0; k < kPre; ++k) {
+      if (s0 + k < ns) {
+        const float* pp = part_of(s0 + k);
+        m[k] = __ldcg(pp + r);
+        l[k] = __ldcg(pp + kRows + r);
+        o[k] = __ldcg(reinterpret_cast<const float4*>(pp + PS + r * D + d4));
+      } else {
+        m[k] = -INFINITY;
+        l[k] = 0.f;
+        o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;  // no unmasked key: zero row
-    for (int sg = 0; sg < ns; ++sg) msh[sg][tid] *= inv;
-  }
-  __syncthreads();
-  auto store = [&](int rr, int dd, const float4& acc) {
-    __nv_bfloat16* yr = p.y + (row0 + rr) * D + dd;
-    yr[0] = __float2bfloat16_rn(acc.x);
-    yr[1] = __float2bfloat16_rn(acc.y);
-    yr[2] = __float2bfloat16_rn(acc.z);
-    yr[3] = __float2bfloat16_rn(acc.w);
-  };
-  auto fma4 = [](float4& acc, const float4& v, float w) {
-    acc.x = fmaf(v.x, w, acc.x);
-    acc.y = fmaf(v.y, w, acc.y);
-    acc.z = fmaf(v.z, w, acc.z);
-    acc.w = fmaf(v.w, w, acc.w);
-  };
-  if (has) {  // the first element, with its first kPre slices already loaded
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    // a new maximum rescales what has been summed so far
+    float mc = M;
 #pragma unroll
-    for (int sg = 0; sg < kPre; ++sg)
-      if (sg < ns) fma4(acc, pre[sg], msh[sg][r]);
-    for (int sg = kPre; sg < ns; ++sg)
-      fma4(acc, __ldcg(reinterpret_cast<const float4*>(part_of(sg) + PS + r * D + d4)), msh[sg][r]);
-    store(r, d4, acc);
+    for (int k = 0; k < kPre; ++k) mc = fmaxf(mc, m[k]);
+    if (mc != -INFINITY && mc != M) {
+      const float c = M == -INFINITY ? 0.f : ptx::ex2(M - mc);
+      L *= c;
+      acc.x *= c;
+      acc.y *= c;
+      acc.z *= c;
+      acc.w *= c;
+      M = mc;
+    }
+#pragma unroll
+    for (int k = 0; k < kPre; ++k) {
+      const float w = m[k] == -INFINITY ? 0.f : ptx::ex2(m[k] - M);
+      L = fmaf(w, l[k], L);
+      acc.x = fmaf(o[k].x, w, acc.x);
+      acc.y = fmaf(o[k].y, w, acc.y);
+      acc.z = fmaf(o[k].z, w, acc.z);
+      acc.w = fmaf(o[k].w, w, acc.w);
+    }
   }
-  for (int i = i0 + kMergeThreads; i < R * per_row; i += kMergeThreads) {
-    const int rr = i / per_row, dd = (i % per_row) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int sg = 0; sg < ns; ++sg)
-      fma4(acc, __ldcg(reinterpret_cast<const float4*>(part_of(sg) + PS + rr * D + dd)), msh[sg][rr]);
-    store(rr, dd, acc);
-  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;  // no unmasked key: zero row
+  store(make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+}
+
+// Column groups of the merge: enough CTAs that each holds about 64 threads.
+int merge_groups(int R, int D) {
+  const int per_row = D / 4;
+  int n = 1;
+  while (n * 2 <= per_row && R * per_row / (n * 2) >= 64) n *= 2;
+  return n;
 }
 
 // ---- host ---------------------------------------------------------------------------
@@ -1026,13 +1024,11 @@ cudaError_t launch_dm(const AttnArgs& a, const DecodeParams& prm, const CUtensor
   cfg.dynamicSmemBytes = S::bytes();
   e = cudaLaunchKernelEx(&cfg, kern, kmap, vmap, qmap, tmap, prm);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.Hkv));
-  cfg.blockDim = dim3(kMergeThreads);
-  cfg.dynamicSmemBytes = static_cast<size_t>(merge_slices(prm.G, prm.max_tiles)) * kRows * 4 * 2;
-  e = cudaFuncSetAttribute(decode_merge_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(cfg.dynamicSmemBytes));
-  if (e != cudaSuccess) return e;
-  e = cudaLaunchKernelEx(&cfg, decode_merge_kernel<MODE>, prm);
+  const int n_cg = merge_groups(prm.R, D);
+  cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.Hkv * n_cg));
+  cfg.blockDim = dim3(static_cast<unsigned>((prm.R * (D / 4 / n_cg) + 31) / 32 * 32));
+  cfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&cfg, decode_merge_kernel<MODE>, prm, n_cg);
   if (e == cudaSuccess) note_launches(prm.plan ? 3 : 2);
   return e;
 }
@@ -1143,12 +1139,10 @@ bool decode_supported(const AttnArgs& a) {
   const int64_t units = a.B * a.Hkv;
   if (a.B > kMaxB || units >= (1 << 20) || max_tiles > 65535) return false;
   if (a.B * a.Hq * a.S_q > 0x7fffffff || units * max_tiles > 0x7fffffff) return false;
-  // a slice must fit the plan's work table (the merge weights table holds a
-  // row per slice of a unit)
+  // a slice must fit the plan's work table
   const int64_t G = grid_for(a.D, units * max_tiles);
   const int64_t slice = (units * max_tiles + G - 1) / G;
-  const int64_t ns = merge_slices(static_cast<int>(G), static_cast<int>(max_tiles));
-  if (slice > kMaxWork || ns * kRows * 8 > 200 * 1024) return false;
+  if (slice > kMaxWork) return false;
   return true;
 }
 
