@@ -81,3 +81,29 @@ def test_host_validation_rejects_bad_arguments(lib):
 
 def test_workspace_size_is_queryable(lib):
     assert extkv.attention_ext_kv_workspace_size(8, 16, 8, 1, 4096, 256, None) >= 0
+
+
+def test_host_validation_of_two_head_sizes(lib):
+    """attention_ext_kv_dv's own checks, all on the host before any launch."""
+    P = ctypes.c_void_p
+    fake = P(0x10000)  # never dereferenced: validation fails first
+
+    def dv_call(dk, dv, softcap=0.0, B=1):
+        return lib.attention_ext_kv_dv(fake, fake, fake, fake, None, None, fake, 1.0, softcap, B, 4, 2, 1, 64,
+                                       dk, dv, extkv.EXTKV_BF16, None, 0, None, None)
+
+    assert dv_call(128, 12) == extkv.EXTKV_ERR_UNSUPPORTED       # Dv not a multiple of 8
+    assert dv_call(128, 520) == extkv.EXTKV_ERR_UNSUPPORTED      # Dv above 512
+    assert dv_call(128, 0) == extkv.EXTKV_ERR_UNSUPPORTED
+    assert "Dv=" in extkv.extkv_last_error()
+    assert dv_call(12, 128) == extkv.EXTKV_ERR_UNSUPPORTED       # Dk not a multiple of 8
+    assert dv_call(128, 256, softcap=-1.0) == extkv.EXTKV_ERR_INVALID_ARG
+    assert dv_call(128, 256, softcap=float("nan")) == extkv.EXTKV_ERR_INVALID_ARG
+    assert dv_call(128, 256, B=0) == extkv.EXTKV_OK               # an empty problem launches nothing
+
+
+def test_workspace_size_with_two_head_sizes(lib):
+    # one head size: the same as the plain query; an empty batch needs nothing
+    same = extkv.attention_ext_kv_workspace_size(1, 16, 8, 2048, 8192, 256, None)
+    assert extkv.attention_ext_kv_workspace_size(1, 16, 8, 2048, 8192, 256, None, Dv=256) == same
+    assert int(lib.attention_ext_kv_workspace_size_dv(0, 16, 8, 2048, 8192, 256, 256, extkv.EXTKV_BF16)) == 0
