@@ -71,8 +71,7 @@ namespace {
 
 constexpr int kBM = 128;                   // query rows per CTA (M, tensor-memory lanes)
 constexpr int kBN = 128;                   // keys per KV tile (N of S = Q K^T)
-constexpr int kMaxThreads = 320;           // producer, MMA, 4 or 8 softmax warps
-constexpr int kPlanKeys = 256;             // keys per plan block (8 per lane)
+constexpr int kPlanKeys = 256;             // keys per block of the extra-term plan (8 per lane)
 constexpr int kPlanThreads = 256;
 constexpr uint32_t kWaitPolls = 1u << 22;  // bounded mbarrier waits
 constexpr int kMaxUnits = 8;
