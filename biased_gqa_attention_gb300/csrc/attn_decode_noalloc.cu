@@ -113,7 +113,7 @@ extern "C" int attention_ext_kv_noalloc(void* y, const void* q, const void* k_ca
     return fail(EXTKV_ERR_UNSUPPORTED,
                 "attention_ext_kv_noalloc: only decode shapes run here (bf16, (Hq/Hkv)*S_q <= 8, "
                 "D in {64,128,256,512})");
-  const size_t need = decode_workspace_bytes(B, Hq, Hkv, S_q, max_seq, D);
+  const size_t need = decode_workspace_bytes(B, Hq, Hkv, S_q, max_seq, D, D);
   if (need > static_cast<size_t>(EXTKV_NOALLOC_SCRATCH_BYTES))
     return fail(EXTKV_ERR_UNSUPPORTED,
                 "attention_ext_kv_noalloc: these sizes need %zu bytes of scratch, more than the "

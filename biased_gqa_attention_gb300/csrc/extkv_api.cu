@@ -163,7 +163,7 @@ size_t attention_ext_kv_workspace_size_dv(int64_t B, int64_t Hq, int64_t Hkv, in
   a.Dv = Dv;
   // enough for whichever kernel runs, automatic or chosen by extkv_set_algo
   size_t need = 0;
-  if (decode_supported(a)) need = decode_workspace_bytes(B, Hq, Hkv, S_q, max_seq, Dk);
+  if (decode_supported(a)) need = decode_workspace_bytes(B, Hq, Hkv, S_q, max_seq, Dk, Dv);
   if (prefill_supported(a)) {
     const size_t pf = prefill_workspace_bytes(B, Hq, S_q, max_seq, Dk, Dv, true);
     need = pf > need ? pf : need;
@@ -283,7 +283,7 @@ int attention_impl(void* y, const void* q, const void* k_cache, const void* v_ca
     return launch_scatter(s->k_cache, s->v_cache, s->k_new, s->v_new, s->write_idx, aa.B, aa.Hkv, s->S_new,
                           aa.max_seq, aa.D, aa.dtype, aa.status, aa.stream);
   };
-  const size_t decode_ws = decode_workspace_bytes(B, Hq, Hkv, S_q, max_seq, D);
+  const size_t decode_ws = decode_workspace_bytes(B, Hq, Hkv, S_q, max_seq, D, Dv);
   // a materialised bias or an extra term needs the prefill kernel's column-mask table
   // the column-mask table (a materialised bias or an extra term) and the
   // partials of key splits (small grids)

@@ -55,7 +55,8 @@ cudaError_t launch_attn_generic(const AttnArgs& a, const char** name);
 
 // Fast paths: `supported` says whether the shape can run; launch returns the error.
 bool decode_supported(const AttnArgs& a);
-size_t decode_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t D);
+size_t decode_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t Dk,
+                              int64_t Dv);
 cudaError_t launch_attn_decode(const AttnArgs& a, const char** name);
 bool prefill_supported(const AttnArgs& a);
 // Dk, Dv: the key and value head sizes (the partial rows of key splits hold Dv columns)

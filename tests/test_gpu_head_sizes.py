@@ -5,8 +5,9 @@
   (small grids), in every bias mode, with a softcap, with an extra term.
 * A value head size that differs from the query-key head size (head_size !=
   v_head_size, "Skill: Attention Optimization", "ORT CUDA Attention Kernel
-  Dispatch"): every pair of 128, 256 and 512 on the prefill kernel (decode
-  steps included), and the exact SIMT kernel for other head sizes.
+  Dispatch"): every pair of 128, 256 and 512 on the prefill kernel and, for
+  decode steps, on the decode kernel (with a softcap: the prefill kernel), and
+  the exact SIMT kernel for other head sizes.
 Each case checks the kernel that ran by name.
 """
 import numpy as np
@@ -21,6 +22,7 @@ pytestmark = pytest.mark.gpu
 
 PRE = "attn_prefill_tcgen05"
 GEN = "attn_generic_bf16"
+DEC = "attn_decode_streamk_mma"
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -108,12 +110,10 @@ def test_prefill_value_head_size_differs_key_splits_and_extra(dk, dv):
         assert max_err(g["y"], o["y"]) <= TOL[w.dtype]
 
 
-@pytest.mark.parametrize("dk,dv,S_q,kernel", [(64, 128, 40, GEN), (96, 200, 7, GEN), (256, 128, 1, PRE),
-                                               (512, 256, 1, PRE)], ids=lambda x: str(x))
+@pytest.mark.parametrize("dk,dv,S_q,kernel", [(64, 128, 40, GEN), (96, 200, 7, GEN), (64, 128, 1, GEN)],
+                         ids=lambda x: str(x))
 def test_value_head_size_differs_other_shapes(dk, dv, S_q, kernel):
-    """Head sizes outside the tensor-core pairs run on the exact SIMT kernel;
-    a decode step with two head sizes runs on the prefill kernel (the decode
-    kernel takes one head size)."""
+    """Head sizes outside the kernels' pairs run on the exact SIMT kernel."""
     w = _w(f"gen_dk{dk}_dv{dv}", 340 + dk // 32 + dv // 8, dk, dv, S_q=S_q, max_seq=520,
            nonpad_range=(max(S_q, 50), 520))
     inp = wl.make_inputs(w, "cuda")
@@ -130,3 +130,42 @@ def test_value_head_size_binding_checks_shapes():
     y_bad = torch.empty_like(inp.q)  # Dk columns instead of Dv
     with pytest.raises(ValueError):
         ek.attention_ext_kv(y_bad, inp.q, inp.k_cache, inp.v_cache, inp.nonpad, w.scale)
+
+
+@pytest.mark.parametrize("mode", ["bias", "fused", "none"])
+@pytest.mark.parametrize("dk,dv", PAIRS, ids=lambda x: str(x))
+def test_decode_value_head_size_differs(dk, dv, mode):
+    """A decode step (one query row per head, group of 4) on the decode kernel,
+    K of Dk and V of Dv columns, ragged nonpad."""
+    w = _w(f"dec_dk{dk}_dv{dv}", 360 + dk // 64 + dv // 32, dk, dv, B=5, Hq=8, Hkv=2, S_q=1, max_seq=1024,
+           window=300, nonpad_range=(1, 1024))
+    inp = wl.make_inputs(w, "cuda")
+    g = run_gpu(inp, mode=mode, scatter=False)
+    assert g["kernel"] == DEC
+    assert g["y"].shape[-1] == dv
+    o = oracle_path(inp, mode=mode, scatter=False)
+    assert max_err(g["y"], o["y"]) <= TOL[w.dtype]
+
+
+@pytest.mark.parametrize("dk,dv", [(256, 512), (512, 128)], ids=lambda x: str(x))
+def test_decode_value_head_size_differs_two_rows_spans_extra_and_poison(dk, dv):
+    """Two query rows per head (S_q = 2), image spans and an extra term in the
+    fused spec, and NaN in every slot at or beyond nonpad."""
+    w = _w(f"dec2_dk{dk}_dv{dv}", 370 + dk // 64 + dv // 32, dk, dv, B=3, Hq=8, Hkv=2, S_q=2, max_seq=768,
+           window=200, nonpad_fixed=600, nonpad_range=None, n_spans=1, span_len=40,
+           span_start_range=(500, 540), extra=True)
+    inp = wl.make_inputs(w, "cuda", poison=True)
+    for mode in ("bias", "fused"):
+        g = run_gpu(inp, mode=mode, scatter=False)
+        assert g["kernel"] == DEC
+        o = oracle_path(inp, mode=mode, scatter=False)
+        assert max_err(g["y"], o["y"]) <= TOL[w.dtype]
+
+
+def test_decode_value_head_size_differs_with_softcap_runs_on_the_prefill_kernel():
+    w = _w("dec_cap_dk256_dv128", 380, 256, 128, B=3, Hq=8, Hkv=2, S_q=1, max_seq=512, nonpad_range=(50, 512))
+    inp = wl.make_inputs(w, "cuda")
+    g = run_gpu(inp, mode="bias", scatter=False, softcap=3.0)
+    assert g["kernel"] == PRE
+    o = oracle_path(inp, mode="bias", scatter=False, softcap=3.0)
+    assert max_err(g["y"], o["y"]) <= TOL[w.dtype]
