@@ -212,9 +212,9 @@ int attention_ext_kv_softcap(void *y, const void *q, const void *k_cache, const 
  * value rows).  Dk == Dv is attention_ext_kv_softcap.  Both head sizes are
  * multiples of 8 in [8, 512]; everything else as attention_ext_kv_softcap.
  * The workspace is attention_ext_kv_workspace_size_dv(...) bytes.  Dk != Dv
- * with each of 128, 256, 512 runs on the tensor-core prefill kernel (a decode
- * step too: the decode kernel takes one head size); other asymmetric pairs run
- * on the exact fp32 SIMT kernel.
+ * with each of 128, 256, 512 runs on the tensor-core prefill kernel, or for a
+ * decode step (g * S_q <= 8 rows per KV head, no softcap) on the decode
+ * kernel; other asymmetric pairs run on the exact fp32 SIMT kernel.
  */
 int attention_ext_kv_dv(void *y, const void *q, const void *k_cache, const void *v_cache, const void *bias,
                         const extkv_bias_spec *fused, const int64_t *nonpad, float scale, float softcap,
