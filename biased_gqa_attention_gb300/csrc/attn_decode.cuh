@@ -6,7 +6,10 @@
 // (Opset 23/24) CUDA Patterns", section 1: GQA by reshaping Q, no KV
 // replication).  Decode is HBM-bound ("Skill: Attention Optimization": decode
 // is memory-bandwidth bound regardless of kernel), so the aim is to stream
-// every live K/V row exactly once with every SM busy to the end.
+// every live K/V row exactly once with every SM busy to the end.  Q and K
+// carry DK columns, V and Y DV (equal, or a pair of 128/256/512: the
+// head_size != v_head_size case of "Skill: Attention Optimization", "ORT CUDA
+// Attention Kernel Dispatch").
 //
 //   Live tiles: 16-key tiles holding at least one key some query row may
 //     attend.  Without a bias they are the tiles below nonpad; with the fused
