@@ -8,13 +8,13 @@ namespace extkv {
 
 namespace {
 
-int grid_for(int64_t Dk, int64_t Dv, int64_t items_max, int64_t B) {
-  if (Dk != Dv) return decode_grid_mixed(Dk, Dv, items_max, B);
+int grid_for(int64_t Dk, int64_t Dv, int64_t items_max) {
+  if (Dk != Dv) return decode_grid_mixed(Dk, Dv, items_max);
   switch (Dk) {
-    case 64: return persistent_grid<64, 64>(items_max, B);
-    case 128: return persistent_grid<128, 128>(items_max, B);
-    case 256: return persistent_grid<256, 256>(items_max, B);
-    default: return persistent_grid<512, 512>(items_max, B);
+    case 64: return persistent_grid<64, 64>(items_max);
+    case 128: return persistent_grid<128, 128>(items_max);
+    case 256: return persistent_grid<256, 256>(items_max);
+    default: return persistent_grid<512, 512>(items_max);
   }
 }
 
@@ -31,7 +31,7 @@ size_t decode_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, i
   (void)Hq;
   (void)S_q;
   const int64_t max_tiles = (max_seq + kTile - 1) / kTile;
-  return ws_layout(B, Hkv, max_tiles, grid_for(Dk, Dv, B * Hkv * max_tiles, B), Dv).total;
+  return ws_layout(B, Hkv, max_tiles, grid_for(Dk, Dv, B * Hkv * max_tiles), Dv).total;
 }
 
 bool decode_supported(const AttnArgs& a) {
@@ -49,7 +49,7 @@ bool decode_supported(const AttnArgs& a) {
   if (a.B > kMaxB || units >= (1 << 20) || max_tiles > 65535) return false;
   if (a.B * a.Hq * a.S_q > 0x7fffffff || units * max_tiles > 0x7fffffff) return false;
   // a slice must fit the plan's work table
-  const int64_t G = grid_for(a.D, a.Dv, units * max_tiles, a.B);
+  const int64_t G = grid_for(a.D, a.Dv, units * max_tiles);
   const int64_t slice = (units * max_tiles + G - 1) / G;
   if (slice > kMaxWork) return false;
   return true;

@@ -379,27 +379,14 @@ struct Smem {
   static constexpr int kQ = SPW * kStageBytes;             // two Q slots (DK = 512)
   static constexpr int kTerm = kQ + (kQReg ? 0 : 2 * kQBytes);  // per stage: 8 rows x 16 keys bf16
   static constexpr int kBars = kTerm + SPW * 256;          // SPW stages + 2 Q slots
-  // the per-batch tables follow, sized by the call's batch count (so that a
-  // small batch leaves room for one more CTA per SM)
-  static constexpr int kTables = (kBars + (SPW + 2) * 8 + 15) & ~15;
-  struct Tables {
-    int prefix;  // int32 [B + 1]
-    int np;      // int32 [B]
-    int wi;      // int32 [B]: write_idx (fused scatter)
-    int runs;    // Runs [B] (no plan); the plan's uint16 [kMaxWork] work table in the same place
-    int end;
-  };
-  static __host__ __device__ __forceinline__ int al16(int x) { return (x + 15) & ~15; }
-  static __host__ __device__ __forceinline__ Tables tables(int B) {
-    Tables t;
-    t.prefix = kTables;
-    t.np = t.prefix + al16((B + 1) * 4);
-    t.wi = t.np + al16(B * 4);
-    t.runs = t.wi + al16(B * 4);
-    t.end = t.runs + (B * 16 > kMaxWork * 2 ? B * 16 : kMaxWork * 2);
-    return t;
-  }
-  static size_t bytes(int B) { return 1024 + tables(B).end; }
+  static constexpr int kPrefix = kBars + (SPW + 2) * 8;    // int32 [kMaxB + 1]
+  static constexpr int kNp = kPrefix + (kMaxB + 1) * 4 + 12;  // int32 [kMaxB]
+  static constexpr int kWi = kNp + kMaxB * 4;              // int32 [kMaxB]: write_idx (fused scatter)
+  static constexpr int kRuns = kWi + kMaxB * 4;            // Runs [kMaxB] (no plan)
+  static constexpr int kWork = kRuns;                      // uint16 [kMaxWork] (plan)
+  static constexpr int kEnd = kRuns + kMaxB * 16;
+  static_assert(kMaxWork * 2 <= kMaxB * 16, "the work table shares the runs table");
+  static constexpr size_t bytes() { return 1024 + kEnd; }
 };
 
 // Position in the item sequence: unit (b, kvh), tile index kk of cnt.
@@ -421,12 +408,11 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBars);  // stages, Q slots
   uint64_t* qbars = bars + SPW;
-  const typename S::Tables tb = S::tables(p.B);
-  int32_t* prefix = reinterpret_cast<int32_t*>(smem + tb.prefix);
-  int32_t* np_s = reinterpret_cast<int32_t*>(smem + tb.np);
-  int32_t* wi_s = reinterpret_cast<int32_t*>(smem + tb.wi);
-  Runs* runs_s = reinterpret_cast<Runs*>(smem + tb.runs);
-  uint16_t* work = reinterpret_cast<uint16_t*>(smem + tb.runs);
+  int32_t* prefix = reinterpret_cast<int32_t*>(smem + S::kPrefix);
+  int32_t* np_s = reinterpret_cast<int32_t*>(smem + S::kNp);
+  int32_t* wi_s = reinterpret_cast<int32_t*>(smem + S::kWi);
+  Runs* runs_s = reinterpret_cast<Runs*>(smem + S::kRuns);
+  uint16_t* work = reinterpret_cast<uint16_t*>(smem + S::kWork);
   const int lane = threadIdx.x;
   const int c = blockIdx.x;
   const float lowest = Elem<__nv_bfloat16>::lowest();
@@ -973,46 +959,28 @@ struct PairCfg {
   static constexpr int SPW = DecodeCfg<(DK > DV ? DK : DV)>::SPW;
 };
 
-// Batch counts are rounded up to a power of two (at least 8) for the tables'
-// size, so that the occupancy is computed for a handful of sizes only.
-inline int batch_bucket(int64_t B) {
-  int b = 8;
-  while (b < B) b *= 2;
-  return b;
-}
-
 template <int DK, int DV>
-size_t decode_smem_bytes(int64_t B) {
-  return Smem<DK, DV, PairCfg<DK, DV>::SPW>::bytes(batch_bucket(B));
-}
-
-template <int DK, int DV>
-int persistent_grid(int64_t items_max, int64_t B) {
-  constexpr int kBuckets = 6;  // 8 .. 256 batches
+int persistent_grid(int64_t items_max) {
+  using S = Smem<DK, DV, PairCfg<DK, DV>::SPW>;
   static std::mutex mu;
-  static int cached_dev[kBuckets] = {-1, -1, -1, -1, -1, -1}, cached_occ[kBuckets] = {};
-  int bucket = 0;
-  while ((8 << bucket) < B && bucket + 1 < kBuckets) ++bucket;
-  const size_t smem = decode_smem_bytes<DK, DV>(B);
+  static int cached_dev = -1, cached_occ = 0;
   int dev = 0;
   cudaGetDevice(&dev);
   int occ;
   {
     std::lock_guard<std::mutex> g(mu);
-    if (cached_dev[bucket] != dev) {
+    if (cached_dev != dev) {
       auto kern = attn_decode_kernel<DK, DV, PairCfg<DK, DV>::SPW, kBias, false>;
-      // the opt-in maximum is always the largest table size (another thread may be launching)
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(decode_smem_bytes<DK, DV>(kMaxB)));
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(S::bytes()));
       int o = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, 32, smem) != cudaSuccess || o <= 0) {
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, 32, S::bytes()) != cudaSuccess || o <= 0) {
         (void)cudaGetLastError();
         o = 1;
       }
-      cached_occ[bucket] = o;
-      cached_dev[bucket] = dev;
+      cached_occ = o;
+      cached_dev = dev;
     }
-    occ = cached_occ[bucket];
+    occ = cached_occ;
   }
   const int64_t g = static_cast<int64_t>(occ) * num_sms();
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(g, items_max)));
@@ -1056,13 +1024,11 @@ cudaError_t launch_dm(const AttnArgs& a, const DecodeParams& prm, const CUtensor
     if (e != cudaSuccess) return e;
   }
   auto kern = attn_decode_kernel<DK, DV, SPW, MODE, CAP>;
-  const size_t smem = decode_smem_bytes<DK, DV>(a.B);
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(decode_smem_bytes<DK, DV>(kMaxB)));
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(S::bytes()));
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(static_cast<unsigned>(prm.G));
   cfg.blockDim = dim3(32);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = S::bytes();
   e = cudaLaunchKernelEx(&cfg, kern, kmap, vmap, qmap, tmap, prm);
   if (e != cudaSuccess) return e;
   const int n_cg = merge_groups(prm.R, DV);
@@ -1090,7 +1056,7 @@ template <int DK, int DV>
 cudaError_t launch_d(const AttnArgs& a, const char** name) {
   const int64_t max_tiles = (a.max_seq + kTile - 1) / kTile;
   const int64_t units = a.B * a.Hkv;
-  const int G = persistent_grid<DK, DV>(units * max_tiles, a.B);
+  const int G = persistent_grid<DK, DV>(units * max_tiles);
   const WsLayout ws = ws_layout(a.B, a.Hkv, max_tiles, G, DV);
   if (!a.workspace || a.ws_bytes < ws.total) return cudaErrorInvalidValue;
   uint8_t* wsb = static_cast<uint8_t*>(a.workspace);
@@ -1173,6 +1139,6 @@ cudaError_t launch_d(const AttnArgs& a, const char** name) {
 
 // Launchers for the head-size pairs of each translation unit.
 cudaError_t launch_attn_decode_mixed(const AttnArgs& a, const char** name);  // Dk != Dv
-int decode_grid_mixed(int64_t Dk, int64_t Dv, int64_t items_max, int64_t B);
+int decode_grid_mixed(int64_t Dk, int64_t Dv, int64_t items_max);
 
 }  // namespace extkv
