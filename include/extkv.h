@@ -146,7 +146,11 @@ int build_bias_from_bool_mask(void *bias, const uint8_t *mask, int64_t B, int64_
  * by extkv_set_algo.  The decode path keeps its live-tile plan and the
  * partial results of units split across CTAs there; the prefill path, with a
  * materialised bias or an extra term, one 64-bit mask of attended keys per
- * (batch, 128-row query tile, 64-key tile); the generic path needs none (0).
+ * (batch, 128-row query tile, 64-key tile), and for a materialised bias each
+ * query row's attended keys per 128-key tile (16 bytes) with a byte per tile
+ * saying whether the bias holds values other than 0 and the sentinel there;
+ * for small grids, the partial rows of key splits; the generic path needs
+ * none (0).
  * The caller allocates it, 256-byte aligned, and may reuse it for every call
  * on one stream; calls that can overlap on the GPU need separate workspaces.
  * Contents need no initialisation and are not preserved between calls.
