@@ -37,6 +37,9 @@ MUTATIONS = {
                                  "orc_load(k_cache, (kv_base + j) * Dv + d, dt)"),
     "causal_strict": ("int causal_ok = !causal || j <= p;", "int causal_ok = !causal || j < p;"),
     "padding_ignored_in_bias": ("if (j >= nonpad) return 0;", ""),
+    "bool_mask_inverted": ("if (mask[i]) orc_store_zero(bias, i, dt);", "if (!mask[i]) orc_store_zero(bias, i, dt);"),
+    "extra_term_dropped": ("if (extra) orc_copy_elem(bias, idx, extra, idx, dt);",
+                           "if (extra) orc_store_zero(bias, idx, dt);"),
 }
 
 
