@@ -37,6 +37,11 @@ MUTATIONS = {
                                  "orc_load(k_cache, (kv_base + j) * Dv + d, dt)"),
     "causal_strict": ("int causal_ok = !causal || j <= p;", "int causal_ok = !causal || j < p;"),
     "padding_ignored_in_bias": ("if (j >= nonpad) return 0;", ""),
+    "scatter_v_from_k": ("orc_copy_elem(v_cache, dst, v_new, src, dt);", "orc_copy_elem(v_cache, dst, k_new, src, dt);"),
+    "q_start_ignored": ("int64_t qs = q_start ? q_start[b] : (np - S_q > 0 ? np - S_q : 0);",
+                        "int64_t qs = (np - S_q > 0 ? np - S_q : 0);"),
+    "denominator_counts_masked": ("    if (!in_u[j]) continue;\n    double w = exp(s[j] - m);\n    denom += w;",
+                                  "    double w = in_u[j] ? exp(s[j] - m) : 0.0;\n    denom += in_u[j] ? w : 1.0;"),
     "bool_mask_inverted": ("if (mask[i]) orc_store_zero(bias, i, dt);", "if (!mask[i]) orc_store_zero(bias, i, dt);"),
     "extra_term_dropped": ("if (extra) orc_copy_elem(bias, idx, extra, idx, dt);",
                            "if (extra) orc_store_zero(bias, idx, dt);"),
