@@ -28,10 +28,8 @@ bool mixed_pair(int64_t Dk, int64_t Dv) {
 
 size_t decode_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t Dk,
                               int64_t Dv) {
-  (void)Hq;
-  (void)S_q;
   const int64_t max_tiles = (max_seq + kTile - 1) / kTile;
-  return ws_layout(B, Hkv, max_tiles, grid_for(Dk, Dv, B * Hkv * max_tiles), Dv).total;
+  return ws_layout(B, Hkv, max_tiles, grid_for(Dk, Dv, B * Hkv * max_tiles), Hq / Hkv * S_q, Dv).total;
 }
 
 bool decode_supported(const AttnArgs& a) {

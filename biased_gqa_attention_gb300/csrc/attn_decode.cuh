@@ -27,7 +27,8 @@
 //     tiles are double-buffered per unit.  Per tile, on the tensor cores
 //     (mma.sync m16n8k16 bf16, fp32 accumulation): S^T = K Q^T with the 16
 //     keys on M and the <= 8 query rows on N; scale, bias, mask; online
-//     softmax in fp32 (base-2, scores max-subtracted before exponentiation);
+//     softmax in fp32 (scores in natural units, the row maximum subtracted
+//     before the base-2 scaling and exponentiation);
 //     P^T moved into the B-operand layout with movmatrix; O^T += V^T P^T.
 //     A unit wholly inside the slice is written directly; a unit split
 //     across slices leaves an fp32 (max, sum, output) partial.
@@ -90,7 +91,10 @@ struct WsLayout {
   size_t count, tiles, info, part, total;
 };
 
-WsLayout ws_layout(int64_t B, int64_t Hkv, int64_t max_tiles, int64_t G, int64_t Dv) {
+// floats of one partial: max[8], sum[8], then the unit's R rows of Dv
+inline int64_t part_floats(int64_t R, int64_t Dv) { return 2 * kRows + R * Dv; }
+
+WsLayout ws_layout(int64_t B, int64_t Hkv, int64_t max_tiles, int64_t G, int64_t R, int64_t Dv) {
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   WsLayout l;
   size_t o = 0;
@@ -100,8 +104,8 @@ WsLayout ws_layout(int64_t B, int64_t Hkv, int64_t max_tiles, int64_t G, int64_t
   o = al(o + static_cast<size_t>(B * max_tiles) * 2);
   l.info = o;  // int4 per unit: first CTA, slices, slot in the first CTA
   o = al(o + static_cast<size_t>(B * Hkv) * 16);
-  l.part = o;  // per CTA, two partials: m[8], l[8], O[8][Dv] fp32
-  o = al(o + static_cast<size_t>(G) * 2 * (2 * kRows + kRows * Dv) * 4);
+  l.part = o;  // per CTA, two partials: m[8], l[8], O[R][Dv] fp32
+  o = al(o + static_cast<size_t>(G) * 2 * part_floats(R, Dv) * 4);
   l.total = o;
   return l;
 }
@@ -117,10 +121,12 @@ struct DecodeParams {
   int B, Hq, Hkv, S_q, g, R, D;  // D: the value head size (columns of Y and of the partials)
   int max_seq, max_tiles;
   int G;     // CTAs of the decode grid
+  int PS;    // floats of one partial (part_floats(R, D))
   int plan;  // 1: live tiles come from the plan kernel
   int32_t* count;
   uint16_t* tiles;
   int4* info;  // per unit: {first CTA, number of slices, slot in the first CTA, 0}; slices 0: no live tile
+  uint32_t polls;  // limit of the pipeline's barrier waits
   float* part;
   int32_t* status;
   // fused scatter (k_new == nullptr: none): the new rows (B, Hkv, S_new, D) go
@@ -386,7 +392,11 @@ struct Smem {
   static constexpr int kWork = kRuns;                      // uint16 [kMaxWork] (plan)
   static constexpr int kEnd = kRuns + kMaxB * 16;
   static_assert(kMaxWork * 2 <= kMaxB * 16, "the work table shares the runs table");
-  static constexpr size_t bytes() { return 1024 + kEnd; }
+  // D = 256: four CTAs per SM, not the five the tables and stages would fit
+  // (measured faster: 19.5 MB of requests in flight at start-up instead of
+  // 24 MB, so the first tiles land sooner and the slices end closer together)
+  static constexpr int kPad = (DK == 256 && DV == 256 && SPW == 2) ? 12 * 1024 : 0;
+  static constexpr size_t bytes() { return 1024 + kEnd + kPad; }
 };
 
 // Position in the item sequence: unit (b, kvh), tile index kk of cnt.
@@ -428,6 +438,7 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
   // Nothing above reads an input; everything below may read what the
   // previous kernel in the stream wrote.
   ptx::grid_dependency_wait();
+  ptx::grid_launch_dependents();
 
   const int64_t T = batch_tables<MODE>(p, lane, prefix, np_s, runs_s, wi_s);
   if (c == 0) {
@@ -518,12 +529,34 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
   int p_row0 = 0, p_bh = 0;
   auto fill = [&](int consumed) {
     while (pk < n && pk < consumed + SPW) {
+      bool q_regs = false;
       if (pk == 0 || pc.kk == 0) {  // first item of a unit: its Q rows
         if (p_seg + 1 > c_seg + 1) break;  // both Q slots busy
         ++p_seg;
         p_bh = pc.b * p.Hkv + pc.kvh;
         p_row0 = (pc.b * p.Hq + pc.kvh * p.g) * p.S_q;
         if constexpr (kQReg) {
+          q_regs = true;  // loaded once this stage's requests are out
+        } else if (lane == 0) {
+          const int slot = p_seg & 1;
+          ptx::mbar_arrive_expect_tx(&qbars[slot], S::kQBytes);
+          ptx::tma_load_3d(smem + S::kQ + slot * S::kQBytes, &qmap, &qbars[slot], 0, p_row0, 0);
+        }
+      }
+      {
+        // the stage's requests from three lanes side by side (a request costs its
+        // issuing thread a fixed time), after lane 0 has armed the barrier
+        const int st = pk % SPW;
+        const int key0 = tile_of(pc, pk) * kTile;
+        uint8_t* dst = smem + st * S::kStageBytes;
+        if (lane == 0) ptx::mbar_arrive_expect_tx(&bars[st], stage_tx);
+        __syncwarp();
+        if (lane == 0) ptx::tma_load_4d(dst, &kmap, &bars[st], 0, key0, 0, p_bh);
+        else if (lane == 1) ptx::tma_load_4d(dst + S::kKTileBytes, &vmap, &bars[st], 0, key0, 0, p_bh);
+        else if (kTerm && lane == 2) ptx::tma_load_2d(smem + S::kTerm + st * 256, &tmap, &bars[st], key0, pc.b * p.S_q);
+      }
+      if constexpr (kQReg) {
+        if (q_regs) {
           // B fragment of k-step ks: the bf16 pair at (row lane/4, d = 16 ks + 2 (lane%4)), and d + 8
           const int row = lane >> 2;
           const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + static_cast<int64_t>(p_row0 + row) * DK) + (lane & 3);
@@ -532,20 +565,7 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
             qn[ks][0] = row < p.R ? __ldg(qrow + 8 * ks) : 0u;
             qn[ks][1] = row < p.R ? __ldg(qrow + 8 * ks + 4) : 0u;
           }
-        } else if (lane == 0) {
-          const int slot = p_seg & 1;
-          ptx::mbar_arrive_expect_tx(&qbars[slot], S::kQBytes);
-          ptx::tma_load_3d(smem + S::kQ + slot * S::kQBytes, &qmap, &qbars[slot], 0, p_row0, 0);
         }
-      }
-      if (lane == 0) {
-        const int st = pk % SPW;
-        const int key0 = tile_of(pc, pk) * kTile;
-        uint8_t* dst = smem + st * S::kStageBytes;
-        ptx::mbar_arrive_expect_tx(&bars[st], stage_tx);
-        ptx::tma_load_4d(dst, &kmap, &bars[st], 0, key0, 0, p_bh);
-        ptx::tma_load_4d(dst + S::kKTileBytes, &vmap, &bars[st], 0, key0, 0, p_bh);
-        if (kTerm) ptx::tma_load_2d(smem + S::kTerm + st * 256, &tmap, &bars[st], key0, pc.b * p.S_q);
       }
       ++pk;
       advance(pc);
@@ -560,7 +580,6 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
   const int r0 = 2 * (lane & 3), r1 = r0 + 1;
   const bool ok0 = r0 < p.R, ok1 = r1 < p.R;
   const int i0 = r0 % p.S_q, i1 = r1 % p.S_q;
-  const float sl2 = p.scale * kLog2e;  // scores in base-2 units
   float o[DV / 16][4];
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   Win32 w0{}, w1{};
@@ -609,8 +628,7 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
     }
     // slot 0: the slice's first unit (it began at or before x0); slot 1: its last
     const int slot = ub <= x0 ? 0 : 1;
-    constexpr int PS = 2 * kRows + kRows * DV;
-    float* part = p.part + (static_cast<int64_t>(c) * 2 + slot) * PS;
+    float* part = p.part + (static_cast<int64_t>(c) * 2 + slot) * p.PS;
     float* o0 = part + 2 * kRows + r0 * DV;
     float* o1 = part + 2 * kRows + r1 * DV;
 #pragma unroll
@@ -668,14 +686,14 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
       if constexpr (!kQReg) {
         const int slot = c_seg & 1;
         q_s = ptx::smem_u32(smem + S::kQ + slot * S::kQBytes);
-        if (__any_sync(0xffffffffu, !ptx::mbar_wait_bounded(&qbars[slot], (c_seg >> 1) & 1, kWaitPolls))) {
+        if (__any_sync(0xffffffffu, !ptx::mbar_wait_bounded(&qbars[slot], (c_seg >> 1) & 1, p.polls))) {
           failed = true;
           break;
         }
       }
     }
     const int st = k % SPW;
-    if (__any_sync(0xffffffffu, !ptx::mbar_wait_bounded(&bars[st], (k / SPW) & 1, kWaitPolls))) {
+    if (__any_sync(0xffffffffu, !ptx::mbar_wait_bounded(&bars[st], (k / SPW) & 1, p.polls))) {
       failed = true;
       break;
     }
@@ -735,7 +753,9 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
       for (int a = 1; a < kAcc; ++a) s[e] += sa[a][e];
     }
 
-    // mask + bias, in base-2 units: s = log2e * (scale*qk + bias).
+    // mask + bias in natural units: s = scale*qk + bias.  The base-2 scaling
+    // comes only after the row maximum is subtracted, so an extreme finite
+    // bias (beyond about 2.4e38 in magnitude) never overflows into a mask.
     // s[0]: key ja, row r0; s[1]: ja, r1; s[2]: jb, r0; s[3]: jb, r1.
     const int kla = lane >> 2, klb = kla + 8;
     const int ja = key0 + kla, jb = key0 + klb;
@@ -775,11 +795,11 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float x = p.softcap * tanhf(s[e] * p.scale / p.softcap);
-        s[e] = live[e] ? (x + bv[e]) * kLog2e : -INFINITY;
+        s[e] = live[e] ? x + bv[e] : -INFINITY;
       }
     } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[e] = live[e] ? fmaf(s[e], sl2, bv[e] * kLog2e) : -INFINITY;
+      for (int e = 0; e < 4; ++e) s[e] = live[e] ? fmaf(s[e], p.scale, bv[e]) : -INFINITY;
     }
 
     // Keys no row attends: zero their V rows (poison must not reach PV).
@@ -802,7 +822,7 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
       __syncwarp();
     }
 
-    // online softmax for rows r0, r1 (base 2)
+    // online softmax for rows r0, r1: weights 2^((s - m) log2 e)
     float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 4));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 4));
@@ -812,9 +832,9 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 16));
     const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
     const float ref0 = n0 == -INFINITY ? 0.f : n0, ref1 = n1 == -INFINITY ? 0.f : n1;  // never -inf - -inf
-    const float c0 = ptx::ex2(m0 - ref0), c1 = ptx::ex2(m1 - ref1);
-    const float p0 = ptx::ex2(s[0] - ref0), p1 = ptx::ex2(s[1] - ref1);
-    const float p2 = ptx::ex2(s[2] - ref0), p3 = ptx::ex2(s[3] - ref1);
+    const float c0 = ptx::ex2((m0 - ref0) * kLog2e), c1 = ptx::ex2((m1 - ref1) * kLog2e);
+    const float p0 = ptx::ex2((s[0] - ref0) * kLog2e), p1 = ptx::ex2((s[1] - ref1) * kLog2e);
+    const float p2 = ptx::ex2((s[2] - ref0) * kLog2e), p3 = ptx::ex2((s[3] - ref1) * kLog2e);
     l0 = fmaf(l0, c0, p0 + p2);
     l1 = fmaf(l1, c1, p1 + p3);
     m0 = n0;
@@ -850,10 +870,15 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
   // finite; the affected units' output is stale (and flagged).
   finish();
   if (failed) {
-    // wait (bounded) for every load still in flight before the CTA exits
-    for (int j = 0; j < pk; ++j) ptx::mbar_wait_bounded(&bars[j % SPW], (j / SPW) & 1, kWaitPolls);
+    // wait (bounded, at the full limit) for every load still in flight before
+    // the CTA exits: the newest request of each stage (items pk - SPW .. pk - 1;
+    // a stage is refilled only after its previous item was consumed, so older
+    // phases are complete) and the Q slots of the newest two units
+    for (int j = pk > SPW ? pk - SPW : 0; j < pk; ++j)
+      ptx::mbar_wait_bounded(&bars[j % SPW], (j / SPW) & 1, kWaitPolls);
     if (!kQReg)
-      for (int sg = 0; sg <= p_seg; ++sg) ptx::mbar_wait_bounded(&qbars[sg & 1], (sg >> 1) & 1, kWaitPolls);
+      for (int sg = p_seg > 0 ? p_seg - 1 : 0; sg <= p_seg; ++sg)
+        ptx::mbar_wait_bounded(&qbars[sg & 1], (sg >> 1) & 1, kWaitPolls);
   }
 }
 
@@ -862,8 +887,8 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
 // One CTA per (unit, group of output columns): thread (r, c) holds row r's
 // float4 c of the group.  Each thread loads, for up to kPre slices at once,
 // the slice's maximum and sum for its row and its partial float4, then forms
-// the weights 2^(max_s - M) in registers; slices are summed in slice order,
-// so the result does not depend on timing.
+// the weights exp(max_s - M) in registers (maxima in natural units); slices
+// are summed in slice order, so the result does not depend on timing.
 template <int MODE>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p, int n_cg) {
   constexpr int kPre = 16;  // slices whose loads are in flight together
@@ -873,6 +898,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   const int cols = D / 4 / n_cg;  // float4 per row in this group
   const int i = threadIdx.x;
   const int r = i / cols, d4 = (cg * cols + i % cols) * 4;
+  ptx::grid_launch_dependents();
   ptx::grid_dependency_wait();
   const int4 info = p.info[u];
   const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + static_cast<int64_t>(kvh) * p.g) * p.S_q;
@@ -891,7 +917,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   const int ns = info.y;
   if (ns == 1) return;  // written by the decode kernel
   constexpr int PS = 2 * kRows;  // header floats of a partial
-  const int stride = PS + kRows * D;
+  const int stride = p.PS;
   // slice s of the unit: CTA info.x + s; the unit is the first unit of every
   // slice after the first, whose slot the decode kernel recorded
   auto part_of = [&](int sg) {
@@ -921,7 +947,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
 #pragma unroll
     for (int k = 0; k < kPre; ++k) mc = fmaxf(mc, m[k]);
     if (mc != -INFINITY && mc != M) {
-      const float c = M == -INFINITY ? 0.f : ptx::ex2(M - mc);
+      const float c = M == -INFINITY ? 0.f : ptx::ex2((M - mc) * kLog2e);
       L *= c;
       acc.x *= c;
       acc.y *= c;
@@ -931,7 +957,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
     }
 #pragma unroll
     for (int k = 0; k < kPre; ++k) {
-      const float w = m[k] == -INFINITY ? 0.f : ptx::ex2(m[k] - M);
+      const float w = m[k] == -INFINITY ? 0.f : ptx::ex2((m[k] - M) * kLog2e);
       L = fmaf(w, l[k], L);
       acc.x = fmaf(o[k].x, w, acc.x);
       acc.y = fmaf(o[k].y, w, acc.y);
@@ -1057,7 +1083,7 @@ cudaError_t launch_d(const AttnArgs& a, const char** name) {
   const int64_t max_tiles = (a.max_seq + kTile - 1) / kTile;
   const int64_t units = a.B * a.Hkv;
   const int G = persistent_grid<DK, DV>(units * max_tiles);
-  const WsLayout ws = ws_layout(a.B, a.Hkv, max_tiles, G, DV);
+  const WsLayout ws = ws_layout(a.B, a.Hkv, max_tiles, G, a.Hq / a.Hkv * a.S_q, DV);
   if (!a.workspace || a.ws_bytes < ws.total) return cudaErrorInvalidValue;
   uint8_t* wsb = static_cast<uint8_t*>(a.workspace);
 
@@ -1110,12 +1136,14 @@ cudaError_t launch_d(const AttnArgs& a, const char** name) {
   prm.max_seq = static_cast<int>(a.max_seq);
   prm.max_tiles = static_cast<int>(max_tiles);
   prm.G = G;
+  prm.PS = static_cast<int>(part_floats(prm.R, DV));
   prm.plan = needs_plan(a);
   prm.count = reinterpret_cast<int32_t*>(wsb + ws.count);
   prm.tiles = reinterpret_cast<uint16_t*>(wsb + ws.tiles);
   prm.info = reinterpret_cast<int4*>(wsb + ws.info);
   prm.part = reinterpret_cast<float*>(wsb + ws.part);
   prm.status = a.status;
+  prm.polls = wait_limit(a.wait_limit_plus1, kWaitPolls);
   prm.kc_w = static_cast<__nv_bfloat16*>(a.kc_w);
   prm.vc_w = static_cast<__nv_bfloat16*>(a.vc_w);
   prm.k_new = static_cast<const __nv_bfloat16*>(a.k_new);

@@ -9,7 +9,9 @@
 // entry point brings its own: a fixed-size array that lives in the library's
 // device image.  Every GPU that loads this code holds the array until the
 // process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cstdio>
 #include <mutex>
@@ -32,26 +34,55 @@ int fail(int code, const char* msg, size_t a = 0, size_t b = 0) {
   return code;
 }
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device (the symbol's host-side name is not a device address).
+// The calling thread's current CUDA context (the driver entry point, so the
+// library needs no link-time dependency on libcuda); nullptr if unavailable.
+CUcontext current_context() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+  });
+  CUcontext c = nullptr;
+  if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
+  return c;
+}
+
+// Device address of g_noalloc_scratch on the current device (the symbol's
+// host-side name is not a device address), looked up once per device and
+// context: a device reset builds a new context and a new copy of the array,
+// so an address cached for the old context is never reused.
 void* scratch_address(cudaError_t* err) {
+  struct Entry {
+    int dev;
+    CUcontext ctx;
+    void* addr;
+  };
   static std::mutex mu;
-  static void* addr[256] = {};
+  static Entry cache[64];
+  static int n = 0;
   int dev = 0;
   *err = cudaGetDevice(&dev);
   if (*err != cudaSuccess) return nullptr;
-  if (dev < 0 || dev >= 256) {
-    *err = cudaErrorInvalidDevice;
-    return nullptr;
-  }
+  const CUcontext ctx0 = current_context();  // nullptr before the runtime made one current
   std::lock_guard<std::mutex> g(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (*err != cudaSuccess) return nullptr;
-    addr[dev] = p;
+  for (int i = 0; ctx0 && i < n; ++i)
+    if (cache[i].dev == dev && cache[i].ctx == ctx0) return cache[i].addr;
+  void* p = nullptr;
+  *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // also makes the primary context current
+  if (*err != cudaSuccess) return nullptr;
+  const CUcontext ctx = ctx0 ? ctx0 : current_context();
+  if (ctx) {
+    int slot = -1;
+    for (int i = 0; i < n; ++i)
+      if (cache[i].dev == dev) slot = i;  // the device's earlier context is gone
+    if (slot < 0) slot = n < 64 ? n++ : 63;
+    cache[slot] = Entry{dev, ctx, p};
   }
-  return addr[dev];
+  return p;
 }
 
 }  // namespace
@@ -67,6 +98,8 @@ extern "C" int attention_ext_kv_noalloc(void* y, const void* q, const void* k_ca
                                         int64_t S_q, int64_t max_seq, int64_t D, int dtype,
                                         int32_t* status, void* stream) {
   set_error("");
+  if (dtype != EXTKV_F32 && dtype != EXTKV_BF16)
+    return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv_noalloc: unknown dtype %zu", static_cast<size_t>(dtype));
   if (B < 0 || S_q < 0 || Hq <= 0 || Hkv <= 0 || max_seq <= 0 || D <= 0 || Hq % Hkv)
     return fail(EXTKV_ERR_INVALID_ARG, "attention_ext_kv_noalloc: bad sizes");
   if (bias && fused)
@@ -109,6 +142,7 @@ extern "C" int attention_ext_kv_noalloc(void* y, const void* q, const void* k_ca
   a.dtype = dtype;
   a.status = status;
   a.stream = static_cast<cudaStream_t>(stream);
+  a.wait_limit_plus1 = wait_limit_setting();
   if (!decode_supported(a))
     return fail(EXTKV_ERR_UNSUPPORTED,
                 "attention_ext_kv_noalloc: only decode shapes run here (bf16, (Hq/Hkv)*S_q <= 8, "
@@ -127,8 +161,10 @@ extern "C" int attention_ext_kv_noalloc(void* y, const void* q, const void* k_ca
   a.workspace = scratch;
   a.ws_bytes = EXTKV_NOALLOC_SCRATCH_BYTES;
   const char* name = "";
+  note_launches(0);
   e = launch_attn_decode(a, &name);
   if (e != cudaSuccess)
     return fail(EXTKV_ERR_CUDA, "attention_ext_kv_noalloc: launch failed (CUDA error %zu)", static_cast<size_t>(e));
+  note_last_call(name);  // extkv_last_kernel() / extkv_last_launches()
   return EXTKV_OK;
 }

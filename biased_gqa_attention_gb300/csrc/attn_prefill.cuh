@@ -26,12 +26,14 @@
 //            then O += P_j V_j; completion is signalled through tcgen05.commit
 //            on mbarriers.  S is double-buffered in tensor memory.
 //   warps 2-5  softmax, one thread per query row (= tensor-memory lane): scale,
-//            bias or in-register mask, online softmax in base 2 with the
-//            running maximum subtracted before exponentiation; the output
-//            accumulator is rescaled in tensor memory only when a row's
-//            maximum grows by more than 2^8 (otherwise the stale maximum keeps
-//            every term below 2^8, exact after the final division); P is
-//            written as bf16 over the first half of its own S buffer.  They
+//            bias or in-register mask, online softmax on scores in natural
+//            units, the running maximum subtracted before the base-2 scaling
+//            and exponentiation (an extreme finite bias never overflows into
+//            a mask); the output accumulator is rescaled in tensor memory
+//            only when a row's maximum grows by more than 8 ln 2 (otherwise
+//            the stale maximum keeps every term below 2^8, exact after the
+//            final division); P is written as bf16 over the first half of
+//            its own S buffer.  They
 //            also copy the Q tile into tensor memory at the start.
 //            Epilogue: O / l from tensor memory to Y (bf16), zero rows where no
 //            key is unmasked.
@@ -158,7 +160,6 @@ struct PrefillParams {
   const uint8_t* impure;
   int rm_stride, n_kt;
   BiasSpec spec;
-  float scale_log2;  // scale * log2(e)
   float scale;
   float softcap;     // > 0: scores capped to softcap * tanh(score / softcap) before the bias
   int B, Hq, Hkv, S_q, max_seq, n_pt, n_tiles;  // n_tiles: 64-key words per colmask row
@@ -168,18 +169,20 @@ struct PrefillParams {
   // Key splits of a query tile (small grids): CTA split s takes its share of
   // the tile's KV tiles and writes an fp32 partial row per query row,
   // part[((b*Hq + h)*n_split + s)*S_q + i][part_stride(Dv)] = O[Dv], max, sum
-  // (max in base-2 units; O and sum relative to it); a merge kernel combines
+  // (max in natural units; O and sum relative to it); a merge kernel combines
   // them.  n_split == 1: the output rows are written directly.
   int n_split;
   float* part;
+  uint32_t polls;  // limit of the pipeline's barrier waits
 };
 
 // floats per partial row: O, then max and sum, rounded to 16 bytes
 __host__ __device__ constexpr int part_stride(int D) { return D + 4; }
 
-// Bounded wait that also gives up once another role has aborted.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+// Bounded wait (at most `limit` polls) that also gives up once another role
+// has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if ((i & 127u) == 127u && *abort) return false;
   }
@@ -189,8 +192,8 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 
 // Bounded wait polling with test_wait (no suspension): for short hand-offs
 // between warps that are usually already complete.
-__device__ __forceinline__ bool spin_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+__device__ __forceinline__ bool spin_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (ptx::mbar_test_wait(bar, parity)) return true;
     if ((i & 127u) == 127u && *abort) return false;
   }
@@ -201,9 +204,9 @@ __device__ __forceinline__ bool spin_or_abort(uint64_t* bar, uint32_t parity, vo
 // Bounded wait for up to three barrier phases at once: the polls are issued
 // back to back so their shared-memory round trips overlap (n = 1 .. 3).
 __device__ __forceinline__ bool wait3_or_abort(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1, uint64_t* b2,
-                                               uint32_t p2, int n, volatile int* abort) {
+                                               uint32_t p2, int n, volatile int* abort, uint32_t limit) {
   bool d0 = false, d1 = n < 2, d2 = n < 3;
-  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+  for (uint32_t i = 0; i < limit; ++i) {
     const bool r0 = d0 || ptx::mbar_try_wait(b0, p0);
     const bool r1 = d1 || ptx::mbar_try_wait(b1, p1);
     const bool r2 = d2 || ptx::mbar_try_wait(b2, p2);
@@ -448,14 +451,13 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_bias_kernel(const _
 
 // ---- softmax helpers ------------------------------------------------------------------
 
-// Scores of 64 keys (half H of a tile) in base 2: t = scale*log2(e)*s
-// (+ log2(e)*term), -inf where the key is masked: outside the row's allowed
-// keys (PARTIAL halves only; `allowed` bit c) or, with a term, term <= lowest.
+// Scores of 64 keys (half H of a tile) in natural units: t = scale*s
+// (+ term), -inf where the key is masked: outside the row's allowed keys
+// (PARTIAL halves only; `allowed` bit c) or, with a term, term <= lowest.
 template <int H, bool TERM, bool PARTIAL, int N>
 __device__ __forceinline__ void half_scores(float (&t)[N], const uint32_t (&sa)[32], const uint32_t (&sb)[32],
-                                            const uint32_t (&tw)[32], uint64_t allowed, float sl2, float lowest) {
-  const uint64_t sl2x2 = ptx::f2(sl2, sl2);
-  const uint64_t l2e = ptx::f2(kLog2e, kLog2e);
+                                            const uint32_t (&tw)[32], uint64_t allowed, float scale, float lowest) {
+  const uint64_t sc2 = ptx::f2(scale, scale);
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
     const uint32_t s0 = c < 16 ? sa[2 * c] : sb[2 * c - 32];
@@ -465,11 +467,11 @@ __device__ __forceinline__ void half_scores(float (&t)[N], const uint32_t (&sa)[
     uint64_t v;
     if (TERM) {
       const float b0 = __uint_as_float(tw[c] << 16), b1 = __uint_as_float(tw[c] & 0xFFFF0000u);
-      v = ptx::fma2(sv, sl2x2, ptx::mul2(ptx::f2(b0, b1), l2e));
+      v = ptx::fma2(sv, sc2, ptx::f2(b0, b1));
       ok0 = b0 > lowest;
       ok1 = b1 > lowest;
     } else {
-      v = ptx::mul2(sv, sl2x2);
+      v = ptx::mul2(sv, sc2);
     }
     if (PARTIAL) {
       ok0 = ok0 && ((allowed >> (2 * c)) & 1);
@@ -497,7 +499,41 @@ __device__ __forceinline__ void half_scores_capped(float (&t)[N], const uint32_t
     }
     if (PARTIAL) ok = ok && ((allowed >> c) & 1);
     const float x = cap * tanhf(__uint_as_float(sv) * scale / cap);
-    t[64 * H + c] = ok ? (x + b) * kLog2e : -INFINITY;
+    t[64 * H + c] = ok ? x + b : -INFINITY;
+  }
+}
+
+// Growth of a row maximum (natural units) beyond which the output
+// accumulator is rescaled: 8 ln 2, so that every weight stays below 2^8.
+constexpr float kRescaleGrow = 5.5451774f;
+
+// Weights of 32 pairs of scores t[T0 + 2c], t[T0 + 2c + 1] against the row's
+// maximum m (natural units): exp(t - m) = 2^(t log2 e - m log2 e), one fused
+// multiply-add per pair while m log2 e is finite; past that (|m| above about
+// 2.36e38, an extreme finite bias) the difference is formed first.  P goes to
+// pk as bf16 pairs, the sum into ls.
+template <int T0, int N>
+__device__ __forceinline__ void exp_pairs(const float (&t)[N], float m, uint32_t (&pk)[32], uint64_t (&ls)[4]) {
+  const float nml = -m * kLog2e;
+  const uint64_t l2e = ptx::f2(kLog2e, kLog2e);
+  if (fabsf(nml) <= 3.0e38f) {
+    const uint64_t nm2 = ptx::f2(nml, nml);
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const uint64_t d = ptx::fma2(ptx::f2(t[T0 + 2 * c], t[T0 + 2 * c + 1]), l2e, nm2);
+      const float e0 = ptx::ex2(ptx::f2_lo(d)), e1 = ptx::ex2(ptx::f2_hi(d));
+      ls[c & 3] = ptx::add2(ls[c & 3], ptx::f2(e0, e1));
+      pk[c] = ptx::pack_bf16x2(e0, e1);
+    }
+  } else {
+    const uint64_t nm2 = ptx::f2(-m, -m);
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const uint64_t d = ptx::mul2(ptx::add2(ptx::f2(t[T0 + 2 * c], t[T0 + 2 * c + 1]), nm2), l2e);
+      const float e0 = ptx::ex2(ptx::f2_lo(d)), e1 = ptx::ex2(ptx::f2_hi(d));
+      ls[c & 3] = ptx::add2(ls[c & 3], ptx::f2(e0, e1));
+      pk[c] = ptx::pack_bf16x2(e0, e1);
+    }
   }
 }
 
@@ -561,6 +597,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
   uint8_t* sT = sm + C::kOffT;
   Bars& bar = *reinterpret_cast<Bars*>(sm + C::kOffBar);
   volatile int* abort = &bar.abort;
+  const uint32_t lim = p.polls;  // pipeline waits; the drains keep the full limit
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // blockIdx.x = (h * n_vc + vc) * n_split + sp: query head, column chunk of Y, key split
@@ -697,7 +734,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
         if (MODE == kBias && j + 1 < T) imp_next = p.impure[imp0 + t_lo + j + 1] != 0;
         if (!imp) return true;  // the row bits suffice
         const int tb = t_issued % C::kTB;
-        if (t_issued >= C::kTB && !wait_or_abort(&bar.t_empty[tb], ((t_issued / C::kTB) - 1) & 1, abort))
+        if (t_issued >= C::kTB && !wait_or_abort(&bar.t_empty[tb], ((t_issued / C::kTB) - 1) & 1, abort, lim))
           return false;
         uint8_t* dst = sT + tb * C::kTermBytes;
         ptx::mbar_arrive_expect_tx(&bar.t_full[tb], C::kTermBytes);
@@ -713,7 +750,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
         const int parts = is_v ? kVP : kKP;
         for (int part = 0; part < parts; ++part) {
           const int u = issued, slot = u % C::kNU;  // units leave in sequence order
-          if (u >= C::kNU && !wait_or_abort(&bar.u_empty[slot], ((u / C::kNU) - 1) & 1, abort)) {
+          if (u >= C::kNU && !wait_or_abort(&bar.u_empty[slot], ((u / C::kNU) - 1) & 1, abort, lim)) {
             ok = false;
             break;
           }
@@ -783,7 +820,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
         if (kBatchK) {  // both units of K_j polled together
           const int s0 = u0 % C::kNU, s1 = (u0 + 1) % C::kNU;
           if (!k_known && !wait3_or_abort(&bar.u_full[s0], (u0 / C::kNU) & 1, &bar.u_full[s1],
-                                          ((u0 + 1) / C::kNU) & 1, &bar.u_full[s0], 0, kKP, abort))
+                                          ((u0 + 1) / C::kNU) & 1, &bar.u_full[s0], 0, kKP, abort, lim))
             return false;
           ptx::tc_fence_after();
         }
@@ -792,7 +829,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
         for (int part = 0; part < kKP; ++part) {
           const int slot = (u0 + part) % C::kNU;
           if (!kBatchK) {
-            if (!wait_or_abort(&bar.u_full[slot], ((u0 + part) / C::kNU) & 1, abort)) return false;
+            if (!wait_or_abort(&bar.u_full[slot], ((u0 + part) / C::kNU) & 1, abort, lim)) return false;
             ptx::tc_fence_after();
           }
           const uint64_t kd = kdesc0 + ((slot * C::kUnitBytes) >> 4);
@@ -813,7 +850,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
         ptx::umma_commit(&bar.s_full[j & 1]);
         return true;
       };
-      bool ok = wait_or_abort(&bar.q_full, 0, abort);
+      bool ok = wait_or_abort(&bar.q_full, 0, abort, lim);
       if (ok) {
         ptx::tc_fence_after();
         ok = issue_qk(0, -1);
@@ -825,10 +862,10 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
         // warps, which zero its dead rows before they release P_j; then P_j
         const int u0 = v_unit<kKP, kVP>(j, T), s0 = u0 % C::kNU, s1 = (u0 + 1) % C::kNU;
         if (!pv_known && !(ok = wait3_or_abort(&bar.u_full[s0], (u0 / C::kNU) & 1, &bar.u_full[s1],
-                                               ((u0 + 1) / C::kNU) & 1, &bar.u_full[s0], 0, kVP, abort)))
+                                               ((u0 + 1) / C::kNU) & 1, &bar.u_full[s0], 0, kVP, abort, lim)))
           break;
         ptx::mbar_arrive(&bar.v_ready[j & 1]);
-        if (!pv_known && !(ok = wait_or_abort(&bar.p_full[j & 1], (j >> 1) & 1, abort))) break;
+        if (!pv_known && !(ok = wait_or_abort(&bar.p_full[j & 1], (j >> 1) & 1, abort, lim))) break;
         ptx::tc_fence_after();
 #pragma unroll
         for (int part = 0; part < kVP; ++part) {
@@ -857,7 +894,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
     const int hh = C::kSplit ? (warp - 2) >> 2 : 0;
     const int quad = warp & 3;
     float* xch = reinterpret_cast<float*>(sm + C::kOffXch);  // [parity][half][row]
-    const float sl2 = p.scale_log2;
+    const float sc = p.scale;
     constexpr bool capped = CAP;
     const float lowest = Elem<__nv_bfloat16>::lowest();
     float m_run = -INFINITY, l_run = 0.f;
@@ -917,7 +954,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
       }
       const bool part0 = !__all_sync(0xffffffffu, al0 == ~0ull);
       const bool part1 = !__all_sync(0xffffffffu, al1 == ~0ull);
-      if (!__all_sync(0xffffffffu, wait_or_abort(&bar.s_full[j & 1], (j >> 1) & 1, abort))) {
+      if (!__all_sync(0xffffffffu, wait_or_abort(&bar.s_full[j & 1], (j >> 1) & 1, abort, lim))) {
         ok = false;
         break;
       }
@@ -936,7 +973,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
           if (termed) {
             // term blocks arrive in the order of the tiles that need one
             const int tb = t_seen % C::kTB;
-            if (!__all_sync(0xffffffffu, wait_or_abort(&bar.t_full[tb], (t_seen / C::kTB) & 1, abort))) {
+            if (!__all_sync(0xffffffffu, wait_or_abort(&bar.t_full[tb], (t_seen / C::kTB) & 1, abort, lim))) {
               ok = false;
               break;
             }
@@ -956,12 +993,12 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
               half_scores_capped<0, false, false>(t, sa, sb, tw, al, p.scale, p.softcap, lowest);
             }
           } else if (termed) {
-            if (part) half_scores<0, true, true>(t, sa, sb, tw, al, sl2, lowest);
-            else half_scores<0, true, false>(t, sa, sb, tw, al, sl2, lowest);
+            if (part) half_scores<0, true, true>(t, sa, sb, tw, al, sc, lowest);
+            else half_scores<0, true, false>(t, sa, sb, tw, al, sc, lowest);
           } else if (part) {
-            half_scores<0, false, true>(t, sa, sb, tw, al, sl2, lowest);
+            half_scores<0, false, true>(t, sa, sb, tw, al, sc, lowest);
           } else {
-            half_scores<0, false, false>(t, sa, sb, tw, al, sl2, lowest);
+            half_scores<0, false, false>(t, sa, sb, tw, al, sc, lowest);
           }
         }
         // the tile's maximum: both halves' maxima through shared memory, the
@@ -973,19 +1010,19 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
         xm[hh * kBM + row] = half_max(t);
         ptx::tc_fence_before();
         ptx::mbar_arrive(&bar.xch[quad][j & 1]);
-        if (!__all_sync(0xffffffffu, spin_or_abort(&bar.xch[quad][j & 1], (j >> 1) & 1, abort))) {
+        if (!__all_sync(0xffffffffu, spin_or_abort(&bar.xch[quad][j & 1], (j >> 1) & 1, abort, lim))) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
         const float mt = fmaxf(xm[row], xm[kBM + row]);  // the same in both warps
         const float m_new = fmaxf(m_run, mt);
-        const bool grow = m_new > m_run + 8.f;
+        const bool grow = m_new > m_run + kRescaleGrow;
         const bool rescale_o = grow && m_run != -INFINITY;
-        const float factor = rescale_o ? ptx::ex2(m_run - m_new) : 1.f;
+        const float factor = rescale_o ? ptx::ex2((m_run - m_new) * kLog2e) : 1.f;
         if (__any_sync(0xffffffffu, rescale_o)) {
           // this warp's half of the output columns, once P_{j-1} V_{j-1} completed
-          if (!__all_sync(0xffffffffu, wait_or_abort(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort))) {
+          if (!__all_sync(0xffffffffu, wait_or_abort(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort, lim))) {
             ok = false;
             break;
           }
@@ -1006,16 +1043,9 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
           m_run = m_new;
         }
         const float m_use = m_run == -INFINITY ? 0.f : m_run;
-        const uint64_t nm = ptx::f2(-m_use, -m_use);
         uint64_t ls[4] = {0, 0, 0, 0};
         uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const uint64_t d = ptx::add2(ptx::f2(t[2 * c], t[2 * c + 1]), nm);
-          const float e0 = ptx::ex2(ptx::f2_lo(d)), e1 = ptx::ex2(ptx::f2_hi(d));
-          ls[c & 3] = ptx::add2(ls[c & 3], ptx::f2(e0, e1));
-          pk[c] = ptx::pack_bf16x2(e0, e1);
-        }
+        exp_pairs<0>(t, m_use, pk, ls);
         ptx::tmem_st32(ts + 32 * hh, pk);  // this half's P over S_j's first half
         const uint64_t lsum = ptx::add2(ptx::add2(ls[0], ls[1]), ptx::add2(ls[2], ls[3]));
         l_run += ptx::f2_lo(lsum) + ptx::f2_hi(lsum);  // this half's share of the row sum
@@ -1031,9 +1061,9 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
             if (part0) half_scores_capped<0, false, true>(t, sa, sb, tw, al0, p.scale, p.softcap, lowest);
             else half_scores_capped<0, false, false>(t, sa, sb, tw, al0, p.scale, p.softcap, lowest);
           } else if (part0) {
-            half_scores<0, false, true>(t, sa, sb, tw, al0, sl2, lowest);
+            half_scores<0, false, true>(t, sa, sb, tw, al0, sc, lowest);
           } else {
-            half_scores<0, false, false>(t, sa, sb, tw, al0, sl2, lowest);
+            half_scores<0, false, false>(t, sa, sb, tw, al0, sc, lowest);
           }
           ptx::tmem_ld32(ts + 64, sa);
           ptx::tmem_ld32(ts + 96, sb);
@@ -1042,16 +1072,16 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
             if (part1) half_scores_capped<1, false, true>(t, sa, sb, tw, al1, p.scale, p.softcap, lowest);
             else half_scores_capped<1, false, false>(t, sa, sb, tw, al1, p.scale, p.softcap, lowest);
           } else if (part1) {
-            half_scores<1, false, true>(t, sa, sb, tw, al1, sl2, lowest);
+            half_scores<1, false, true>(t, sa, sb, tw, al1, sc, lowest);
           } else {
-            half_scores<1, false, false>(t, sa, sb, tw, al1, sl2, lowest);
+            half_scores<1, false, false>(t, sa, sb, tw, al1, sc, lowest);
           }
         } else {
           // term blocks arrive in the order of the tiles that need one
           const int tb = t_seen % C::kTB;
           const uint8_t* tblk = sT + tb * C::kTermBytes;
           if (C::kTerm &&
-              !__all_sync(0xffffffffu, wait_or_abort(&bar.t_full[tb], (t_seen / C::kTB) & 1, abort))) {
+              !__all_sync(0xffffffffu, wait_or_abort(&bar.t_full[tb], (t_seen / C::kTB) & 1, abort, lim))) {
             ok = false;
             break;
           }
@@ -1067,9 +1097,9 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
             else
               half_scores_capped<0, C::kTerm, false>(t, sa, sb, tw, al0, p.scale, p.softcap, lowest);
           } else if (part0) {
-            half_scores<0, C::kTerm, true>(t, sa, sb, tw, al0, sl2, lowest);
+            half_scores<0, C::kTerm, true>(t, sa, sb, tw, al0, sc, lowest);
           } else {
-            half_scores<0, C::kTerm, false>(t, sa, sb, tw, al0, sl2, lowest);
+            half_scores<0, C::kTerm, false>(t, sa, sb, tw, al0, sc, lowest);
           }
           ptx::tmem_ld32(ts + 64, sa);
           ptx::tmem_ld32(ts + 96, sb);
@@ -1085,20 +1115,20 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
             else
               half_scores_capped<1, C::kTerm, false>(t, sa, sb, tw, al1, p.scale, p.softcap, lowest);
           } else if (part1) {
-            half_scores<1, C::kTerm, true>(t, sa, sb, tw, al1, sl2, lowest);
+            half_scores<1, C::kTerm, true>(t, sa, sb, tw, al1, sc, lowest);
           } else {
-            half_scores<1, C::kTerm, false>(t, sa, sb, tw, al1, sl2, lowest);
+            half_scores<1, C::kTerm, false>(t, sa, sb, tw, al1, sc, lowest);
           }
         }
         const float mt = tile_max(t);
-        // lazy rescale: only when the running maximum grows by more than 2^8
+        // lazy rescale: only when the running maximum grows by more than 8 ln 2
         const float m_new = fmaxf(m_run, mt);
-        const bool grow = m_new > m_run + 8.f;  // false while the row has no unmasked key
+        const bool grow = m_new > m_run + kRescaleGrow;  // false while the row has no unmasked key
         const bool rescale_o = grow && m_run != -INFINITY;
-        const float factor = rescale_o ? ptx::ex2(m_run - m_new) : 1.f;
+        const float factor = rescale_o ? ptx::ex2((m_run - m_new) * kLog2e) : 1.f;
         if (__any_sync(0xffffffffu, rescale_o)) {
           // the output accumulator holds P_{j-1} V_{j-1} once that product completes
-          if (!__all_sync(0xffffffffu, wait_or_abort(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort))) {
+          if (!__all_sync(0xffffffffu, wait_or_abort(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort, lim))) {
             ok = false;
             break;
           }
@@ -1119,21 +1149,18 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
           m_run = m_new;
         }
         const float m_use = m_run == -INFINITY ? 0.f : m_run;
-        const uint64_t nm = ptx::f2(-m_use, -m_use);
         uint64_t ls[4] = {0, 0, 0, 0};
-  #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        // P_j over the first half of S_j: QK_{j+2}, the next writer of this
+        // buffer, is issued after P_j V_j and the tensor pipe runs in order
+        {
           uint32_t pk[32];
-  #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const uint64_t d = ptx::add2(ptx::f2(t[64 * hh + 2 * c], t[64 * hh + 2 * c + 1]), nm);
-            const float e0 = ptx::ex2(ptx::f2_lo(d)), e1 = ptx::ex2(ptx::f2_hi(d));
-            ls[c & 3] = ptx::add2(ls[c & 3], ptx::f2(e0, e1));
-            pk[c] = ptx::pack_bf16x2(e0, e1);
-          }
-          // P_j over the first half of S_j: QK_{j+2}, the next writer of this
-          // buffer, is issued after P_j V_j and the tensor pipe runs in order
-          ptx::tmem_st32(ts + 32 * hh, pk);
+          exp_pairs<0>(t, m_use, pk, ls);
+          ptx::tmem_st32(ts, pk);
+        }
+        {
+          uint32_t pk[32];
+          exp_pairs<64>(t, m_use, pk, ls);
+          ptx::tmem_st32(ts + 32, pk);
         }
         const uint64_t lsum = ptx::add2(ptx::add2(ls[0], ls[1]), ptx::add2(ls[2], ls[3]));
         l_run += ptx::f2_lo(lsum) + ptx::f2_hi(lsum);
@@ -1142,7 +1169,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
         // zero the V rows of dead keys once V_j has landed (the MMA thread,
         // which consumes the units in order, says so: a parity wait on the
         // units' own barriers could match a slot's previous phase)
-        if (!__all_sync(0xffffffffu, wait_or_abort(&bar.v_ready[j & 1], (j >> 1) & 1, abort))) {
+        if (!__all_sync(0xffffffffu, wait_or_abort(&bar.v_ready[j & 1], (j >> 1) & 1, abort, lim))) {
           ok = false;
           break;
         }
@@ -1168,7 +1195,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
     }
     // epilogue: O / l, zero rows without an unmasked key
     if (ok && T > 0 &&
-        !__all_sync(0xffffffffu, wait_or_abort(&bar.pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort)))
+        !__all_sync(0xffffffffu, wait_or_abort(&bar.pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort, lim)))
       ok = false;
     ptx::tc_fence_after();
     if constexpr (C::kSplit) {
@@ -1176,7 +1203,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
       float* xl = xch + (T & 1) * 2 * kBM;
       xl[hh * kBM + row] = l_run;
       ptx::mbar_arrive(&bar.xch[quad][T & 1]);
-      if (!__all_sync(0xffffffffu, spin_or_abort(&bar.xch[quad][T & 1], (T >> 1) & 1, abort))) ok = false;
+      if (!__all_sync(0xffffffffu, spin_or_abort(&bar.xch[quad][T & 1], (T >> 1) & 1, abort, lim))) ok = false;
       l_run = xl[row] + xl[kBM + row];
     }
     const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -1261,7 +1288,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
 
 // ---- merge of the key splits ----------------------------------------------------------
 
-// One warp per query row: weights 2^(max_s - M) of the splits (lane s holds
+// One warp per query row: weights exp(max_s - M) of the splits (lane s holds
 // split s; n_split <= kMaxSplit), then the row's columns four per lane, summed in
 // split order (the result does not depend on timing).  A row whose splits
 // saw no unmasked key is an exact zero row.
@@ -1285,7 +1312,7 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillParams 
 #pragma unroll
     for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float ref = M == -INFINITY ? 0.f : M;
-    const float w = (lane < ns && m != -INFINITY) ? ptx::ex2(m - ref) : 0.f;
+    const float w = (lane < ns && m != -INFINITY) ? ptx::ex2((m - ref) * kLog2e) : 0.f;
     float L = w * l;
 #pragma unroll
     for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
@@ -1419,7 +1446,6 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
   prm.n_kt = n_key_tiles(a.max_seq);
   prm.rm_stride = prm.n_kt * 16;
   prm.spec = BiasSpec{a.causal, a.window, a.span_offsets, a.spans, a.extra, a.q_start};
-  prm.scale_log2 = a.scale * kLog2e;
   prm.scale = a.scale;
   prm.softcap = a.softcap;
   prm.B = static_cast<int>(a.B);
@@ -1433,6 +1459,7 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
   prm.n_vc = static_cast<int>(Dvf / DV);
   prm.status = a.status;
   prm.n_split = prefill_splits(a.B, a.Hq * prm.n_vc, a.S_q);
+  prm.polls = wait_limit(a.wait_limit_plus1, kWaitPolls);
   prm.part = reinterpret_cast<float*>(wsb + term_tables_bytes(a.B, a.S_q, a.max_seq));
 
   if (MODE == kBias) {

@@ -18,6 +18,7 @@ thread_local char g_error[512] = "";
 thread_local const char* g_last_kernel = "";
 thread_local int g_launches = 0, g_last_launches = 0;
 thread_local int g_algo = EXTKV_ALGO_AUTO;
+thread_local uint32_t g_wait_limit_plus1 = 0;  // 0: the kernels' own limit; n + 1: n polls
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -53,6 +54,13 @@ int check_workspace(const AttnArgs& a, size_t need) {
 void set_error(const char* msg) { snprintf(g_error, sizeof g_error, "%s", msg); }
 
 void note_launches(int n) { g_launches = n; }
+
+uint32_t wait_limit_setting() { return g_wait_limit_plus1; }
+
+void note_last_call(const char* name) {
+  g_last_kernel = name;
+  g_last_launches = g_launches;
+}
 
 int num_sms() {
   // Cached per device; the SM count never changes for a device.
@@ -260,6 +268,7 @@ int attention_impl(void* y, const void* q, const void* k_cache, const void* v_ca
   a.workspace = workspace;
   a.ws_bytes = ws_bytes;
   a.stream = static_cast<cudaStream_t>(stream);
+  a.wait_limit_plus1 = g_wait_limit_plus1;
 
   const char* name = "";
   cudaError_t e;
@@ -416,6 +425,12 @@ const char* extkv_last_error(void) { return g_error; }
 const char* extkv_last_kernel(void) { return g_last_kernel; }
 
 int extkv_last_launches(void) { return g_last_launches; }
+
+int extkv_set_wait_polls(int polls) {
+  const int prev = static_cast<int>(g_wait_limit_plus1) - 1;
+  g_wait_limit_plus1 = polls < 0 ? 0u : static_cast<uint32_t>(polls) + 1u;
+  return prev;
+}
 
 int extkv_set_algo(int algo) {
   if (algo < EXTKV_ALGO_AUTO || algo > EXTKV_ALGO_PREFILL)

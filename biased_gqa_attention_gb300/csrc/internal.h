@@ -39,6 +39,9 @@ struct AttnArgs {
   const void* v_new;
   const int64_t* write_idx;
   int64_t S_new;
+  // limit of the pipeline's barrier waits: 0, the kernels' own limit; n + 1,
+  // n polls (a test sets a tiny one to make the waits run out)
+  uint32_t wait_limit_plus1;
 };
 
 // Each launcher returns cudaSuccess or the launch error; `name` receives the
@@ -72,5 +75,16 @@ void set_error(const char* msg);
 // Records how many kernels the attention launcher just launched (read back
 // through extkv_last_launches()).
 void note_launches(int n);
+
+// The calling thread's extkv_set_wait_polls() setting, as AttnArgs::wait_limit_plus1.
+uint32_t wait_limit_setting();
+
+// The poll limit of a pipeline wait for a call's wait_limit_plus1.
+inline uint32_t wait_limit(uint32_t plus1, uint32_t own) { return plus1 ? plus1 - 1 : own; }
+
+// Records a successful attention call made outside attention_ext_kv's own
+// dispatch: extkv_last_kernel() then names `name`, and extkv_last_launches()
+// the count the launcher noted.
+void note_last_call(const char* name);
 
 }  // namespace extkv

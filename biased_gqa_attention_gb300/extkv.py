@@ -27,6 +27,7 @@ SYMBOLS = ("ext_kv_scatter", "build_static_cache_bias", "attention_ext_kv_worksp
            "build_bias_from_bool_mask", "attention_ext_kv_dv", "attention_ext_kv_workspace_size_dv",
            "extkv_clear_status", "extkv_read_status",
            "extkv_last_error", "extkv_last_kernel", "extkv_last_launches", "extkv_set_algo",
+           "extkv_set_wait_polls",
            "attention_ext_kv_noalloc")
 
 
@@ -80,6 +81,8 @@ def load(path: str = LIB_PATH):
     lib.extkv_last_kernel.restype = ctypes.c_char_p
     lib.extkv_last_launches.restype = ctypes.c_int
     lib.extkv_set_algo.argtypes = [I]
+    lib.extkv_set_wait_polls.argtypes = [I]
+    lib.extkv_set_wait_polls.restype = I
     for name in ("ext_kv_scatter", "build_static_cache_bias", "attention_ext_kv", "attention_ext_kv_noalloc",
                  "extkv_clear_status", "extkv_read_status", "extkv_set_algo"):
         getattr(lib, name).restype = I
@@ -270,7 +273,7 @@ def attention_ext_kv_noalloc(y, q, k_cache, v_cache, nonpad, scale, bias=None,
                              fused: Optional[BiasSpec] = None, status=None, stream=None):
     """attention_ext_kv without a workspace, for callers that cannot allocate
     device memory (for instance an operator that is handed only its input and
-    output buffers).  Decode shapes only; the scratch is a static 16 MiB array
+    output buffers).  Decode shapes only; the scratch is a static 8 MiB array
     inside the library, shared by every call on the device, so calls that may
     overlap on the GPU must not use it concurrently."""
     for t, n in ((y, "y"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
@@ -324,6 +327,27 @@ def extkv_set_algo(algo: int) -> int:
     if prev < 0:
         _check(prev)
     return prev
+
+
+def extkv_set_wait_polls(polls: int) -> int:
+    """Poll limit of the kernels' pipeline waits for this thread (0: give up
+    at once; negative: the kernels' own limit); returns the previous setting.
+    For failure-detection tests."""
+    return int(load().extkv_set_wait_polls(int(polls)))
+
+
+class wait_polls:
+    """Context manager setting the pipeline-wait poll limit for the calling thread."""
+
+    def __init__(self, polls: int):
+        self.polls = polls
+
+    def __enter__(self):
+        self.prev = extkv_set_wait_polls(self.polls)
+        return self
+
+    def __exit__(self, *exc):
+        extkv_set_wait_polls(self.prev)
 
 
 class use_algo:

@@ -257,10 +257,14 @@ int attention_ext_kv_scatter(void *y, const void *q, void *k_cache, void *v_cach
                              int32_t *status, void *stream);
 
 /*
- * Size of the static scratch array behind attention_ext_kv_noalloc: 16 MiB of
- * device memory, held by every GPU that loads this library until exit.
+ * Size of the static scratch array behind attention_ext_kv_noalloc: 8 MiB of
+ * device memory, held by every GPU that loads this library until exit.  The
+ * decode call's scratch is its plan tables plus two fp32 partials per CTA of
+ * the persistent grid, (16 + R * D) floats each, R = (Hq/Hkv) * S_q: about
+ * 2.6 MB for Hq/Hkv = 2, D = 256; a D = 512 decode with 8 query rows per
+ * unit over the full grid needs about 10 MB and is refused.
  */
-#define EXTKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define EXTKV_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 /*
  * attention_ext_kv for callers that cannot allocate device memory.  The pages
@@ -275,7 +279,13 @@ int attention_ext_kv_scatter(void *y, const void *q, void *k_cache, void *v_cach
  *     other shapes, and sizes whose scratch would exceed the array, return
  *     EXTKV_ERR_UNSUPPORTED with a message.
  *   - The first call on a device looks up the array's device address (one
- *     cudaGetSymbolAddress); make that first call outside any stream capture.
+ *     cudaGetSymbolAddress), and so does the first call after the device's
+ *     context was rebuilt (cudaDeviceReset); make those calls outside any
+ *     stream capture.
+ *   - An unknown dtype returns EXTKV_ERR_INVALID_ARG; fp32 is refused as
+ *     EXTKV_ERR_UNSUPPORTED (the decode kernel is bf16 only).
+ *   - extkv_last_kernel() and extkv_last_launches() report this call as they
+ *     do attention_ext_kv.
  *   - Every call on a device shares the one array, and it keeps the previous
  *     call's contents (the call clears what must start at zero itself).  Calls
  *     that can overlap on the GPU -- on different streams without ordering --
@@ -316,6 +326,21 @@ const char *extkv_last_kernel(void);
 int extkv_last_launches(void);
 
 /*
+ * Limit, in polls, of the attention kernels' pipeline waits for the calling
+ * thread's later calls: polls >= 0 sets it (0: a wait that is not already
+ * complete gives up at once); a negative value restores the kernels' own
+ * limit (about 4 million polls), the default.  For failure-detection tests:
+ * with a tiny limit a wait runs out before its data lands, the kernel sets
+ * EXTKV_DEV_TIMEOUT in the status word, waits (at the full limit) for its own
+ * copies in flight, frees its tensor memory and returns; the output of that
+ * call is not valid.  Returns the previous setting (negative: the default).
+ * The pages state the rule this serves, not the mechanism: every launch is
+ * checked and a failure never passes silently ("ONNX Domain Attention
+ * (Opset 23/24) CUDA Patterns", section 5).
+ */
+int extkv_set_wait_polls(int polls);
+
+/*
  * Attention kernel selection for the calling thread.  EXTKV_ALGO_AUTO picks
  * by shape and type; the others force one kernel, and attention_ext_kv then
  * returns EXTKV_ERR_UNSUPPORTED for shapes that kernel cannot run.  Returns
@@ -324,7 +349,7 @@ int extkv_last_launches(void);
 #define EXTKV_ALGO_AUTO 0
 #define EXTKV_ALGO_GENERIC 1 /* fp32 SIMT, one warp per query row: any supported shape */
 #define EXTKV_ALGO_DECODE 2  /* stream-K split-KV decode: bf16, S_q*Hq/Hkv <= 8, D in {64,128,256,512} */
-#define EXTKV_ALGO_PREFILL 3 /* tcgen05/TMEM prefill: bf16, D in {64,128,256} */
+#define EXTKV_ALGO_PREFILL 3 /* tcgen05/TMEM prefill: bf16, head sizes 64/64 or any pair of 128, 256, 512 */
 int extkv_set_algo(int algo);
 
 #ifdef __cplusplus

@@ -171,6 +171,47 @@ def test_sentinel_and_minus_inf_mask_but_finite_negative_does_not():
     assert (oracle.attention(q, k, vn, None, [0], 1.0) == 0).all()
 
 
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_huge_finite_biases_stay_unmasked_and_compete_among_themselves(dt):
+    """Biases in (lowest, -2.4e38) are finite, so they do not mask (section 6
+    of the ORT page); only their differences count (softmax is invariant to a
+    shared shift).  Two live keys at -3.0e38 and -2.9e38: the gap of about
+    1e37 gives the first a weight exp(-1e37) = 0, so the row is the second
+    key's value row exactly.  Equal huge values on three keys: the scores'
+    own differences vanish next to them in fp64, so the row is the mean of
+    the three value rows.  +3e38 on one key among ordinary biases: that key's
+    row exactly."""
+    rng = np.random.default_rng(5)
+    v = np.array([[1, 2], [3, 4], [5, 6], [7, 8]], np.float32).reshape(1, 1, 4, 2)
+    k = rng.standard_normal((1, 1, 4, 2)).astype(np.float32)
+    q = rng.standard_normal((1, 1, 1, 2)).astype(np.float32)
+    if dt == "bf16":
+        to = lambda a: _rand_bits(np.asarray(a, np.float32))  # noqa: E731
+        v, k, q = to(v), to(k), to(q)
+        low = np.uint16(0xFF7F)
+    else:
+        to = lambda a: np.asarray(a, np.float32)  # noqa: E731
+        low = np.array([0xFF7FFFFF], np.uint32).view(np.float32)[0]
+    vf = oracle.to_f64(v)[0, 0]
+
+    def row(vals):
+        b = to(np.array(vals, np.float32)).reshape(1, 1, 1, 4)
+        b[0, 0, 0, [i for i, x in enumerate(vals) if x is None]] = low
+        return oracle.attention(q, k, v, b, [4], 1.0)[0, 0, 0]
+
+    assert (row([None, -3.0e38, -2.9e38, None]) == vf[2]).all()
+    y = row([-3.0e38, -3.0e38, None, -3.0e38])
+    np.testing.assert_allclose(y, (vf[0] + vf[1] + vf[3]) / 3, rtol=0, atol=1e-15)
+    assert (row([0.0, 3.0e38, 0.0, 0.0]) == vf[1]).all()
+
+
+def _rand_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bits, round to nearest even (None entries are filled after)."""
+    x = np.nan_to_num(x.astype(np.float32), nan=0.0)
+    u = x.view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
 def _setup(dt, rng, B=2, Hq=4, Hkv=2, S_q=6, L=40, D=8):
     nonpad = np.array([33, 21], np.int64)[:B]
     q = _rand((B, Hq, S_q, D), dt, rng)
