@@ -2,15 +2,35 @@
 // queries, keys and values up to 256 (and value head sizes that are whole
 // multiples of it), which shapes it takes, its workspace, and the dispatch
 // over the head-size groups (each group compiled in its own translation unit).
-#include "attn_prefill.cuh"
+#include "attn_prefill_pair.cuh"
 
 namespace extkv {
+
+namespace {
+
+// Head size 256 on CTA pairs: the two query heads of a pair share a KV head
+// (an even group size) and the grid is large enough not to split keys.
+bool pair_ok(const AttnArgs& a) {
+  return a.prefill_pairs && a.D == 256 && a.Dv == 256 && (a.Hq / a.Hkv) % 2 == 0 &&
+         prefill_splits(a.B, a.Hq, a.S_q) == 1;
+}
+
+template <bool CAP>
+cudaError_t launch_pair_c(const AttnArgs& a, const char** name) {
+  if (a.bias) return launch_pair<kBias, CAP>(a, name);
+  if (a.fused) return a.extra ? launch_pair<kFusedExtra, CAP>(a, name) : launch_pair<kFused, CAP>(a, name);
+  return launch_pair<kNone, CAP>(a, name);
+}
+
+}  // namespace
 
 cudaError_t launch_attn_prefill_equal(const AttnArgs& a, const char** name) {
   switch (a.D) {
     case 64: return launch_kv<64, 64>(a, name);
     case 128: return launch_kv<128, 128>(a, name);
-    case 256: return launch_kv<256, 256>(a, name);
+    case 256:
+      if (pair_ok(a)) return a.softcap > 0.f ? launch_pair_c<true>(a, name) : launch_pair_c<false>(a, name);
+      return launch_kv<256, 256>(a, name);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1381,6 +1381,67 @@ size_t term_tables_bytes(int64_t B, int64_t S_q, int64_t max_seq) {
 // 256-column chunks (one CTA each).
 int64_t v_chunk(int64_t Dv) { return Dv > 256 ? 256 : Dv; }
 
+// The kernel parameters of a prefill call with `dv_chunk` output columns per
+// CTA, and the plan kernel a materialised bias or an extra term needs
+// (launched here, on the call's stream, ahead of the attention kernel).
+cudaError_t prefill_setup(const AttnArgs& a, int mode, int dv_chunk, PrefillParams* out) {
+  PrefillParams& prm = *out;
+  const int64_t Dvf = a.Dv;
+  const void* term = mode == kBias ? a.bias : (mode == kFusedExtra ? a.extra : nullptr);
+  prm.y = static_cast<__nv_bfloat16*>(a.y);
+  prm.q = static_cast<const __nv_bfloat16*>(a.q);
+  prm.nonpad = a.nonpad;
+  uint8_t* wsb = static_cast<uint8_t*>(a.workspace);
+  const size_t off_rowmask = colmask_bytes(a.B, a.S_q, a.max_seq);
+  const size_t off_impure = off_rowmask + rowmask_bytes(a.B, a.S_q, a.max_seq);
+  prm.colmask = reinterpret_cast<const uint64_t*>(wsb);
+  prm.rowmask = wsb + off_rowmask;
+  prm.impure = wsb + off_impure;
+  prm.n_kt = n_key_tiles(a.max_seq);
+  prm.rm_stride = prm.n_kt * 16;
+  prm.spec = BiasSpec{a.causal, a.window, a.span_offsets, a.spans, a.extra, a.q_start};
+  prm.scale = a.scale;
+  prm.softcap = a.softcap;
+  prm.B = static_cast<int>(a.B);
+  prm.Hq = static_cast<int>(a.Hq);
+  prm.Hkv = static_cast<int>(a.Hkv);
+  prm.S_q = static_cast<int>(a.S_q);
+  prm.max_seq = static_cast<int>(a.max_seq);
+  prm.n_pt = n_query_tiles(a.S_q);
+  prm.n_tiles = n_mask_words(a.max_seq);
+  prm.Dv = static_cast<int>(Dvf);
+  prm.n_vc = static_cast<int>(Dvf / dv_chunk);
+  prm.status = a.status;
+  prm.n_split = prefill_splits(a.B, a.Hq * prm.n_vc, a.S_q);
+  prm.polls = wait_limit(a.wait_limit_plus1, kWaitPolls);
+  prm.part = reinterpret_cast<float*>(wsb + term_tables_bytes(a.B, a.S_q, a.max_seq));
+
+  if (mode == kBias) {
+    static std::once_flag plan_once;
+    static cudaError_t plan_err = cudaSuccess;
+    std::call_once(plan_once, [] {
+      plan_err = cudaFuncSetAttribute(prefill_plan_bias_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      kPlanSmem);
+    });
+    if (plan_err != cudaSuccess) return plan_err;
+    prefill_plan_bias_kernel<<<dim3(prm.n_kt, prm.n_pt, prm.B), kPlanThreads, kPlanSmem,
+                               a.stream>>>(static_cast<const __nv_bfloat16*>(term), a.nonpad,
+                                           static_cast<uint64_t*>(a.workspace), prm.S_q, prm.max_seq,
+                                           prm.n_pt, prm.n_tiles, wsb + off_rowmask, prm.rm_stride,
+                                           wsb + off_impure, prm.n_kt, a.status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  } else if (mode == kFusedExtra) {
+    prefill_plan_kernel<true><<<dim3(n_plan_chunks(a.max_seq), prm.n_pt, prm.B), kPlanThreads, 0, a.stream>>>(
+        static_cast<const __nv_bfloat16*>(term), a.nonpad, prm.spec, static_cast<uint64_t*>(a.workspace),
+        prm.S_q, prm.max_seq, prm.n_pt, prm.n_tiles);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+
+  return cudaSuccess;
+}
+
 template <int DK, int DV, int MODE, bool CAP>
 cudaError_t launch_dm(const AttnArgs& a, const char** name) {
   using C = Cfg<DK, DV, MODE>;
@@ -1434,56 +1495,7 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
   }
 
   PrefillParams prm;
-  prm.y = static_cast<__nv_bfloat16*>(a.y);
-  prm.q = static_cast<const __nv_bfloat16*>(a.q);
-  prm.nonpad = a.nonpad;
-  uint8_t* wsb = static_cast<uint8_t*>(a.workspace);
-  const size_t off_rowmask = colmask_bytes(a.B, a.S_q, a.max_seq);
-  const size_t off_impure = off_rowmask + rowmask_bytes(a.B, a.S_q, a.max_seq);
-  prm.colmask = reinterpret_cast<const uint64_t*>(wsb);
-  prm.rowmask = wsb + off_rowmask;
-  prm.impure = wsb + off_impure;
-  prm.n_kt = n_key_tiles(a.max_seq);
-  prm.rm_stride = prm.n_kt * 16;
-  prm.spec = BiasSpec{a.causal, a.window, a.span_offsets, a.spans, a.extra, a.q_start};
-  prm.scale = a.scale;
-  prm.softcap = a.softcap;
-  prm.B = static_cast<int>(a.B);
-  prm.Hq = static_cast<int>(a.Hq);
-  prm.Hkv = static_cast<int>(a.Hkv);
-  prm.S_q = static_cast<int>(a.S_q);
-  prm.max_seq = static_cast<int>(a.max_seq);
-  prm.n_pt = n_query_tiles(a.S_q);
-  prm.n_tiles = n_mask_words(a.max_seq);
-  prm.Dv = static_cast<int>(Dvf);
-  prm.n_vc = static_cast<int>(Dvf / DV);
-  prm.status = a.status;
-  prm.n_split = prefill_splits(a.B, a.Hq * prm.n_vc, a.S_q);
-  prm.polls = wait_limit(a.wait_limit_plus1, kWaitPolls);
-  prm.part = reinterpret_cast<float*>(wsb + term_tables_bytes(a.B, a.S_q, a.max_seq));
-
-  if (MODE == kBias) {
-    static std::once_flag plan_once;
-    static cudaError_t plan_err = cudaSuccess;
-    std::call_once(plan_once, [] {
-      plan_err = cudaFuncSetAttribute(prefill_plan_bias_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      kPlanSmem);
-    });
-    if (plan_err != cudaSuccess) return plan_err;
-    prefill_plan_bias_kernel<<<dim3(prm.n_kt, prm.n_pt, prm.B), kPlanThreads, kPlanSmem,
-                               a.stream>>>(static_cast<const __nv_bfloat16*>(term), a.nonpad,
-                                           static_cast<uint64_t*>(a.workspace), prm.S_q, prm.max_seq,
-                                           prm.n_pt, prm.n_tiles, wsb + off_rowmask, prm.rm_stride,
-                                           wsb + off_impure, prm.n_kt, a.status);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  } else if (MODE == kFusedExtra) {
-    prefill_plan_kernel<true><<<dim3(n_plan_chunks(a.max_seq), prm.n_pt, prm.B), kPlanThreads, 0, a.stream>>>(
-        static_cast<const __nv_bfloat16*>(term), a.nonpad, prm.spec, static_cast<uint64_t*>(a.workspace),
-        prm.S_q, prm.max_seq, prm.n_pt, prm.n_tiles);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
+  if (cudaError_t e = prefill_setup(a, MODE, DV, &prm); e != cudaSuccess) return e;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(prm.Hq * prm.n_vc * prm.n_split, prm.n_pt, prm.B);

@@ -269,6 +269,7 @@ int attention_impl(void* y, const void* q, const void* k_cache, const void* v_ca
   a.ws_bytes = ws_bytes;
   a.stream = static_cast<cudaStream_t>(stream);
   a.wait_limit_plus1 = g_wait_limit_plus1;
+  a.prefill_pairs = g_algo == EXTKV_ALGO_PREFILL_PAIR ? 1 : 0;
 
   const char* name = "";
   cudaError_t e;
@@ -309,6 +310,7 @@ int attention_impl(void* y, const void* q, const void* k_cache, const void* v_ca
       e = launch_decode_with(a, sc, &name);
       break;
     case EXTKV_ALGO_PREFILL:
+    case EXTKV_ALGO_PREFILL_PAIR:
       if (!prefill_supported(a))
         return fail(EXTKV_ERR_UNSUPPORTED, "attention_ext_kv: the prefill kernel cannot run this shape/type");
       if (int rc = check_workspace(a, prefill_ws)) return rc;
@@ -433,7 +435,7 @@ int extkv_set_wait_polls(int polls) {
 }
 
 int extkv_set_algo(int algo) {
-  if (algo < EXTKV_ALGO_AUTO || algo > EXTKV_ALGO_PREFILL)
+  if (algo < EXTKV_ALGO_AUTO || algo > EXTKV_ALGO_PREFILL_PAIR)
     return fail(EXTKV_ERR_INVALID_ARG, "extkv_set_algo: unknown algorithm %d", algo);
   int prev = g_algo;
   g_algo = algo;

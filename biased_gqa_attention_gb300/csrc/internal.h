@@ -42,6 +42,9 @@ struct AttnArgs {
   // limit of the pipeline's barrier waits: 0, the kernels' own limit; n + 1,
   // n polls (a test sets a tiny one to make the waits run out)
   uint32_t wait_limit_plus1;
+  // 1: the prefill at head size 256 may run on CTA pairs (2-SM MMAs); 0: one
+  // CTA per query tile only
+  int prefill_pairs;
 };
 
 // Each launcher returns cudaSuccess or the launch error; `name` receives the

@@ -349,7 +349,14 @@ int extkv_set_wait_polls(int polls);
 #define EXTKV_ALGO_AUTO 0
 #define EXTKV_ALGO_GENERIC 1 /* fp32 SIMT, one warp per query row: any supported shape */
 #define EXTKV_ALGO_DECODE 2  /* stream-K split-KV decode: bf16, S_q*Hq/Hkv <= 8, D in {64,128,256,512} */
-#define EXTKV_ALGO_PREFILL 3 /* tcgen05/TMEM prefill: bf16, head sizes 64/64 or any pair of 128, 256, 512 */
+#define EXTKV_ALGO_PREFILL 3 /* tcgen05/TMEM prefill: bf16, head sizes 64/64 or any pair of 128, 256, 512;
+                                one CTA per query tile */
+#define EXTKV_ALGO_PREFILL_PAIR 4 /* the same prefill on CTA pairs with 2-SM MMAs (two query heads of a
+                                     KV head as one M = 256 tile) where the shape allows it: head size
+                                     256/256, an even group, no split over keys; otherwise the
+                                     EXTKV_ALGO_PREFILL kernel.  Opt-in: slower than one CTA per tile
+                                     on the shapes measured (the pair waits on both halves' softmax
+                                     before each P.V) */
 int extkv_set_algo(int algo);
 
 #ifdef __cplusplus

@@ -118,7 +118,7 @@ def test_decode_kernel_extreme_biases(w, mode):
 @pytest.mark.parametrize("w", [PREFILL_SPLIT, PREFILL_WIDE, DECODE], ids=lambda w: w.name)
 def test_prefill_kernel_extreme_biases(w, mode):
     y, ref, kernel = _run(w, ek.ALGO_PREFILL, mode, seed=12)
-    assert kernel == "attn_prefill_tcgen05", kernel
+    assert kernel.startswith("attn_prefill_tcgen05"), kernel
     assert max_err(y, ref) <= TOL[w.dtype]
 
 

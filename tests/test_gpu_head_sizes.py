@@ -52,21 +52,21 @@ D512_SPANS_EXTRA = _w("pf_d512_spans_extra", 303, 512, B=1, Hq=8, Hkv=1, S_q=160
 def test_prefill_head_size_512(w, mode):
     inp = wl.make_inputs(w, "cuda")
     g = run_gpu(inp, mode=mode, algo=ek.ALGO_PREFILL)
-    assert g["kernel"] == PRE
+    assert g["kernel"].startswith(PRE)
     o = oracle_path(inp, mode=mode)
     assert max_err(g["y"], o["y"]) <= TOL[w.dtype]
 
 
 def test_prefill_head_size_512_is_the_automatic_choice():
     inp = wl.make_inputs(D512_GRID, "cuda")
-    assert run_gpu(inp, mode="bias")["kernel"] == PRE
+    assert run_gpu(inp, mode="bias")["kernel"].startswith(PRE)
 
 
 @pytest.mark.parametrize("mode", ["bias", "fused"])
 def test_prefill_head_size_512_softcap(mode):
     inp = wl.make_inputs(D512_SPLIT, "cuda")
     g = run_gpu(inp, mode=mode, algo=ek.ALGO_PREFILL, softcap=2.0)
-    assert g["kernel"] == PRE
+    assert g["kernel"].startswith(PRE)
     o = oracle_path(inp, mode=mode, softcap=2.0)
     assert max_err(g["y"], o["y"]) <= TOL[torch.bfloat16]
 
@@ -91,7 +91,7 @@ def test_prefill_value_head_size_differs(dk, dv, mode):
            nonpad_range=(150, 640))
     inp = wl.make_inputs(w, "cuda")
     g = run_gpu(inp, mode=mode, algo=ek.ALGO_PREFILL, scatter=False)
-    assert g["kernel"] == PRE
+    assert g["kernel"].startswith(PRE)
     assert g["y"].shape[-1] == dv
     o = oracle_path(inp, mode=mode, scatter=False)
     assert max_err(g["y"], o["y"]) <= TOL[w.dtype]
@@ -105,7 +105,7 @@ def test_prefill_value_head_size_differs_key_splits_and_extra(dk, dv):
     inp = wl.make_inputs(w, "cuda")
     for mode in ("bias", "fused"):
         g = run_gpu(inp, mode=mode, algo=ek.ALGO_PREFILL, scatter=False)
-        assert g["kernel"] == PRE
+        assert g["kernel"].startswith(PRE)
         o = oracle_path(inp, mode=mode, scatter=False)
         assert max_err(g["y"], o["y"]) <= TOL[w.dtype]
 
@@ -166,6 +166,6 @@ def test_decode_value_head_size_differs_with_softcap_runs_on_the_prefill_kernel(
     w = _w("dec_cap_dk256_dv128", 380, 256, 128, B=3, Hq=8, Hkv=2, S_q=1, max_seq=512, nonpad_range=(50, 512))
     inp = wl.make_inputs(w, "cuda")
     g = run_gpu(inp, mode="bias", scatter=False, softcap=3.0)
-    assert g["kernel"] == PRE
+    assert g["kernel"].startswith(PRE)
     o = oracle_path(inp, mode="bias", scatter=False, softcap=3.0)
     assert max_err(g["y"], o["y"]) <= TOL[w.dtype]

@@ -47,7 +47,7 @@ def _built():
 def test_prefill_kernel_forced(w, mode):
     inp = wl.make_inputs(w, "cuda")
     g = run_gpu(inp, mode=mode, algo=ek.ALGO_PREFILL)
-    assert g["kernel"] == PRE
+    assert g["kernel"].startswith(PRE)
     o = oracle_path(inp, mode=mode)
     err = max_err(g["y"], o["y"])
     assert err <= TOL[w.dtype], err
@@ -60,7 +60,7 @@ def test_prefill_key_tail_not_a_multiple_of_8(mode):
                     dtype=torch.bfloat16, causal=True, window=300, nonpad_range=(100, 777))
     inp = wl.make_inputs(w, "cuda")
     g = run_gpu(inp, mode=mode, algo=ek.ALGO_PREFILL)
-    assert g["kernel"] == PRE
+    assert g["kernel"].startswith(PRE)
     o = oracle_path(inp, mode=mode)
     assert max_err(g["y"], o["y"]) <= TOL[w.dtype]
 
@@ -68,8 +68,8 @@ def test_prefill_key_tail_not_a_multiple_of_8(mode):
 @pytest.mark.parametrize("w", [wl.C3, wl.C5, wl.small(wl.C3), wl.small(wl.C5)], ids=lambda w: w.name)
 def test_prefill_workloads_pick_the_prefill_kernel(w):
     inp = wl.make_inputs(w, "cuda")
-    assert run_gpu(inp, mode="bias")["kernel"] == PRE
-    assert run_gpu(inp, mode="fused")["kernel"] == PRE
+    assert run_gpu(inp, mode="bias")["kernel"].startswith(PRE)
+    assert run_gpu(inp, mode="fused")["kernel"].startswith(PRE)
 
 
 @pytest.mark.parametrize("mode", ["bias", "fused"])
@@ -109,7 +109,7 @@ def test_prefill_empty_batch_negative_offset_and_unreachable_rows():
     for mode in ("bias", "fused", "none"):
         g = run_gpu(inp, mode=mode, algo=ek.ALGO_PREFILL, scatter=False)
         o = oracle_path(inp, mode=mode, scatter=False)
-        assert g["kernel"] == PRE
+        assert g["kernel"].startswith(PRE)
         assert (g["y"][0] == 0).all()
         assert max_err(g["y"], o["y"]) <= TOL[w.dtype]
     qs = torch.tensor([-5, -100, 100], dtype=torch.int64, device="cuda")
@@ -148,7 +148,7 @@ def test_prefill_full_c3_sampled_rows_in_every_mode():
     rows = sample_rows(w, 192)
     for mode in ("bias", "fused", "none"):
         g = run_gpu(inp, mode=mode)
-        assert g["kernel"] == PRE
+        assert g["kernel"].startswith(PRE)
         o = oracle_path(inp, rows=rows, mode=mode)
         assert max_err(g["y"], o["y"], rows) <= TOL[w.dtype]
 
@@ -184,6 +184,6 @@ def test_prefill_bias_with_mask_only_and_dense_tiles_interleaved():
     with ek.use_algo(ek.ALGO_PREFILL):
         ek.attention_ext_kv(y, inp.q, inp.k_cache, inp.v_cache, inp.nonpad, w.scale,
                             bias=from_raw(b16, torch.bfloat16).cuda())
-        assert ek.extkv_last_kernel() == PRE
+        assert ek.extkv_last_kernel().startswith(PRE)
     ref = oracle.attention(raw(inp.q), raw(inp.k_cache), raw(inp.v_cache), b16, nonpad, np.float32(w.scale))
     assert max_err(y, ref) <= TOL[w.dtype]

@@ -57,7 +57,7 @@ CASES = [
 def test_softcap_matches_the_oracle(w, kernel, mode, cap):
     inp = wl.make_inputs(w, "cuda")
     y, ran = _run(inp, mode, cap)
-    assert ran == kernel
+    assert ran.startswith(kernel), ran
     o = oracle_path(inp, mode=mode, scatter=False, softcap=cap)
     assert max_err(y, o["y"]) <= TOL[w.dtype]
 

@@ -18,14 +18,16 @@ from biased_gqa_attention_gb300 import extkv as ek
 from biased_gqa_attention_gb300 import workloads as wl
 from gpu_path import TOL, max_err, oracle_path, run_gpu, spec_of
 
-# a decode shape with the in-kernel merge (small partials), one whose
-# partials go through the merge kernel, and two prefill shapes (key splits
-# and not)
+# two decode shapes, two single-SM prefill shapes (with key splits) and the
+# prefill on CTA pairs, on a shape large enough for the prefill on CTA pairs (head size 256, group of 2)
+PAIR_SHAPE = wl.Workload("timeout_pair", 322, B=2, Hq=8, Hkv=4, D=256, S_q=700, max_seq=2048,
+                         dtype=torch.bfloat16, causal=True, window=500, nonpad_fixed=1900)
 CASES = [
     (ek.ALGO_DECODE, wl.small(wl.C2), "bias"),
     (ek.ALGO_DECODE, wl.small(wl.C4), "fused"),
     (ek.ALGO_PREFILL, wl.small(wl.C5), "bias"),
     (ek.ALGO_PREFILL, wl.small(wl.C3), "fused"),
+    (ek.ALGO_PREFILL_PAIR, PAIR_SHAPE, "bias"),
 ]
 
 
