@@ -113,6 +113,29 @@ def _check(code: int):
         raise ExtKVError(code, load().extkv_last_error().decode())
 
 
+class PreparedCall:
+    """One library call with its arguments marshalled once (pointers, sizes,
+    the bias specification, the stream): calling it issues the same C call
+    again, without the per-call checks and conversions of the Python layer.
+    For a step repeated over the same buffers; the tensors it was prepared
+    with must stay alive and in place, and their contents may change between
+    calls."""
+
+    __slots__ = ("_fn", "_args", "_keep")
+
+    def __init__(self, fn, args, keep=()):
+        self._fn = fn
+        # ctypes instances of the declared argument types: the call converts nothing
+        self._args = tuple(a if a is None or isinstance(a, ctypes._SimpleCData) or type(a).__name__ == "CArgObject"
+                           else t(a) for a, t in zip(args, fn.argtypes))
+        self._keep = keep  # the objects the pointers refer to (bias specification, workspace, tensors)
+
+    def __call__(self):
+        code = self._fn(*self._args)
+        if code != EXTKV_OK:
+            raise ExtKVError(code, load().extkv_last_error().decode())
+
+
 def _need(t, name, dims=None, dtype=None):
     if t is None:
         return
@@ -158,16 +181,27 @@ def ext_kv_scatter(k_cache, v_cache, k_new, v_new, write_idx, status=None, strea
                                  _stream(stream)))
 
 
-def build_static_cache_bias(bias, spec: BiasSpec, nonpad, status=None, stream=None):
-    """Materialise the (B,1,S_q,max_seq) bias of ``spec`` into ``bias``."""
+def _marshal_bias(bias, spec: BiasSpec, nonpad, status, stream):
     _need(bias, "bias", dims=4)
     _need(nonpad, "nonpad", dims=1, dtype=torch.int64)
     B, one, S_q, max_seq = bias.shape
     if one != 1:
         raise ValueError("bias must be (B,1,S_q,max_seq)")
     c = spec._c()
-    _check(load().build_static_cache_bias(_p(bias), ctypes.byref(c), _p(nonpad), B, S_q, max_seq,
-                                          _dt(bias), _p(status), _stream(stream)))
+    lib = load()
+    return lib.build_static_cache_bias, (_p(bias), ctypes.byref(c), _p(nonpad), B, S_q, max_seq, _dt(bias),
+                                         _p(status), _stream(stream)), (c, bias, nonpad, status)
+
+
+def build_static_cache_bias(bias, spec: BiasSpec, nonpad, status=None, stream=None):
+    """Materialise the (B,1,S_q,max_seq) bias of ``spec`` into ``bias``."""
+    fn, args, _ = _marshal_bias(bias, spec, nonpad, status, stream)
+    _check(fn(*args))
+
+
+def prepare_build_static_cache_bias(bias, spec: BiasSpec, nonpad, status=None, stream=None) -> PreparedCall:
+    """build_static_cache_bias with its arguments marshalled once (PreparedCall)."""
+    return PreparedCall(*_marshal_bias(bias, spec, nonpad, status, stream))
 
 
 def attention_ext_kv_workspace_size(B, Hq, Hkv, S_q, max_seq, D, dtype, Dv=None) -> int:
@@ -188,16 +222,7 @@ def new_workspace(q: torch.Tensor, k_cache: torch.Tensor, v_cache: Optional[torc
     return torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
 
 
-def attention_ext_kv(y, q, k_cache, v_cache, nonpad, scale, bias=None, fused: Optional[BiasSpec] = None,
-                     workspace=None, status=None, stream=None, softcap: float = 0.0):
-    """Y = softmax(cap(scale*QK^T) + bias)V over the external cache; writes ``y`` (B,Hq,S_q,Dv).
-    ``softcap`` > 0 caps the scaled scores to softcap*tanh(x/softcap) before the
-    bias (attention_ext_kv_softcap); 0 is plain attention_ext_kv.  A v_cache
-    whose head size Dv differs from q's and k_cache's Dk goes through
-    attention_ext_kv_dv.
-
-    ``workspace`` (uint8 device tensor of attention_ext_kv_workspace_size bytes)
-    is allocated here when not given."""
+def _marshal_attention(y, q, k_cache, v_cache, nonpad, scale, bias, fused, workspace, status, stream, softcap):
     for t, n in ((y, "y"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
         _need(t, n, dims=4, dtype=q.dtype)
     _need(bias, "bias", dims=4, dtype=q.dtype)
@@ -214,17 +239,40 @@ def attention_ext_kv(y, q, k_cache, v_cache, nonpad, scale, bias=None, fused: Op
         if need:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    lib = load()
+    keep = (c, workspace, y, q, k_cache, v_cache, bias, nonpad, status)
     args = (_p(y), _p(q), _p(k_cache), _p(v_cache), _p(bias), None if c is None else ctypes.byref(c), _p(nonpad),
             float(scale))
     if Dv != D:
-        _check(load().attention_ext_kv_dv(*args, float(softcap), B, Hq, Hkv, S_q, max_seq, D, Dv, _dt(q),
-                                          _p(workspace), ws, _p(status), _stream(stream)))
-        return
+        return lib.attention_ext_kv_dv, (*args, float(softcap), B, Hq, Hkv, S_q, max_seq, D, Dv, _dt(q),
+                                         _p(workspace), ws, _p(status), _stream(stream)), keep
     tail = (B, Hq, Hkv, S_q, max_seq, D, _dt(q), _p(workspace), ws, _p(status), _stream(stream))
     if softcap:
-        _check(load().attention_ext_kv_softcap(*args, float(softcap), *tail))
-    else:
-        _check(load().attention_ext_kv(*args, *tail))
+        return lib.attention_ext_kv_softcap, (*args, float(softcap), *tail), keep
+    return lib.attention_ext_kv, (*args, *tail), keep
+
+
+def attention_ext_kv(y, q, k_cache, v_cache, nonpad, scale, bias=None, fused: Optional[BiasSpec] = None,
+                     workspace=None, status=None, stream=None, softcap: float = 0.0):
+    """Y = softmax(cap(scale*QK^T) + bias)V over the external cache; writes ``y`` (B,Hq,S_q,Dv).
+    ``softcap`` > 0 caps the scaled scores to softcap*tanh(x/softcap) before the
+    bias (attention_ext_kv_softcap); 0 is plain attention_ext_kv.  A v_cache
+    whose head size Dv differs from q's and k_cache's Dk goes through
+    attention_ext_kv_dv.
+
+    ``workspace`` (uint8 device tensor of attention_ext_kv_workspace_size bytes)
+    is allocated here when not given."""
+    fn, args, _ = _marshal_attention(y, q, k_cache, v_cache, nonpad, scale, bias, fused, workspace, status,
+                                     stream, softcap)
+    _check(fn(*args))
+
+
+def prepare_attention_ext_kv(y, q, k_cache, v_cache, nonpad, scale, bias=None, fused: Optional[BiasSpec] = None,
+                             workspace=None, status=None, stream=None, softcap: float = 0.0) -> PreparedCall:
+    """attention_ext_kv with its arguments marshalled once (PreparedCall); the
+    workspace, when not given, is allocated here and kept by the call."""
+    return PreparedCall(*_marshal_attention(y, q, k_cache, v_cache, nonpad, scale, bias, fused, workspace,
+                                            status, stream, softcap))
 
 
 def build_bias_from_bool_mask(bias, mask, stream=None):
@@ -239,10 +287,8 @@ def build_bias_from_bool_mask(bias, mask, stream=None):
     _check(load().build_bias_from_bool_mask(_p(bias), _p(mask), B, S_q, max_seq, _dt(bias), _stream(stream)))
 
 
-def attention_ext_kv_scatter(y, q, k_cache, v_cache, k_new, v_new, write_idx, nonpad, scale, bias=None,
-                             fused: Optional[BiasSpec] = None, workspace=None, status=None, stream=None):
-    """ext_kv_scatter of (k_new, v_new) at write_idx, then attention_ext_kv over
-    the updated caches, in one call (fused into the decode kernel where it runs)."""
+def _marshal_attention_scatter(y, q, k_cache, v_cache, k_new, v_new, write_idx, nonpad, scale, bias, fused,
+                               workspace, status, stream):
     for t, n in ((y, "y"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (k_new, "k_new"),
                  (v_new, "v_new")):
         _need(t, n, dims=4, dtype=q.dtype)
@@ -262,11 +308,29 @@ def attention_ext_kv_scatter(y, q, k_cache, v_cache, k_new, v_new, write_idx, no
         if need:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load().attention_ext_kv_scatter(_p(y), _p(q), _p(k_cache), _p(v_cache), _p(k_new), _p(v_new),
-                                           _p(write_idx), S_new, _p(bias),
-                                           None if c is None else ctypes.byref(c), _p(nonpad), float(scale),
-                                           B, Hq, Hkv, S_q, max_seq, D, _dt(q), _p(workspace), ws,
-                                           _p(status), _stream(stream)))
+    keep = (c, workspace, y, q, k_cache, v_cache, k_new, v_new, write_idx, bias, nonpad, status)
+    return load().attention_ext_kv_scatter, (_p(y), _p(q), _p(k_cache), _p(v_cache), _p(k_new), _p(v_new),
+                                             _p(write_idx), S_new, _p(bias),
+                                             None if c is None else ctypes.byref(c), _p(nonpad), float(scale),
+                                             B, Hq, Hkv, S_q, max_seq, D, _dt(q), _p(workspace), ws,
+                                             _p(status), _stream(stream)), keep
+
+
+def attention_ext_kv_scatter(y, q, k_cache, v_cache, k_new, v_new, write_idx, nonpad, scale, bias=None,
+                             fused: Optional[BiasSpec] = None, workspace=None, status=None, stream=None):
+    """ext_kv_scatter of (k_new, v_new) at write_idx, then attention_ext_kv over
+    the updated caches, in one call (fused into the decode kernel where it runs)."""
+    fn, args, _ = _marshal_attention_scatter(y, q, k_cache, v_cache, k_new, v_new, write_idx, nonpad, scale,
+                                             bias, fused, workspace, status, stream)
+    _check(fn(*args))
+
+
+def prepare_attention_ext_kv_scatter(y, q, k_cache, v_cache, k_new, v_new, write_idx, nonpad, scale, bias=None,
+                                     fused: Optional[BiasSpec] = None, workspace=None, status=None,
+                                     stream=None) -> PreparedCall:
+    """attention_ext_kv_scatter with its arguments marshalled once (PreparedCall)."""
+    return PreparedCall(*_marshal_attention_scatter(y, q, k_cache, v_cache, k_new, v_new, write_idx, nonpad,
+                                                    scale, bias, fused, workspace, status, stream))
 
 
 def attention_ext_kv_noalloc(y, q, k_cache, v_cache, nonpad, scale, bias=None,

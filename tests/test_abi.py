@@ -107,3 +107,35 @@ def test_workspace_size_with_two_head_sizes(lib):
     same = extkv.attention_ext_kv_workspace_size(1, 16, 8, 2048, 8192, 256, None)
     assert extkv.attention_ext_kv_workspace_size(1, 16, 8, 2048, 8192, 256, None, Dv=256) == same
     assert int(lib.attention_ext_kv_workspace_size_dv(0, 16, 8, 2048, 8192, 256, 256, extkv.EXTKV_BF16)) == 0
+
+
+def test_prepared_calls_marshal_once_and_reissue_the_call(lib):
+    """extkv.prepare_*: the arguments are converted once to the declared ctypes
+    types, and every call re-issues the C function (its host checks included).
+    CPU only: an empty batch launches nothing, an odd head size fails its
+    host check before any pointer is used."""
+    import torch
+
+    q = torch.zeros((0, 4, 1, 64), dtype=torch.bfloat16)
+    kc = torch.zeros((0, 2, 64, 64), dtype=torch.bfloat16)
+    nonpad = torch.zeros(0, dtype=torch.int64)
+    call = extkv.prepare_attention_ext_kv(torch.empty_like(q), q, kc, kc, nonpad, 0.125, stream=0)
+    assert all(a is None or isinstance(a, ctypes._SimpleCData) or type(a).__name__ == "CArgObject"
+               for a in call._args)
+    call()
+    call()
+    spec = extkv.BiasSpec(causal=True, window=16)
+    bias = torch.zeros((0, 1, 1, 64), dtype=torch.bfloat16)
+    extkv.prepare_build_static_cache_bias(bias, spec, nonpad, stream=0)()
+    scat = extkv.prepare_attention_ext_kv_scatter(torch.empty_like(q), q, kc, kc, kc[:, :, :1], kc[:, :, :1],
+                                                  nonpad, nonpad, 0.125, fused=spec, stream=0)
+    scat()
+    # a head size that is not a multiple of 8: refused on every call
+    q12 = torch.zeros((1, 4, 1, 12), dtype=torch.bfloat16)
+    k12 = torch.zeros((1, 2, 64, 12), dtype=torch.bfloat16)
+    bad = extkv.prepare_attention_ext_kv(torch.empty_like(q12), q12, k12, k12, torch.ones(1, dtype=torch.int64),
+                                         0.125, stream=0)
+    for _ in range(2):
+        with pytest.raises(extkv.ExtKVError) as e:
+            bad()
+        assert e.value.code == extkv.EXTKV_ERR_UNSUPPORTED

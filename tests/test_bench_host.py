@@ -76,3 +76,18 @@ def test_max_over_ranks_and_whole_job_value_gloo():
         assert (rank, local, world) == (r, r, 2)
         assert tmax == 2.0
         assert v == pytest.approx(100.0 * 2 / 2.0)
+
+
+def test_reference_arm_reports_the_same_config_as_ours(capsys):
+    """bench.py --impl reference (the oracle on the host cores) prints one JSON
+    line whose config is the dict the repo's arm builds for the same workload."""
+    import json
+    import bench
+    w = wl.C1_DECODE
+    bench.main(["--impl", "reference", "--workload", w.name, "--steps", "2", "--warmup", "1"])
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    nonpad, _, spans = wl.structure(w)
+    sb = bench.step_bytes(w, nonpad.numpy(), spans, "bias")
+    assert line["impl"] == "reference"
+    assert line["config"] == bench.step_config(w, "bias", 1, True, sb)
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
