@@ -1041,7 +1041,7 @@ cudaError_t launch_dm(const AttnArgs& a, const DecodeParams& prm, const CUtensor
   if (prm.plan) {
     const size_t plan_smem = 128 + ((max_tiles + 127) / 128) * 128 + kPlanScanBytes + 16;
     auto pk = decode_plan_kernel<MODE == kBias ? kBias : kFused>;
-    e = cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(plan_smem));
+    e = set_max_dynamic_smem(reinterpret_cast<const void*>(pk), plan_smem);
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(static_cast<unsigned>(a.B));
     cfg.blockDim = dim3(kPlanThreads);
@@ -1050,7 +1050,7 @@ cudaError_t launch_dm(const AttnArgs& a, const DecodeParams& prm, const CUtensor
     if (e != cudaSuccess) return e;
   }
   auto kern = attn_decode_kernel<DK, DV, SPW, MODE, CAP>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(S::bytes()));
+  e = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), S::bytes());
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(static_cast<unsigned>(prm.G));
   cfg.blockDim = dim3(32);

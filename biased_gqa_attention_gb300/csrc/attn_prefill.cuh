@@ -1417,13 +1417,9 @@ cudaError_t prefill_setup(const AttnArgs& a, int mode, int dv_chunk, PrefillPara
   prm.part = reinterpret_cast<float*>(wsb + term_tables_bytes(a.B, a.S_q, a.max_seq));
 
   if (mode == kBias) {
-    static std::once_flag plan_once;
-    static cudaError_t plan_err = cudaSuccess;
-    std::call_once(plan_once, [] {
-      plan_err = cudaFuncSetAttribute(prefill_plan_bias_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      kPlanSmem);
-    });
-    if (plan_err != cudaSuccess) return plan_err;
+    if (cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(prefill_plan_bias_kernel), kPlanSmem);
+        e != cudaSuccess)
+      return e;
     prefill_plan_bias_kernel<<<dim3(prm.n_kt, prm.n_pt, prm.B), kPlanThreads, kPlanSmem,
                                a.stream>>>(static_cast<const __nv_bfloat16*>(term), a.nonpad,
                                            static_cast<uint64_t*>(a.workspace), prm.S_q, prm.max_seq,
@@ -1445,13 +1441,10 @@ cudaError_t prefill_setup(const AttnArgs& a, int mode, int dv_chunk, PrefillPara
 template <int DK, int DV, int MODE, bool CAP>
 cudaError_t launch_dm(const AttnArgs& a, const char** name) {
   using C = Cfg<DK, DV, MODE>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_prefill_kernel<DK, DV, MODE, CAP>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-  });
-  if (attr_err != cudaSuccess) return attr_err;
+  if (cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(attn_prefill_kernel<DK, DV, MODE, CAP>),
+                                           C::kSmem);
+      e != cudaSuccess)
+    return e;
   const int64_t Dvf = a.Dv;  // the whole value head size
   if (Dvf % DV) return cudaErrorInvalidValue;
 

@@ -569,13 +569,10 @@ __global__ void __launch_bounds__(PairCfg<MODE>::kThreads, 1)
 template <int MODE, bool CAP>
 cudaError_t launch_pair(const AttnArgs& a, const char** name) {
   using C = PairCfg<MODE>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_prefill_pair_kernel<MODE, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    C::kSmem);
-  });
-  if (attr_err != cudaSuccess) return attr_err;
+  if (cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(attn_prefill_pair_kernel<MODE, CAP>),
+                                           C::kSmem);
+      e != cudaSuccess)
+    return e;
   CUtensorMap qmap, kmap, vmap, tmap, ymap;
   const uint64_t units = static_cast<uint64_t>(a.B * a.Hkv);
   const uint64_t k_dims[4] = {64, static_cast<uint64_t>(a.max_seq), 4, units};

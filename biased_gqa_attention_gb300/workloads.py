@@ -101,7 +101,21 @@ C5 = Workload(
     description="bf16 prefill at random offsets, causal + window 4096 + dense term, then KV-shared")
 
 ALL = [C1_PREFILL, C1_DECODE, C2, C3, C4, C5]
-BY_NAME = {w.name: w for w in ALL}
+
+# Decode steps outside the decode kernel's shapes (more than 256 batches; more
+# than 8 query rows per KV head), which run on the prefill kernel: the cost of
+# leaving the decode path, measured and tested beside the five workloads.
+DECODE_B512 = Workload(
+    "decode_b512_hq16_hkv8_d256_w1024", 6, B=512, Hq=16, Hkv=8, D=256, S_q=1, max_seq=4096,
+    dtype=torch.bfloat16, causal=True, window=1024, nonpad_range=(512, 4096),
+    description="C2 at 512 batches (beyond the decode kernel's batch tables)")
+DECODE_G16 = Workload(
+    "decode_b8_hq32_hkv2_d128_w1024", 7, B=8, Hq=32, Hkv=2, D=128, S_q=1, max_seq=4096,
+    dtype=torch.bfloat16, causal=True, window=1024, nonpad_range=(512, 4096),
+    description="decode with 16 query heads per KV head (beyond the decode kernel's 8 rows per unit)")
+CLIFFS = [DECODE_B512, DECODE_G16]
+
+BY_NAME = {w.name: w for w in ALL + CLIFFS}
 
 
 def small(w: Workload) -> Workload:
@@ -119,6 +133,10 @@ def small(w: Workload) -> Workload:
     if w.config_id == 5:
         return w.replace(name=w.name + "_small", B=3, S_q=77, max_seq=1200, window=300,
                          offset_range=(0, 1100))
+    if w.config_id == 6:  # still beyond 256 batches
+        return w.replace(name=w.name + "_small", B=300, max_seq=512, window=200, nonpad_range=(1, 512))
+    if w.config_id == 7:
+        return w.replace(name=w.name + "_small", B=3, max_seq=1000, window=200, nonpad_range=(130, 1000))
     raise ValueError(w)
 
 
