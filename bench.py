@@ -664,7 +664,12 @@ def run_reference(args, rank, local, world):
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel, per
 # (workload, mode), from an ncu capture of the kernel as committed (the capture's summary under
 # profiles/ names the template).  A kernel change makes an entry stale: drop it.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # attn_decode_kernel<256, 256, 2, 1, 0> (the step's call, with the fused scatter)
+    ("decode_b8_hq16_hkv8_d256_w1024", "bias"): 65.45e6,
+    # attn_prefill_kernel<256, 256, 1, 0>
+    ("prefill_s2048_hq16_hkv8_d256_w1024_spans", "bias"): 43.04e6,
+}
 
 
 def main(argv=None):
