@@ -9,10 +9,11 @@ namespace extkv {
 namespace {
 
 // Head size 256 on CTA pairs: the two query heads of a pair share a KV head
-// (an even group size) and the grid is large enough not to split keys.
+// (an even group size), the grid is large enough not to split keys, and the
+// rows are not packed (a pair holds one tile of each of its two heads).
 bool pair_ok(const AttnArgs& a) {
   return a.prefill_pairs && a.D == 256 && a.Dv == 256 && (a.Hq / a.Hkv) % 2 == 0 &&
-         prefill_splits(a.B, a.Hq, a.S_q) == 1;
+         !packs_rows(a.Hq, a.Hkv, a.S_q) && prefill_splits(a.B, a.Hq, a.S_q) == 1;
 }
 
 template <bool CAP>
@@ -35,11 +36,11 @@ cudaError_t launch_attn_prefill_equal(const AttnArgs& a, const char** name) {
   }
 }
 
-size_t prefill_workspace_bytes(int64_t B, int64_t Hq, int64_t S_q, int64_t max_seq, int64_t Dk, int64_t Dv,
-                               bool term) {
+size_t prefill_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t Dk,
+                               int64_t Dv, bool term) {
   (void)Dk;
   const int64_t n_vc = Dv / v_chunk(Dv);
-  const int ns = prefill_splits(B, Hq * n_vc, S_q);
+  const int ns = prefill_call_splits(B, Hq, Hkv, S_q, n_vc);
   if (!term && ns == 1) return 0;
   const size_t part = ns > 1 ? static_cast<size_t>(ns) * B * Hq * S_q * part_stride(static_cast<int>(Dv)) * 4 : 0;
   return term_tables_bytes(B, S_q, max_seq) + part;  // the partials follow the (maybe unused) term tables

@@ -174,6 +174,11 @@ struct PrefillParams {
   int n_split;
   float* part;
   uint32_t polls;  // limit of the pipeline's barrier waits
+  // Packed query rows (all positions of a query fit one tile, S_q <= 128, and
+  // a KV head serves several query heads): a tile holds the rows (head, s) of
+  // the group's heads one after the other, n_pk tiles per KV head, so each
+  // KV tile is read once for the whole group.
+  int packed, n_pk;
 };
 
 // floats per partial row: O, then max and sum, rounded to 16 bytes
@@ -600,12 +605,17 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
   const uint32_t lim = p.polls;  // pipeline waits; the drains keep the full limit
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // blockIdx.x = (h * n_vc + vc) * n_split + sp: query head, column chunk of Y, key split
+  // blockIdx.x = (hx * n_vc + vc) * n_split + sp: the tile's query head (or, with
+  // packed rows, hx = hk * n_pk + packed tile), column chunk of Y, key split
   const int sp = blockIdx.x % p.n_split, hv = blockIdx.x / p.n_split, pt = blockIdx.y, b = blockIdx.z;
-  const int h = hv / p.n_vc, vc = hv % p.n_vc;
+  const int hx = hv / p.n_vc, vc = hv % p.n_vc;
   const int g = p.Hq / p.Hkv;
-  const int hk = h / g;
-  const int q0 = pt * kBM;
+  const int hk = p.packed ? hx / p.n_pk : hx / g;
+  const int q0 = pt * kBM;  // position of the tile's first row (0 with packed rows)
+  // the tile's rows in the (B * Hq * S_q) query-row space, and how many are real
+  const int64_t row_base = p.packed ? (static_cast<int64_t>(b) * p.Hq + hk * g) * p.S_q + (hx % p.n_pk) * kBM
+                                    : (static_cast<int64_t>(b) * p.Hq + hx) * p.S_q + q0;
+  const int rows_here = p.packed ? min(kBM, g * p.S_q - (hx % p.n_pk) * kBM) : min(kBM, p.S_q - q0);
 
   if (tid == 0) {
     ptx::mbar_init(&bar.q_full, C::kQSmem ? 1 : C::kSoftWarps * 32);
@@ -646,24 +656,30 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
   // a shared-memory Q tile is needed whenever any key is live: start it first
   if (C::kQSmem && warp == 0 && lane == 0) {
     ptx::mbar_arrive_expect_tx(&bar.q_full, C::kQBytes);
-    ptx::tma_load_3d(sQ, &qmap, &bar.q_full, 0, (b * p.Hq + h) * p.S_q + q0, 0);
+    ptx::tma_load_3d(sQ, &qmap, &bar.q_full, 0, static_cast<int>(row_base), 0);
   }
 
   const int64_t np64 = p.nonpad[b];
   const bool bad = bad_nonpad(np64, p.max_seq);
-  if (bad && tid == 0 && h == 0 && vc == 0 && pt == 0 && sp == 0) report(p.status, EXTKV_DEV_BAD_NONPAD);
+  if (bad && tid == 0 && hx == 0 && vc == 0 && pt == 0 && sp == 0) report(p.status, EXTKV_DEV_BAD_NONPAD);
   const int np = bad ? 0 : static_cast<int>(np64);
   const int64_t qs = bad ? 0 : query_start(p.spec.q_start, b, np64, p.S_q);
   const uint64_t* cmrow = C::kTerm ? p.colmask + (static_cast<int64_t>(b) * p.n_pt + pt) * p.n_tiles : nullptr;
   const int64_t imp0 = MODE == kBias ? (static_cast<int64_t>(b) * p.n_pt + pt) * p.n_kt : 0;
 
-  // softmax threads: this thread's query row and its allowed key intervals
+  // softmax threads: this thread's query row (tile row `row`: query head h at
+  // position pos; prow: its row in the plan's tables and the term blocks,
+  // which are laid out by position) and its allowed key intervals
   const bool is_sm = warp >= 2;
   const int row = 32 * (warp & 3) + lane;
-  const bool row_valid = is_sm && q0 + row < p.S_q;
+  const bool row_valid = is_sm && row < rows_here;
+  const int64_t flat = row_base + row;
+  const int h = p.packed ? static_cast<int>(flat / p.S_q) - b * p.Hq : hx;
+  const int pos = p.packed ? static_cast<int>(flat % p.S_q) : q0 + row;
+  const int prow = p.packed ? pos : row;
   int a1 = 0, b1 = np, a2 = 0, b2 = 0;  // allowed keys: [a1, b1) U [a2, b2)
   if (kFusedMode && is_sm) {
-    const RowWindow w = row_window(p.spec, b, qs + q0 + row, np);
+    const RowWindow w = row_window(p.spec, b, qs + pos, np);
     const int64_t bl = w.band_lo < 0 ? 0 : w.band_lo, bh = w.band_hi < np ? w.band_hi : np;
     const int64_t sl = w.span_lo < 0 ? 0 : w.span_lo, sh = w.span_hi < np ? w.span_hi : np;
     a1 = static_cast<int>(bl < bh ? bl : 0);
@@ -903,7 +919,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
     if (!C::kQSmem && T > 0) {
       // this row of Q into tensor memory (rows past the chunk: zeros)
       const uint4* qrow =
-          reinterpret_cast<const uint4*>(p.q + ((static_cast<int64_t>(b) * p.Hq + h) * p.S_q + q0 + row) * DK);
+          reinterpret_cast<const uint4*>(p.q + (row_base + row) * DK);
 #pragma unroll
       for (int c = 0; c < DK / 64; ++c) {
         if (C::kSplit && (c & 1) != hh) continue;  // the pair shares the chunks
@@ -942,7 +958,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
       uint64_t al0, al1;
       if (pure) {
         const uint4 rb = *reinterpret_cast<const uint4*>(
-            p.rowmask + ((static_cast<int64_t>(b) * p.n_pt + pt) * kBM + row) * p.rm_stride + tile * 16);
+            p.rowmask + ((static_cast<int64_t>(b) * p.n_pt + pt) * kBM + prow) * p.rm_stride + tile * 16);
         al0 = rb.x | (static_cast<uint64_t>(rb.y) << 32);
         al1 = rb.z | (static_cast<uint64_t>(rb.w) << 32);
       } else if (kFusedMode) {
@@ -978,7 +994,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
               break;
             }
             ++t_seen;
-            load_swizzled_row(tw, sT + tb * C::kTermBytes + hh * (C::kTermBytes / 2), row);
+            load_swizzled_row(tw, sT + tb * C::kTermBytes + hh * (C::kTermBytes / 2), prow);
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&bar.t_empty[tb]);
           }
@@ -1089,7 +1105,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
           uint32_t sa[32], sb[32], tw[32];
           ptx::tmem_ld32(ts, sa);
           ptx::tmem_ld32(ts + 32, sb);
-          if (C::kTerm) load_swizzled_row(tw, tblk, row);
+          if (C::kTerm) load_swizzled_row(tw, tblk, prow);
           ptx::tmem_wait_ld();
           if constexpr (capped) {
             if (part0)
@@ -1104,7 +1120,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
           ptx::tmem_ld32(ts + 64, sa);
           ptx::tmem_ld32(ts + 96, sb);
           if (C::kTerm) {
-            load_swizzled_row(tw, tblk + C::kTermBytes / 2, row);
+            load_swizzled_row(tw, tblk + C::kTermBytes / 2, prow);
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&bar.t_empty[tb]);
           }
@@ -1219,8 +1235,8 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
     if (p.n_split > 1) {
       // a partial row of this split: unnormalised O (this CTA's DV columns),
       // the running max and sum (the same in every column chunk)
-      float* prow = p.part + ((static_cast<int64_t>(b * p.Hq + h) * p.n_split + sp) * p.S_q + q0 + row) *
-                                 part_stride(p.Dv);
+      float* prow_out = p.part + ((static_cast<int64_t>(b * p.Hq + h) * p.n_split + sp) * p.S_q + pos) *
+                                     part_stride(p.Dv);
       const bool live = ok && T > 0;
 #pragma unroll 1
       for (int c = c32_lo; c < c32_hi; ++c) {
@@ -1235,14 +1251,41 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
         if (row_valid) {
 #pragma unroll
           for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(prow + vc * DV + 32 * c + 4 * q) =
+            *reinterpret_cast<float4*>(prow_out + vc * DV + 32 * c + 4 * q) =
                 make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]), __uint_as_float(o[4 * q + 2]),
                             __uint_as_float(o[4 * q + 3]));
         }
       }
       if (row_valid && vc == 0 && hh == 0) {
-        prow[p.Dv] = live ? m_run : -INFINITY;
-        prow[p.Dv + 1] = live ? l_run : 0.f;
+        prow_out[p.Dv] = live ? m_run : -INFINITY;
+        prow_out[p.Dv + 1] = live ? l_run : 0.f;
+      }
+    } else if (p.packed) {
+      // packed rows: a warp's 32 rows may belong to several query heads, so
+      // each thread writes its own row (rows past the group's are not written)
+      __nv_bfloat16* yrow = p.y + (row_base + row) * p.Dv + vc * DV;
+#pragma unroll 1
+      for (int cb = cb_lo; cb < cb_hi; ++cb) {
+        uint32_t o[64];
+        if (ok && T > 0) {
+          ptx::tmem_ld32(tl + C::kOCol + 64 * cb, *reinterpret_cast<uint32_t(*)[32]>(o));
+          ptx::tmem_ld32(tl + C::kOCol + 64 * cb + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
+          ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) o[e] = 0;
+        }
+        if (ok && row_valid) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 2 * e]) * inv,
+                                      __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
+            *reinterpret_cast<uint4*>(yrow + 64 * cb + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
       }
     } else {
       uint8_t* stage = sKV + quad * kNB * 4096;
@@ -1347,13 +1390,30 @@ int n_plan_chunks(int64_t max_seq) { return static_cast<int>((max_seq + kPlanKey
 // the plan's column-mask table: one 64-bit word per 64 keys
 int n_mask_words(int64_t max_seq) { return static_cast<int>((max_seq + 63) / 64); }
 
-// Key splits per query tile: a grid of fewer CTAs than half the SMs has its
-// query tiles' key ranges split so that about one CTA per SM works.
-int prefill_splits(int64_t B, int64_t Hq, int64_t S_q) {
-  const int64_t ctas = B * Hq * n_query_tiles(S_q);
+// Key splits: a grid of fewer CTAs than half the SMs has its tiles' key
+// ranges split so that about one CTA per SM works.
+int splits_for(int64_t ctas) {
   const int sms = num_sms();
   if (ctas <= 0 || ctas * 2 > sms) return 1;
   return static_cast<int>(std::min<int64_t>(kMaxSplit, std::max<int64_t>(1, sms / ctas)));
+}
+int prefill_splits(int64_t B, int64_t Hq, int64_t S_q) { return splits_for(B * Hq * n_query_tiles(S_q)); }
+
+// The tiles per KV head with packed rows, and whether a call packs them: all
+// positions fit one tile and packing takes fewer tiles than one per query
+// head (otherwise the tiles are the same and the unpacked epilogue's TMA
+// stores are kept).
+int packed_tiles(int64_t Hq, int64_t Hkv, int64_t S_q) {
+  return static_cast<int>((Hq / Hkv * S_q + kBM - 1) / kBM);
+}
+bool packs_rows(int64_t Hq, int64_t Hkv, int64_t S_q) {
+  return S_q <= kBM && packed_tiles(Hq, Hkv, S_q) < Hq / Hkv;
+}
+
+// Key splits of a call with n_vc column chunks of Y, packed or not.
+int prefill_call_splits(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t n_vc) {
+  if (packs_rows(Hq, Hkv, S_q)) return splits_for(B * Hkv * packed_tiles(Hq, Hkv, S_q) * n_vc);
+  return prefill_splits(B, Hq * n_vc, S_q);
 }
 
 // bytes of the column-mask table, rounded to 256
@@ -1412,7 +1472,9 @@ cudaError_t prefill_setup(const AttnArgs& a, int mode, int dv_chunk, PrefillPara
   prm.Dv = static_cast<int>(Dvf);
   prm.n_vc = static_cast<int>(Dvf / dv_chunk);
   prm.status = a.status;
-  prm.n_split = prefill_splits(a.B, a.Hq * prm.n_vc, a.S_q);
+  prm.packed = packs_rows(a.Hq, a.Hkv, a.S_q) ? 1 : 0;
+  prm.n_pk = prm.packed ? packed_tiles(a.Hq, a.Hkv, a.S_q) : 0;
+  prm.n_split = prefill_call_splits(a.B, a.Hq, a.Hkv, a.S_q, prm.n_vc);
   prm.polls = wait_limit(a.wait_limit_plus1, kWaitPolls);
   prm.part = reinterpret_cast<float*>(wsb + term_tables_bytes(a.B, a.S_q, a.max_seq));
 
@@ -1491,7 +1553,8 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
   if (cudaError_t e = prefill_setup(a, MODE, DV, &prm); e != cudaSuccess) return e;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(prm.Hq * prm.n_vc * prm.n_split, prm.n_pt, prm.B);
+  // blockIdx.x: (query head, or packed tile of a KV head) x column chunk x key split
+  cfg.gridDim = dim3((prm.packed ? prm.Hkv * prm.n_pk : prm.Hq) * prm.n_vc * prm.n_split, prm.n_pt, prm.B);
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = a.stream;
@@ -1511,7 +1574,7 @@ cudaError_t launch_dm(const AttnArgs& a, const char** name) {
     e = cudaLaunchKernelEx(&cfg, prefill_merge_kernel, prm, prm.Dv);
     if (e != cudaSuccess) return e;
   }
-  *name = "attn_prefill_tcgen05";
+  *name = prm.packed ? "attn_prefill_tcgen05_packed" : "attn_prefill_tcgen05";
   // the plan kernel, the attention kernel, the merge of the key splits
   note_launches((C::kTerm ? 2 : 1) + (prm.n_split > 1 ? 1 : 0));
   return cudaGetLastError();

@@ -173,7 +173,7 @@ size_t attention_ext_kv_workspace_size_dv(int64_t B, int64_t Hq, int64_t Hkv, in
   size_t need = 0;
   if (decode_supported(a)) need = decode_workspace_bytes(B, Hq, Hkv, S_q, max_seq, Dk, Dv);
   if (prefill_supported(a)) {
-    const size_t pf = prefill_workspace_bytes(B, Hq, S_q, max_seq, Dk, Dv, true);
+    const size_t pf = prefill_workspace_bytes(B, Hq, Hkv, S_q, max_seq, Dk, Dv, true);
     need = pf > need ? pf : need;
   }
   return need;
@@ -297,7 +297,7 @@ int attention_impl(void* y, const void* q, const void* k_cache, const void* v_ca
   // a materialised bias or an extra term needs the prefill kernel's column-mask table
   // the column-mask table (a materialised bias or an extra term) and the
   // partials of key splits (small grids)
-  const size_t prefill_ws = prefill_workspace_bytes(B, Hq, S_q, max_seq, D, Dv, bias || (fused && fused->extra));
+  const size_t prefill_ws = prefill_workspace_bytes(B, Hq, Hkv, S_q, max_seq, D, Dv, bias || (fused && fused->extra));
   switch (g_algo) {
     case EXTKV_ALGO_GENERIC:
       if ((e = scatter_first(a, sc)) != cudaSuccess) break;

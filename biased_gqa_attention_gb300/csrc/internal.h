@@ -66,8 +66,8 @@ size_t decode_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, i
 cudaError_t launch_attn_decode(const AttnArgs& a, const char** name);
 bool prefill_supported(const AttnArgs& a);
 // Dk, Dv: the key and value head sizes (the partial rows of key splits hold Dv columns)
-size_t prefill_workspace_bytes(int64_t B, int64_t Hq, int64_t S_q, int64_t max_seq, int64_t Dk, int64_t Dv,
-                               bool term);
+size_t prefill_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t Dk,
+                               int64_t Dv, bool term);
 cudaError_t launch_attn_prefill(const AttnArgs& a, const char** name);
 
 int num_sms();

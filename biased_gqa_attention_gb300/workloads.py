@@ -177,7 +177,12 @@ def structure(w: Workload):
     if w.n_spans:
         lo, hi = w.span_start_range
         for b in range(B):
+            tries = 0
             while len(spans[b]) < w.n_spans:
+                tries += 1
+                if tries > 100000:  # the spans drawn so far leave no room for another
+                    raise ValueError(f"{w.name}: cannot place {w.n_spans} disjoint spans of {w.span_len} "
+                                     f"with starts in [{lo}, {hi}]")
                 s = int(torch.randint(lo, hi + 1, (1,), generator=gen))
                 if all(s + w.span_len <= t or t + w.span_len <= s for t, _ in spans[b]):
                     spans[b].append((s, w.span_len))
