@@ -434,6 +434,57 @@ int extkv_set_wait_polls(int polls) {
   return prev;
 }
 
+struct extkv_step {
+  cudaGraphExec_t exec;
+};
+
+int extkv_step_begin(void** stream) {
+  if (!stream) return fail(EXTKV_ERR_INVALID_ARG, "extkv_step_begin: null stream pointer");
+  *stream = nullptr;
+  cudaStream_t s = nullptr;
+  cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return cuda_fail(e, "extkv_step_begin: stream");
+  // thread-local mode: other threads' CUDA calls do not touch the capture
+  e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) {
+    cudaStreamDestroy(s);
+    return cuda_fail(e, "extkv_step_begin: capture");
+  }
+  *stream = s;
+  return EXTKV_OK;
+}
+
+int extkv_step_end(void* stream, extkv_step** step) {
+  if (!stream || !step) return fail(EXTKV_ERR_INVALID_ARG, "extkv_step_end: null argument");
+  *step = nullptr;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaGraph_t g = nullptr;
+  cudaError_t e = cudaStreamEndCapture(s, &g);
+  cudaStreamDestroy(s);
+  if (e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    return cuda_fail(e, "extkv_step_end: capture");
+  }
+  cudaGraphExec_t x = nullptr;
+  e = cudaGraphInstantiate(&x, g, 0);
+  cudaGraphDestroy(g);  // the instantiated graph does not refer to it
+  if (e != cudaSuccess) return cuda_fail(e, "extkv_step_end: instantiate");
+  *step = new extkv_step{x};
+  return EXTKV_OK;
+}
+
+int extkv_step_launch(const extkv_step* step, void* stream) {
+  if (!step) return fail(EXTKV_ERR_INVALID_ARG, "extkv_step_launch: null step");
+  const cudaError_t e = cudaGraphLaunch(step->exec, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? EXTKV_OK : cuda_fail(e, "extkv_step_launch");
+}
+
+void extkv_step_free(extkv_step* step) {
+  if (!step) return;
+  cudaGraphExecDestroy(step->exec);
+  delete step;
+}
+
 int extkv_set_algo(int algo) {
   if (algo < EXTKV_ALGO_AUTO || algo > EXTKV_ALGO_PREFILL_PAIR)
     return fail(EXTKV_ERR_INVALID_ARG, "extkv_set_algo: unknown algorithm %d", algo);

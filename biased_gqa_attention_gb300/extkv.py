@@ -28,7 +28,8 @@ SYMBOLS = ("ext_kv_scatter", "build_static_cache_bias", "attention_ext_kv_worksp
            "extkv_clear_status", "extkv_read_status",
            "extkv_last_error", "extkv_last_kernel", "extkv_last_launches", "extkv_set_algo",
            "extkv_set_wait_polls",
-           "attention_ext_kv_noalloc")
+           "attention_ext_kv_noalloc",
+           "extkv_step_begin", "extkv_step_end", "extkv_step_launch", "extkv_step_free")
 
 
 class ExtKVError(RuntimeError):
@@ -83,6 +84,14 @@ def load(path: str = LIB_PATH):
     lib.extkv_set_algo.argtypes = [I]
     lib.extkv_set_wait_polls.argtypes = [I]
     lib.extkv_set_wait_polls.restype = I
+    lib.extkv_step_begin.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+    lib.extkv_step_begin.restype = I
+    lib.extkv_step_end.argtypes = [P, ctypes.POINTER(ctypes.c_void_p)]
+    lib.extkv_step_end.restype = I
+    lib.extkv_step_launch.argtypes = [P, P]
+    lib.extkv_step_launch.restype = I
+    lib.extkv_step_free.argtypes = [P]
+    lib.extkv_step_free.restype = None
     for name in ("ext_kv_scatter", "build_static_cache_bias", "attention_ext_kv", "attention_ext_kv_noalloc",
                  "extkv_clear_status", "extkv_read_status", "extkv_set_algo"):
         getattr(lib, name).restype = I
@@ -426,3 +435,48 @@ class use_algo:
 
     def __exit__(self, *exc):
         extkv_set_algo(self.prev)
+
+
+class RecordedStep:
+    """A step recorded with StepRecorder: calling it starts every recorded
+    library call again with one launch, on ``stream`` (a torch stream or a raw
+    handle; default the current stream)."""
+
+    __slots__ = ("_h",)
+
+    def __init__(self, handle: int):
+        self._h = ctypes.c_void_p(handle)
+
+    def __call__(self, stream=None):
+        code = load().extkv_step_launch(self._h, _stream(stream))
+        if code != EXTKV_OK:
+            raise ExtKVError(code, load().extkv_last_error().decode())
+
+    def __del__(self):
+        if _lib is not None and self._h:
+            _lib.extkv_step_free(self._h)
+            self._h = ctypes.c_void_p()
+
+
+class StepRecorder:
+    """Records the library calls issued with ``stream=rec.stream`` inside the
+    block into ``rec.step`` (extkv_step_begin / extkv_step_end).  Issue each
+    call once before recording it, and call nothing that synchronises inside."""
+
+    def __enter__(self):
+        h = ctypes.c_void_p()
+        _check(load().extkv_step_begin(ctypes.byref(h)))
+        self.stream = h.value
+        self.step = None
+        return self
+
+    def __exit__(self, exc_type, exc, tb):
+        out = ctypes.c_void_p()
+        code = load().extkv_step_end(ctypes.c_void_p(self.stream), ctypes.byref(out))
+        if exc_type is not None:
+            if out.value:
+                load().extkv_step_free(out)
+            return False
+        _check(code)
+        self.step = RecordedStep(out.value)
+        return False

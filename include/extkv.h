@@ -341,6 +341,35 @@ int extkv_last_launches(void);
 int extkv_set_wait_polls(int polls);
 
 /*
+ * Recorded steps.  A caller that issues the same library calls over the same
+ * buffers every step (a decode loop) can record them once and then start the
+ * whole step with one launch, instead of one host launch per kernel (the
+ * decode path of attention_ext_kv launches three).
+ *   extkv_step_begin   creates a stream, starts capturing the calling thread's
+ *                      work on it into a CUDA graph, and returns the stream in
+ *                      *stream; the library calls that follow are issued with it.
+ *   extkv_step_end     ends that capture, instantiates the graph, destroys the
+ *                      stream and returns the step in *step (null on an error,
+ *                      and the capture is discarded).
+ *   extkv_step_launch  starts the step on `stream` (any stream of the same
+ *                      device): every call of it runs again, reading and
+ *                      writing the buffers it was recorded with -- their
+ *                      contents may change between launches, their addresses
+ *                      may not -- and the status word it was given.
+ *   extkv_step_free    releases a step (null: nothing).
+ * Between begin and end call nothing that synchronises (extkv_read_status),
+ * and issue each call once before recording it, so that its first-use setup
+ * (kernel attributes, tensor maps) stays outside the capture.  The caller owns
+ * the step.  Returns EXTKV_OK, EXTKV_ERR_INVALID_ARG for a null argument, or
+ * EXTKV_ERR_CUDA (message in extkv_last_error).
+ */
+typedef struct extkv_step extkv_step;
+int extkv_step_begin(void **stream);
+int extkv_step_end(void *stream, extkv_step **step);
+int extkv_step_launch(const extkv_step *step, void *stream);
+void extkv_step_free(extkv_step *step);
+
+/*
  * Attention kernel selection for the calling thread.  EXTKV_ALGO_AUTO picks
  * by shape and type; the others force one kernel, and attention_ext_kv then
  * returns EXTKV_ERR_UNSUPPORTED for shapes that kernel cannot run.  Returns

@@ -139,3 +139,15 @@ def test_prepared_calls_marshal_once_and_reissue_the_call(lib):
         with pytest.raises(extkv.ExtKVError) as e:
             bad()
         assert e.value.code == extkv.EXTKV_ERR_UNSUPPORTED
+
+
+def test_recorded_step_entry_points_check_their_arguments(lib):
+    """extkv_step_*: null arguments are refused on the host (no CUDA call)."""
+    P = ctypes.c_void_p
+    assert lib.extkv_step_begin(None) == extkv.EXTKV_ERR_INVALID_ARG
+    out = ctypes.c_void_p(0x1234)
+    assert lib.extkv_step_end(None, ctypes.byref(out)) == extkv.EXTKV_ERR_INVALID_ARG
+    assert lib.extkv_step_end(P(0x10000), None) == extkv.EXTKV_ERR_INVALID_ARG
+    assert lib.extkv_step_launch(None, None) == extkv.EXTKV_ERR_INVALID_ARG
+    assert "null" in extkv.extkv_last_error()
+    lib.extkv_step_free(None)  # releasing nothing is a no-op
