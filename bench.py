@@ -579,19 +579,22 @@ def secondary(args, device, peaks, peak_src):
     from biased_gqa_attention_gb300 import extkv as ek
     res = {}
     stream = torch.cuda.Stream(device)
-    # C3-C5, then two decode steps outside the decode kernel's shapes (the
-    # cost of the fallback to the prefill kernel)
-    for w in (wl.C3, wl.C4, wl.C5, *wl.CLIFFS):
+    # C3-C5, two decode steps outside the decode kernel's shapes (the cost of
+    # the fallback to the prefill kernel), then C2 and C3 in the other bias mode
+    other = "fused" if args.mode == "bias" else "bias"
+    runs = [(w, args.mode) for w in (wl.C3, wl.C4, wl.C5, *wl.CLIFFS)] + [(wl.C2, other), (wl.C3, other)]
+    for w, mode in runs:
+        key = w.name if mode == args.mode else f"{w.name}@{mode}"
         nonpad, _, spans = wl.structure(w)
         nonpad = nonpad.numpy()
-        ab, af = attention_work(w, nonpad, spans, args.mode)
+        ab, af = attention_work(w, nonpad, spans, mode)
         touched = ab if w.S_q == 1 else ab + w.B * w.S_q * w.max_seq * 2
         R = min(_rotation(touched, device), 6)
-        dec = Decoder(w, device, args.mode, R)
+        dec = Decoder(w, device, mode, R)
         with torch.cuda.stream(stream):
             for r in range(R):
                 dec.scatter(r)
-                if args.mode == "bias":
+                if mode == "bias":
                     dec.bias(r)
             for i in range(3):
                 dec.attention(i % R)
@@ -612,18 +615,18 @@ def secondary(args, device, peaks, peak_src):
         assert ek.extkv_read_status(dec.status) == ek.EXTKV_OK, ek.extkv_last_error()
         if w.S_q == 1:
             ach = ab / (ms / 1e3) / 1e9
-            res[w.name] = {"bound": "hbm", "achieved": round(ach, 1), "unit": "GB/s",
+            res[key] = {"bound": "hbm", "achieved": round(ach, 1), "unit": "GB/s",
                            "peak": peaks["hbm_gbs"], "frac": round(ach / peaks["hbm_gbs"], 4),
                            "launch_us": round(ms * 1e3, 2), "kernel": ek.extkv_last_kernel(),
                            "launches": ek.extkv_last_launches(), "algorithmic_bytes": ab}
         else:
             ach = af / (ms / 1e3) / 1e12
-            res[w.name] = {"bound": "tensor", "achieved": round(ach, 2), "unit": "TFLOP/s",
+            res[key] = {"bound": "tensor", "achieved": round(ach, 2), "unit": "TFLOP/s",
                            "peak": peaks["bf16_tflops"], "frac": round(ach / peaks["bf16_tflops"], 4),
                            "launch_us": round(ms * 1e3, 2), "kernel": ek.extkv_last_kernel(),
                            "launches": ek.extkv_last_launches(), "algorithmic_flops": af}
-        res[w.name]["peak_source"] = peak_src
-        res[w.name]["timing"] = f"CUDA graph of {n} attention calls over {R} rotating input sets"
+        res[key]["peak_source"] = peak_src
+        res[key]["timing"] = f"CUDA graph of {n} attention calls over {R} rotating input sets"
         del dec, g
         torch.cuda.empty_cache()
     return res
