@@ -11,6 +11,10 @@
 // tensor cores' time for it.  On a pair, each SM stores half of every K and V
 // tile (64 keys of K, 128 columns of V) and serves that half to both tensor
 // cores: about 190 KB per SM per tile, below the tensor-core time.
+// Measured, the pair is slower than the single-SM kernel on the shapes tried
+// (a 128-key tile every 2.0 us against 1.5 us: each P V waits for the softmax
+// of both halves, and Q K_{j+2} for P_j V_j, across the two SMs), so it runs
+// only when asked for (EXTKV_ALGO_PREFILL_PAIR).
 //
 // Layout of the work: cluster (b, head pair, tile of 128 query rows); CTA
 // rank r (0 or 1) holds query head 2m + r: its Q tile, its S and O in its own
