@@ -8,13 +8,13 @@ namespace extkv {
 
 namespace {
 
-int grid_for(int64_t Dk, int64_t Dv, int64_t items_max) {
-  if (Dk != Dv) return decode_grid_mixed(Dk, Dv, items_max);
+DecodeShape shape_for(int64_t Dk, int64_t Dv, int64_t B, int64_t items_max) {
+  if (Dk != Dv) return decode_shape_mixed(Dk, Dv, B, items_max);
   switch (Dk) {
-    case 64: return persistent_grid<64, 64>(items_max);
-    case 128: return persistent_grid<128, 128>(items_max);
-    case 256: return persistent_grid<256, 256>(items_max);
-    default: return persistent_grid<512, 512>(items_max);
+    case 64: return decode_shape<64, 64>(B, items_max);
+    case 128: return decode_shape<128, 128>(B, items_max);
+    case 256: return decode_shape<256, 256>(B, items_max);
+    default: return decode_shape<512, 512>(B, items_max);
   }
 }
 
@@ -29,7 +29,7 @@ bool mixed_pair(int64_t Dk, int64_t Dv) {
 size_t decode_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t Dk,
                               int64_t Dv) {
   const int64_t max_tiles = (max_seq + kTile - 1) / kTile;
-  return ws_layout(B, Hkv, max_tiles, grid_for(Dk, Dv, B * Hkv * max_tiles), Hq / Hkv * S_q, Dv).total;
+  return ws_layout(B, Hkv, max_tiles, shape_for(Dk, Dv, B, B * Hkv * max_tiles).G, Hq / Hkv * S_q, Dv).total;
 }
 
 bool decode_supported(const AttnArgs& a) {
@@ -44,13 +44,11 @@ bool decode_supported(const AttnArgs& a) {
   if ((a.bias || (a.fused && a.extra)) && a.max_seq % 8) return false;
   const int64_t max_tiles = (a.max_seq + kTile - 1) / kTile;
   const int64_t units = a.B * a.Hkv;
-  if (a.B > kMaxB || units >= (1 << 20) || max_tiles > 65535) return false;
+  if (a.B > kMaxBatches || units >= (1 << 20) || max_tiles > 65535) return false;
   if (a.B * a.Hq * a.S_q > 0x7fffffff || units * max_tiles > 0x7fffffff) return false;
-  // a slice must fit the plan's work table
-  const int64_t G = grid_for(a.D, a.Dv, units * max_tiles);
-  const int64_t slice = (units * max_tiles + G - 1) / G;
-  if (slice > kMaxWork) return false;
-  return true;
+  // the per-batch tables and the longest slice's work list fit shared memory
+  const DecodeShape d = shape_for(a.D, a.Dv, a.B, units * max_tiles);
+  return d.occ > 0 && d.slice <= d.wc;
 }
 
 cudaError_t launch_attn_decode(const AttnArgs& a, const char** name) {

@@ -53,13 +53,24 @@
 
 namespace extkv {
 
+// A decode call's grid (G CTAs, occ resident per SM), the batches its shared
+// tables hold (tb), the items its work list holds (wc), its longest slice and
+// its dynamic shared memory.
+struct DecodeShape {
+  int G, tb, wc, occ;
+  int64_t slice;
+  size_t bytes;
+};
+
 namespace {
 
 constexpr int kTile = 16;                  // keys per tile (M of the QK^T mma)
 constexpr int kRows = 8;                   // query rows per unit (N of the mma)
 constexpr uint32_t kWaitPolls = 1u << 22;  // bounded mbarrier waits
-constexpr int kMaxWork = 512;              // items of one slice (plan mode table)
-constexpr int kMaxB = 256;                 // batches (tables in shared memory)
+constexpr int kMaxWork = 512;              // items of one slice the default tables hold (plan mode)
+constexpr int kMaxB = 256;                 // batches the default tables hold (shared memory)
+constexpr int kMaxBatches = 1024;          // batches the decode kernel takes (larger tables)
+constexpr int kWorkCap = 16384;            // items of one slice it takes
 constexpr int kPlanThreads = 256;
 constexpr int kPlanScanBytes = 64 * 1024;  // bias rows staged by the plan
 constexpr int kMergeThreads = 256;
@@ -121,6 +132,7 @@ struct DecodeParams {
   int B, Hq, Hkv, S_q, g, R, D;  // D: the value head size (columns of Y and of the partials)
   int max_seq, max_tiles;
   int G;     // CTAs of the decode grid
+  int tb;    // batches the shared-memory tables hold (>= B, a multiple of 32)
   int PS;    // floats of one partial (part_floats(R, D))
   int plan;  // 1: live tiles come from the plan kernel
   int32_t* count;
@@ -418,11 +430,13 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBars);  // stages, Q slots
   uint64_t* qbars = bars + SPW;
+  // per-batch tables for p.tb batches, then the slice's work list over the runs table
+  // (the default layout of Smem when p.tb = kMaxB)
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + S::kPrefix);
-  int32_t* np_s = reinterpret_cast<int32_t*>(smem + S::kNp);
-  int32_t* wi_s = reinterpret_cast<int32_t*>(smem + S::kWi);
-  Runs* runs_s = reinterpret_cast<Runs*>(smem + S::kRuns);
-  uint16_t* work = reinterpret_cast<uint16_t*>(smem + S::kWork);
+  int32_t* np_s = prefix + p.tb + 4;  // (tb + 1) entries and 12 bytes
+  int32_t* wi_s = np_s + p.tb;
+  Runs* runs_s = reinterpret_cast<Runs*>(wi_s + p.tb);
+  uint16_t* work = reinterpret_cast<uint16_t*>(runs_s);
   const int lane = threadIdx.x;
   const int c = blockIdx.x;
   const float lowest = Elem<__nv_bfloat16>::lowest();
@@ -985,31 +999,62 @@ struct PairCfg {
   static constexpr int SPW = DecodeCfg<(DK > DV ? DK : DV)>::SPW;
 };
 
+// Shared memory of a decode CTA whose tables hold tb batches and a work list
+// of wc items: the default layout (with its occupancy pad) at least.
 template <int DK, int DV>
-int persistent_grid(int64_t items_max) {
+size_t decode_smem(int tb, int wc) {
   using S = Smem<DK, DV, PairCfg<DK, DV>::SPW>;
+  const size_t tables = static_cast<size_t>(tb + 1) * 4 + 12 + static_cast<size_t>(tb) * 8 +
+                        std::max<size_t>(static_cast<size_t>(tb) * 16, static_cast<size_t>(wc) * 2);
+  return std::max<size_t>(S::bytes(), 1024 + S::kPrefix + tables);
+}
+
+// Resident decode CTAs per SM at `bytes` of shared memory (per device and size).
+template <int DK, int DV>
+int decode_occupancy(size_t bytes) {
   static std::mutex mu;
-  static int cached_dev = -1, cached_occ = 0;
+  struct Entry {
+    int dev;
+    size_t bytes;
+    int occ;
+  };
+  static Entry entries[32];
+  static int n = 0;
   int dev = 0;
   cudaGetDevice(&dev);
-  int occ;
-  {
-    std::lock_guard<std::mutex> g(mu);
-    if (cached_dev != dev) {
-      auto kern = attn_decode_kernel<DK, DV, PairCfg<DK, DV>::SPW, kBias, false>;
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(S::bytes()));
-      int o = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, 32, S::bytes()) != cudaSuccess || o <= 0) {
-        (void)cudaGetLastError();
-        o = 1;
-      }
-      cached_occ = o;
-      cached_dev = dev;
-    }
-    occ = cached_occ;
+  std::lock_guard<std::mutex> g(mu);
+  for (int i = 0; i < n; ++i)
+    if (entries[i].dev == dev && entries[i].bytes == bytes) return entries[i].occ;
+  auto kern = attn_decode_kernel<DK, DV, PairCfg<DK, DV>::SPW, kBias, false>;
+  int o = 0;
+  if (set_max_dynamic_smem(reinterpret_cast<const void*>(kern), bytes) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, 32, bytes) != cudaSuccess || o <= 0) {
+    (void)cudaGetLastError();
+    o = 0;
   }
-  const int64_t g = static_cast<int64_t>(occ) * num_sms();
-  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(g, items_max)));
+  if (n < 32) entries[n++] = Entry{dev, bytes, o};
+  return o;
+}
+
+// Grid and shared-memory tables of a call over B batches and at most
+// items_max work items: the tables hold max(B, 256) batches and the longest
+// slice; the slice follows from the grid, the grid from the shared memory the
+// tables take (a few rounds settle it).  occ 0: the tables do not fit.
+template <int DK, int DV>
+DecodeShape decode_shape(int64_t B, int64_t items_max) {
+  DecodeShape d;
+  d.tb = static_cast<int>((std::max<int64_t>(B, kMaxB) + 31) / 32 * 32);
+  d.wc = kMaxWork;
+  for (int round = 0; round < 4; ++round) {
+    d.bytes = decode_smem<DK, DV>(d.tb, d.wc);
+    d.occ = decode_occupancy<DK, DV>(d.bytes);
+    const int64_t g = static_cast<int64_t>(std::max(d.occ, 1)) * num_sms();
+    d.G = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(g, items_max)));
+    d.slice = (items_max + d.G - 1) / d.G;
+    if (d.slice <= d.wc || d.slice > kWorkCap) break;
+    d.wc = static_cast<int>((d.slice + 63) / 64 * 64);
+  }
+  return d;
 }
 
 inline bool needs_plan(const AttnArgs& a) {
@@ -1027,7 +1072,7 @@ inline int mode_of(const AttnArgs& a) {
 template <int DK, int DV, int MODE, bool CAP>
 cudaError_t launch_dm(const AttnArgs& a, const DecodeParams& prm, const CUtensorMap& kmap,
                       const CUtensorMap& vmap, const CUtensorMap& qmap, const CUtensorMap& tmap,
-                      int64_t max_tiles) {
+                      int64_t max_tiles, size_t smem) {
   constexpr int SPW = PairCfg<DK, DV>::SPW;
   using S = Smem<DK, DV, SPW>;
   cudaLaunchAttribute pdl[1];
@@ -1050,11 +1095,11 @@ cudaError_t launch_dm(const AttnArgs& a, const DecodeParams& prm, const CUtensor
     if (e != cudaSuccess) return e;
   }
   auto kern = attn_decode_kernel<DK, DV, SPW, MODE, CAP>;
-  e = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), S::bytes());
+  e = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(static_cast<unsigned>(prm.G));
   cfg.blockDim = dim3(32);
-  cfg.dynamicSmemBytes = S::bytes();
+  cfg.dynamicSmemBytes = smem;
   e = cudaLaunchKernelEx(&cfg, kern, kmap, vmap, qmap, tmap, prm);
   if (e != cudaSuccess) return e;
   const int n_cg = merge_groups(prm.R, DV);
@@ -1068,13 +1113,13 @@ cudaError_t launch_dm(const AttnArgs& a, const DecodeParams& prm, const CUtensor
 
 template <int DK, int DV, int MODE>
 cudaError_t launch_dmc(const AttnArgs& a, const DecodeParams& prm, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                       const CUtensorMap& qmap, const CUtensorMap& tmap, int64_t max_tiles) {
+                       const CUtensorMap& qmap, const CUtensorMap& tmap, int64_t max_tiles, size_t smem) {
   if constexpr (DK == DV) {
-    return a.softcap > 0.f ? launch_dm<DK, DV, MODE, true>(a, prm, kmap, vmap, qmap, tmap, max_tiles)
-                           : launch_dm<DK, DV, MODE, false>(a, prm, kmap, vmap, qmap, tmap, max_tiles);
+    return a.softcap > 0.f ? launch_dm<DK, DV, MODE, true>(a, prm, kmap, vmap, qmap, tmap, max_tiles, smem)
+                           : launch_dm<DK, DV, MODE, false>(a, prm, kmap, vmap, qmap, tmap, max_tiles, smem);
   } else {  // two head sizes: no softcap instantiation (the prefill kernel takes that case)
     if (a.softcap > 0.f) return cudaErrorInvalidValue;
-    return launch_dm<DK, DV, MODE, false>(a, prm, kmap, vmap, qmap, tmap, max_tiles);
+    return launch_dm<DK, DV, MODE, false>(a, prm, kmap, vmap, qmap, tmap, max_tiles, smem);
   }
 }
 
@@ -1082,7 +1127,9 @@ template <int DK, int DV>
 cudaError_t launch_d(const AttnArgs& a, const char** name) {
   const int64_t max_tiles = (a.max_seq + kTile - 1) / kTile;
   const int64_t units = a.B * a.Hkv;
-  const int G = persistent_grid<DK, DV>(units * max_tiles);
+  const DecodeShape shape = decode_shape<DK, DV>(a.B, units * max_tiles);
+  if (shape.occ <= 0 || shape.slice > shape.wc) return cudaErrorInvalidValue;
+  const int G = shape.G;
   const WsLayout ws = ws_layout(a.B, a.Hkv, max_tiles, G, a.Hq / a.Hkv * a.S_q, DV);
   if (!a.workspace || a.ws_bytes < ws.total) return cudaErrorInvalidValue;
   uint8_t* wsb = static_cast<uint8_t*>(a.workspace);
@@ -1136,6 +1183,7 @@ cudaError_t launch_d(const AttnArgs& a, const char** name) {
   prm.max_seq = static_cast<int>(a.max_seq);
   prm.max_tiles = static_cast<int>(max_tiles);
   prm.G = G;
+  prm.tb = shape.tb;
   prm.PS = static_cast<int>(part_floats(prm.R, DV));
   prm.plan = needs_plan(a);
   prm.count = reinterpret_cast<int32_t*>(wsb + ws.count);
@@ -1153,10 +1201,10 @@ cudaError_t launch_d(const AttnArgs& a, const char** name) {
 
   cudaError_t e;
   switch (mode_of(a)) {
-    case kNone: e = launch_dmc<DK, DV, kNone>(a, prm, kmap, vmap, qmap, tmap, max_tiles); break;
-    case kBias: e = launch_dmc<DK, DV, kBias>(a, prm, kmap, vmap, qmap, tmap, max_tiles); break;
-    case kFused: e = launch_dmc<DK, DV, kFused>(a, prm, kmap, vmap, qmap, tmap, max_tiles); break;
-    default: e = launch_dmc<DK, DV, kFusedExtra>(a, prm, kmap, vmap, qmap, tmap, max_tiles); break;
+    case kNone: e = launch_dmc<DK, DV, kNone>(a, prm, kmap, vmap, qmap, tmap, max_tiles, shape.bytes); break;
+    case kBias: e = launch_dmc<DK, DV, kBias>(a, prm, kmap, vmap, qmap, tmap, max_tiles, shape.bytes); break;
+    case kFused: e = launch_dmc<DK, DV, kFused>(a, prm, kmap, vmap, qmap, tmap, max_tiles, shape.bytes); break;
+    default: e = launch_dmc<DK, DV, kFusedExtra>(a, prm, kmap, vmap, qmap, tmap, max_tiles, shape.bytes); break;
   }
   if (e != cudaSuccess) return e;
   *name = prm.k_new ? "attn_decode_streamk_mma_scatter" : "attn_decode_streamk_mma";
@@ -1167,6 +1215,6 @@ cudaError_t launch_d(const AttnArgs& a, const char** name) {
 
 // Launchers for the head-size pairs of each translation unit.
 cudaError_t launch_attn_decode_mixed(const AttnArgs& a, const char** name);  // Dk != Dv
-int decode_grid_mixed(int64_t Dk, int64_t Dv, int64_t items_max);
+DecodeShape decode_shape_mixed(int64_t Dk, int64_t Dv, int64_t B, int64_t items_max);
 
 }  // namespace extkv

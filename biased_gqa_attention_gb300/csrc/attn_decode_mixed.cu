@@ -7,13 +7,13 @@
 
 namespace extkv {
 
-int decode_grid_mixed(int64_t Dk, int64_t Dv, int64_t items_max) {
-  if (Dk == 128 && Dv == 256) return persistent_grid<128, 256>(items_max);
-  if (Dk == 128 && Dv == 512) return persistent_grid<128, 512>(items_max);
-  if (Dk == 256 && Dv == 128) return persistent_grid<256, 128>(items_max);
-  if (Dk == 256 && Dv == 512) return persistent_grid<256, 512>(items_max);
-  if (Dk == 512 && Dv == 128) return persistent_grid<512, 128>(items_max);
-  return persistent_grid<512, 256>(items_max);
+DecodeShape decode_shape_mixed(int64_t Dk, int64_t Dv, int64_t B, int64_t items_max) {
+  if (Dk == 128 && Dv == 256) return decode_shape<128, 256>(B, items_max);
+  if (Dk == 128 && Dv == 512) return decode_shape<128, 512>(B, items_max);
+  if (Dk == 256 && Dv == 128) return decode_shape<256, 128>(B, items_max);
+  if (Dk == 256 && Dv == 512) return decode_shape<256, 512>(B, items_max);
+  if (Dk == 512 && Dv == 128) return decode_shape<512, 128>(B, items_max);
+  return decode_shape<512, 256>(B, items_max);
 }
 
 cudaError_t launch_attn_decode_mixed(const AttnArgs& a, const char** name) {

@@ -102,13 +102,14 @@ C5 = Workload(
 
 ALL = [C1_PREFILL, C1_DECODE, C2, C3, C4, C5]
 
-# Decode steps outside the decode kernel's shapes (more than 256 batches; more
-# than 8 query rows per KV head), which run on the prefill kernel: the cost of
-# leaving the decode path, measured and tested beside the five workloads.
+# Decode steps at the edges of the decode kernel's shapes, measured and tested
+# beside the five workloads: 512 batches (larger than its default shared-memory
+# tables, sized per call), and 16 query heads per KV head (more than the 8 query
+# rows of a decode unit: such steps run on the prefill kernel).
 DECODE_B512 = Workload(
     "decode_b512_hq16_hkv8_d256_w1024", 6, B=512, Hq=16, Hkv=8, D=256, S_q=1, max_seq=4096,
     dtype=torch.bfloat16, causal=True, window=1024, nonpad_range=(512, 4096),
-    description="C2 at 512 batches (beyond the decode kernel's batch tables)")
+    description="C2 at 512 batches (per-call tables larger than the default 256 batches)")
 DECODE_G16 = Workload(
     "decode_b8_hq32_hkv2_d128_w1024", 7, B=8, Hq=32, Hkv=2, D=128, S_q=1, max_seq=4096,
     dtype=torch.bfloat16, causal=True, window=1024, nonpad_range=(512, 4096),
