@@ -15,9 +15,14 @@
  * Conventions shared by every entry point
  *   - Pointers named *_cache, q, y, bias, extra, status, workspace, nonpad,
  *     write_idx, q_start, spans, span_offsets are DEVICE pointers, owned by
- *     the caller.  The library allocates no memory and keeps no pointer after
- *     a call returns.  Structs passed by pointer (extkv_bias_spec) are HOST
- *     memory, read during the call only.
+ *     the caller.  A call allocates no device memory (the workspace is the
+ *     caller's; attention_ext_kv_noalloc uses a static array of the library)
+ *     and no pointer is used after the call's kernels finish, except by a
+ *     recorded step (extkv_step_*), which replays its calls on the buffers it
+ *     was recorded with until it is freed.  Host-side caches of encoded
+ *     tensor maps are keyed by pointer values and never dereferenced.
+ *     Structs passed by pointer (extkv_bias_spec) are HOST memory, read
+ *     during the call only.
  *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL is the legacy default stream) and never synchronises, except
  *     extkv_read_status.
