@@ -29,7 +29,9 @@ bool mixed_pair(int64_t Dk, int64_t Dv) {
 size_t decode_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t Dk,
                               int64_t Dv) {
   const int64_t max_tiles = (max_seq + kTile - 1) / kTile;
-  return ws_layout(B, Hkv, max_tiles, shape_for(Dk, Dv, B, B * Hkv * max_tiles).G, Hq / Hkv * S_q, Dv).total;
+  const int64_t gr = Hq / Hkv * S_q, n_rg = row_groups(gr);
+  return ws_layout(B, Hkv * n_rg, max_tiles, shape_for(Dk, Dv, B, B * Hkv * n_rg * max_tiles).G,
+                   std::min<int64_t>(gr, kRows), Dv).total;
 }
 
 bool decode_supported(const AttnArgs& a) {
@@ -39,11 +41,13 @@ bool decode_supported(const AttnArgs& a) {
   } else if (a.D != 64 && a.D != 128 && a.D != 256 && a.D != 512) {
     return false;
   }
-  if ((a.Hq / a.Hkv) * a.S_q > kRows) return false;
+  // up to kMaxRowGroups units of 8 query rows per KV head; a stage's bias or
+  // extra-term block holds the 16 keys of every query position (S_q <= 8)
+  if ((a.Hq / a.Hkv) * a.S_q > kRows * kMaxRowGroups || a.S_q > kRows) return false;
   // 16-byte rows for the bias / extra-term block copies
   if ((a.bias || (a.fused && a.extra)) && a.max_seq % 8) return false;
   const int64_t max_tiles = (a.max_seq + kTile - 1) / kTile;
-  const int64_t units = a.B * a.Hkv;
+  const int64_t units = a.B * a.Hkv * row_groups((a.Hq / a.Hkv) * a.S_q);
   if (a.B > kMaxBatches || units >= (1 << 20) || max_tiles > 65535) return false;
   if (a.B * a.Hq * a.S_q > 0x7fffffff || units * max_tiles > 0x7fffffff) return false;
   // the per-batch tables and the longest slice's work list fit shared memory

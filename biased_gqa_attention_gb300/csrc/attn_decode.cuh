@@ -1,10 +1,10 @@
 // attn_decode.cuh -- stream-K split-KV decode attention over the external
 // static cache.
 //
-// Work unit: one (batch b, KV head) pair and its R = (Hq/Hkv) * S_q query
-// rows (R <= 8), which share every K/V row they read ("ONNX Domain Attention
-// (Opset 23/24) CUDA Patterns", section 1: GQA by reshaping Q, no KV
-// replication).  Decode is HBM-bound ("Skill: Attention Optimization": decode
+// Work unit: one (batch b, KV head, row group): up to 8 of the KV head's
+// R = (Hq/Hkv) * S_q query rows (R <= 64, in at most 8 groups), which share
+// every K/V row they read ("ONNX Domain Attention (Opset 23/24) CUDA
+// Patterns", section 1: GQA by reshaping Q, no KV replication).  Decode is HBM-bound ("Skill: Attention Optimization": decode
 // is memory-bandwidth bound regardless of kernel), so the aim is to stream
 // every live K/V row exactly once with every SM busy to the end.  Q and K
 // carry DK columns, V and Y DV (equal, or a pair of 128/256/512: the
@@ -66,6 +66,7 @@ namespace {
 
 constexpr int kTile = 16;                  // keys per tile (M of the QK^T mma)
 constexpr int kRows = 8;                   // query rows per unit (N of the mma)
+constexpr int kMaxRowGroups = 8;           // units of 8 rows per KV head (g * S_q <= 64; S_q <= 8)
 constexpr uint32_t kWaitPolls = 1u << 22;  // bounded mbarrier waits
 constexpr int kMaxWork = 512;              // items of one slice the default tables hold (plan mode)
 constexpr int kMaxB = 256;                 // batches the default tables hold (shared memory)
@@ -105,6 +106,9 @@ struct WsLayout {
 // floats of one partial: max[8], sum[8], then the unit's R rows of Dv
 inline int64_t part_floats(int64_t R, int64_t Dv) { return 2 * kRows + R * Dv; }
 
+// A KV head's gr = (Hq / Hkv) * S_q query rows as units of at most 8 rows
+inline int64_t row_groups(int64_t gr) { return (gr + kRows - 1) / kRows; }
+
 WsLayout ws_layout(int64_t B, int64_t Hkv, int64_t max_tiles, int64_t G, int64_t R, int64_t Dv) {
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   WsLayout l;
@@ -113,7 +117,7 @@ WsLayout ws_layout(int64_t B, int64_t Hkv, int64_t max_tiles, int64_t G, int64_t
   o = al(o + static_cast<size_t>(B) * 4);
   l.tiles = o;  // uint16 live tile list per batch (plan mode)
   o = al(o + static_cast<size_t>(B * max_tiles) * 2);
-  l.info = o;  // int4 per unit: first CTA, slices, slot in the first CTA
+  l.info = o;  // int4 per unit: first CTA, slices, slot in the first CTA (Hkv: units of a batch)
   o = al(o + static_cast<size_t>(B * Hkv) * 16);
   l.part = o;  // per CTA, two partials: m[8], l[8], O[R][Dv] fp32
   o = al(o + static_cast<size_t>(G) * 2 * part_floats(R, Dv) * 4);
@@ -130,6 +134,9 @@ struct DecodeParams {
   float scale;
   float softcap;  // > 0: scores capped before the bias
   int B, Hq, Hkv, S_q, g, R, D;  // D: the value head size (columns of Y and of the partials)
+  // R: query rows of a unit (at most 8); a KV head's GR = g * S_q rows form n_rg
+  // units of up to 8 rows (row groups) that read the same K/V tiles
+  int GR, n_rg;
   int max_seq, max_tiles;
   int G;     // CTAs of the decode grid
   int tb;    // batches the shared-memory tables hold (>= B, a multiple of 32)
@@ -333,7 +340,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeP
 // ---- per-batch tables shared by the decode and merge kernels --------------------
 
 // Fills np_s[b] and (without a plan) runs_s[b], then prefix_s[b] = first item
-// of batch b (Hkv units of cnt[b] items each), prefix_s[B] = T.  One warp.
+// of batch b (Hkv * n_rg units of cnt[b] items each), prefix_s[B] = T.  One warp.
 template <int MODE>
 __device__ __forceinline__ int64_t batch_tables(const DecodeParams& p, int lane, int32_t* prefix_s,
                                                 int32_t* np_s, Runs* runs_s, int32_t* wi_s) {
@@ -356,7 +363,7 @@ __device__ __forceinline__ int64_t batch_tables(const DecodeParams& p, int lane,
         runs_s[b] = r;
         cnt = r.count();
       }
-      v = cnt * p.Hkv;
+      v = cnt * p.Hkv * p.n_rg;
     }
     int incl = v;
     for (int o = 1; o < 32; o <<= 1) {
@@ -411,9 +418,9 @@ struct Smem {
   static constexpr size_t bytes() { return 1024 + kEnd + kPad; }
 };
 
-// Position in the item sequence: unit (b, kvh), tile index kk of cnt.
+// Position in the item sequence: unit (b, kvh, row group rg), tile index kk of cnt.
 struct Cursor {
-  int b, kvh, kk, cnt;
+  int b, kvh, rg, kk, cnt;
 };
 
 // CAP: the scores are softcapped (a separate instantiation, so that the
@@ -460,7 +467,7 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
     for (int b = lane; b < p.B; b += 32) {
       if (prefix[b + 1] != prefix[b]) continue;
       if (!p.plan && bad_nonpad(p.nonpad[b], p.max_seq)) report(p.status, EXTKV_DEV_BAD_NONPAD);
-      for (int h = 0; h < p.Hkv; ++h) p.info[b * p.Hkv + h] = make_int4(-1, 0, 0, 0);
+      for (int u = 0; u < p.Hkv * p.n_rg; ++u) p.info[b * p.Hkv * p.n_rg + u] = make_int4(-1, 0, 0, 0);
     }
   }
   // Slice over min(G, T) CTAs: every slice holds at least one item.
@@ -497,24 +504,29 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
   const int64_t x0 = (static_cast<int64_t>(c) * T) / G, x1 = (static_cast<int64_t>(c + 1) * T) / G;
   const int n = static_cast<int>(x1 - x0);
 
+  const int upb = p.Hkv * p.n_rg;  // units of a batch
   auto cursor_at = [&](int64_t x) {
     Cursor q;
     q.b = batch_of(prefix, p.B, x);
-    q.cnt = (prefix[q.b + 1] - prefix[q.b]) / p.Hkv;
+    q.cnt = (prefix[q.b + 1] - prefix[q.b]) / upb;
     const int r = static_cast<int>(x - prefix[q.b]);
-    q.kvh = r / q.cnt;
-    q.kk = r - q.kvh * q.cnt;
+    const int u = r / q.cnt;
+    q.kvh = u / p.n_rg;
+    q.rg = u - q.kvh * p.n_rg;
+    q.kk = r - u * q.cnt;
     return q;
   };
   auto advance = [&](Cursor& q) {
     if (++q.kk < q.cnt) return;
     q.kk = 0;
+    if (++q.rg < p.n_rg) return;
+    q.rg = 0;
     if (++q.kvh < p.Hkv) return;
     q.kvh = 0;
     do {
       ++q.b;
     } while (q.b < p.B && prefix[q.b + 1] == prefix[q.b]);
-    if (q.b < p.B) q.cnt = (prefix[q.b + 1] - prefix[q.b]) / p.Hkv;
+    if (q.b < p.B) q.cnt = (prefix[q.b + 1] - prefix[q.b]) / upb;
   };
   if (p.plan) {
     // the slice's tile numbers, from the plan's per-batch lists
@@ -540,7 +552,7 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
   Cursor pc = cursor_at(x0);
   int pk = 0, p_seg = -1, c_seg = -1;
   const uint32_t stage_tx = S::kStageBytes + (kTerm ? 32u * p.S_q : 0u);
-  int p_row0 = 0, p_bh = 0;
+  int p_row0 = 0, p_bh = 0, p_nr = 0;
   auto fill = [&](int consumed) {
     while (pk < n && pk < consumed + SPW) {
       bool q_regs = false;
@@ -548,7 +560,8 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
         if (p_seg + 1 > c_seg + 1) break;  // both Q slots busy
         ++p_seg;
         p_bh = pc.b * p.Hkv + pc.kvh;
-        p_row0 = (pc.b * p.Hq + pc.kvh * p.g) * p.S_q;
+        p_row0 = (pc.b * p.Hq + pc.kvh * p.g) * p.S_q + pc.rg * kRows;
+        p_nr = min(kRows, p.GR - pc.rg * kRows);
         if constexpr (kQReg) {
           q_regs = true;  // loaded once this stage's requests are out
         } else if (lane == 0) {
@@ -576,8 +589,8 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
           const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + static_cast<int64_t>(p_row0 + row) * DK) + (lane & 3);
 #pragma unroll
           for (int ks = 0; ks < kKSteps; ++ks) {
-            qn[ks][0] = row < p.R ? __ldg(qrow + 8 * ks) : 0u;
-            qn[ks][1] = row < p.R ? __ldg(qrow + 8 * ks + 4) : 0u;
+            qn[ks][0] = row < p_nr ? __ldg(qrow + 8 * ks) : 0u;
+            qn[ks][1] = row < p_nr ? __ldg(qrow + 8 * ks + 4) : 0u;
           }
         }
       }
@@ -592,8 +605,9 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
   constexpr int kAcc = kKSteps >= 16 ? 4 : 2;  // independent QK^T accumulator chains
   uint32_t qf[kQReg ? kKSteps : 1][2];
   const int r0 = 2 * (lane & 3), r1 = r0 + 1;
-  const bool ok0 = r0 < p.R, ok1 = r1 < p.R;
-  const int i0 = r0 % p.S_q, i1 = r1 % p.S_q;
+  // this lane's two rows of the current unit: real or not, and their query positions
+  bool ok0 = false, ok1 = false;
+  int i0 = 0, i1 = 0;
   float o[DV / 16][4];
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   Win32 w0{}, w1{};
@@ -620,7 +634,8 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
     l1 += __shfl_xor_sync(0xffffffffu, l1, 8);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 16);
     const Cursor& u = cur_unit;
-    const int64_t row0 = (static_cast<int64_t>(u.b) * p.Hq + static_cast<int64_t>(u.kvh) * p.g) * p.S_q;
+    const int64_t row0 =
+        (static_cast<int64_t>(u.b) * p.Hq + static_cast<int64_t>(u.kvh) * p.g) * p.S_q + u.rg * kRows;
     if (ub >= x0 && ub + u.cnt <= x1) {
       const bool live0 = l0 > 0.f && !failed, live1 = l1 > 0.f && !failed;
       const float inv0 = live0 ? 1.f / l0 : 0.f, inv1 = live1 ? 1.f / l1 : 0.f;
@@ -680,11 +695,18 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
       fill(k);  // the producer may now enter the next unit
       cur_unit = cc;
       ub = x0 + k - cc.kk;
+      {
+        const int nr = min(kRows, p.GR - cc.rg * kRows);  // rows of this unit
+        ok0 = r0 < nr;
+        ok1 = r1 < nr;
+        i0 = (cc.rg * kRows + r0) % p.S_q;
+        i1 = (cc.rg * kRows + r1) % p.S_q;
+      }
       if (cc.kk == 0 && lane == 0) {
         // this slice holds the unit's first item: record where its partials live
         const int64_t last = ub + cc.cnt - 1;
         const int c_last = static_cast<int>(((last + 1) * G - 1) / T);  // slice holding `last`
-        p.info[cc.b * p.Hkv + cc.kvh] = make_int4(c, c_last - c + 1, ub <= x0 ? 0 : 1, 0);
+        p.info[(cc.b * p.Hkv + cc.kvh) * p.n_rg + cc.rg] = make_int4(c, c_last - c + 1, ub <= x0 ? 0 : 1, 0);
       }
       np = np_s[cc.b];
       if (p.k_new) w_new = wi_s[cc.b];  // -1: the scatter skipped this batch, no patch
@@ -907,15 +929,15 @@ template <int MODE>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p, int n_cg) {
   constexpr int kPre = 16;  // slices whose loads are in flight together
   const int u = blockIdx.x / n_cg, cg = blockIdx.x % n_cg;
-  const int b = u / p.Hkv, kvh = u % p.Hkv;
-  const int D = p.D, R = p.R;
+  const int b = u / (p.Hkv * p.n_rg), kvh = (u / p.n_rg) % p.Hkv, rg = u % p.n_rg;
+  const int D = p.D, R = min(kRows, p.GR - rg * kRows);  // rows of this unit
   const int cols = D / 4 / n_cg;  // float4 per row in this group
   const int i = threadIdx.x;
   const int r = i / cols, d4 = (cg * cols + i % cols) * 4;
   ptx::grid_launch_dependents();
   ptx::grid_dependency_wait();
   const int4 info = p.info[u];
-  const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + static_cast<int64_t>(kvh) * p.g) * p.S_q;
+  const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + static_cast<int64_t>(kvh) * p.g) * p.S_q + rg * kRows;
   if (i >= R * cols) return;
   auto store = [&](const float4& acc) {
     __nv_bfloat16* yr = p.y + (row0 + r) * D + d4;
@@ -1103,7 +1125,7 @@ cudaError_t launch_dm(const AttnArgs& a, const DecodeParams& prm, const CUtensor
   e = cudaLaunchKernelEx(&cfg, kern, kmap, vmap, qmap, tmap, prm);
   if (e != cudaSuccess) return e;
   const int n_cg = merge_groups(prm.R, DV);
-  cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.Hkv * n_cg));
+  cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.Hkv * prm.n_rg * n_cg));
   cfg.blockDim = dim3(static_cast<unsigned>((prm.R * (DV / 4 / n_cg) + 31) / 32 * 32));
   cfg.dynamicSmemBytes = 0;
   e = cudaLaunchKernelEx(&cfg, decode_merge_kernel<MODE>, prm, n_cg);
@@ -1126,11 +1148,12 @@ cudaError_t launch_dmc(const AttnArgs& a, const DecodeParams& prm, const CUtenso
 template <int DK, int DV>
 cudaError_t launch_d(const AttnArgs& a, const char** name) {
   const int64_t max_tiles = (a.max_seq + kTile - 1) / kTile;
-  const int64_t units = a.B * a.Hkv;
-  const DecodeShape shape = decode_shape<DK, DV>(a.B, units * max_tiles);
+  const int64_t units = a.B * a.Hkv;  // K/V heads (the views' last dimension)
+  const int64_t gr = a.Hq / a.Hkv * a.S_q, n_rg = row_groups(gr);
+  const DecodeShape shape = decode_shape<DK, DV>(a.B, units * n_rg * max_tiles);
   if (shape.occ <= 0 || shape.slice > shape.wc) return cudaErrorInvalidValue;
   const int G = shape.G;
-  const WsLayout ws = ws_layout(a.B, a.Hkv, max_tiles, G, a.Hq / a.Hkv * a.S_q, DV);
+  const WsLayout ws = ws_layout(a.B, a.Hkv * n_rg, max_tiles, G, std::min<int64_t>(gr, kRows), DV);
   if (!a.workspace || a.ws_bytes < ws.total) return cudaErrorInvalidValue;
   uint8_t* wsb = static_cast<uint8_t*>(a.workspace);
 
@@ -1178,7 +1201,9 @@ cudaError_t launch_d(const AttnArgs& a, const char** name) {
   prm.Hkv = static_cast<int>(a.Hkv);
   prm.S_q = static_cast<int>(a.S_q);
   prm.g = static_cast<int>(a.Hq / a.Hkv);
-  prm.R = static_cast<int>(a.Hq / a.Hkv * a.S_q);
+  prm.GR = static_cast<int>(gr);
+  prm.n_rg = static_cast<int>(n_rg);
+  prm.R = static_cast<int>(std::min<int64_t>(gr, kRows));
   prm.D = DV;
   prm.max_seq = static_cast<int>(a.max_seq);
   prm.max_tiles = static_cast<int>(max_tiles);

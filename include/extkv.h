@@ -382,7 +382,8 @@ void extkv_step_free(extkv_step *step);
  */
 #define EXTKV_ALGO_AUTO 0
 #define EXTKV_ALGO_GENERIC 1 /* fp32 SIMT, one warp per query row: any supported shape */
-#define EXTKV_ALGO_DECODE 2  /* stream-K split-KV decode: bf16, S_q*Hq/Hkv <= 8, D in {64,128,256,512} */
+#define EXTKV_ALGO_DECODE 2  /* stream-K split-KV decode: bf16, S_q <= 8, S_q*Hq/Hkv <= 64, up to 1024
+                                batches, D in {64,128,256,512} */
 #define EXTKV_ALGO_PREFILL 3 /* tcgen05/TMEM prefill: bf16, head sizes 64/64 or any pair of 128, 256, 512;
                                 one CTA per query tile */
 #define EXTKV_ALGO_PREFILL_PAIR 4 /* the same prefill on CTA pairs with 2-SM MMAs (two query heads of a
