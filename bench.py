@@ -256,6 +256,11 @@ class Decoder:
             self.sets.append(s)
         self.status = ek.new_status(device)
         self.workspace = ek.new_workspace(base.q, base.k_cache)
+        # The sets were drawn and copied on the current stream, and their blocks
+        # may be ones the caching allocator took back from the generator's
+        # temporaries with writes still queued there; the steps run on another
+        # stream, so nothing of that work may still be pending when they start.
+        torch.cuda.synchronize(device)
 
     def scatter(self, r):
         s = self.sets[r]
@@ -515,6 +520,9 @@ def run_e2e(dec: Decoder, K: int, W: int, world: int, device):
             views[k].copy_(d[k])
             d[k] = views[k]
         dev_bufs.append(b)
+    # the buffers were filled on the current stream; the copy streams below
+    # write them next, and an event nobody has recorded yet orders nothing
+    torch.cuda.synchronize(device)
     R = len(dec.sets)
     y_hosts = [torch.empty(s["y"].shape, dtype=s["y"].dtype, pin_memory=True) for _ in range(R)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
