@@ -439,6 +439,7 @@ def run_ours(args, rank, local, world):
     # status after the timed region: no device-side error may hide in the numbers
     assert ek.extkv_read_status(dec.status) == ek.EXTKV_OK, ek.extkv_last_error()
     kernel = ek.extkv_last_kernel()
+    traffic = args.traffic if args.traffic is not None else NCU_TRAFFIC.get((w.name, args.mode, kernel))
 
     # e2e: the public API with pinned host buffers, copies inside the timed region
     e2e = run_e2e(dec, K, W, world, device)
@@ -448,13 +449,13 @@ def run_ours(args, rank, local, world):
     if attn_avg_ms and prefill:
         achieved = attn_f / (attn_avg_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": args.traffic,
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
                 "kernel": kernel, "launch_us": round(attn_avg_ms * 1e3, 3),
                 "algorithmic_flops": attn_f, "peak_source": peak_src}
     elif attn_avg_ms:
         achieved = attn_b / (attn_avg_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": args.traffic,
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                 "kernel": kernel, "launch_us": round(attn_avg_ms * 1e3, 3),
                 "algorithmic_bytes": attn_b, "peak_source": peak_src}
 
@@ -719,13 +720,14 @@ def run_reference(args, rank, local, world):
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel, per
-# (workload, mode), from an ncu capture of the kernel as committed (the capture's summary under
-# profiles/ names the template).  A kernel change makes an entry stale: drop it.
+# (workload, mode, the name extkv_last_kernel() reports), from an ncu capture of the kernel as
+# committed (the capture's summary under profiles/ names the template).  A call that runs another
+# kernel finds no entry (traffic null); a change to a kernel makes its entry stale: drop it.
 NCU_TRAFFIC = {
     # attn_decode_kernel<256, 256, 2, 1, 0> (the step's call, with the fused scatter)
-    ("decode_b8_hq16_hkv8_d256_w1024", "bias"): 65.45e6,
+    ("decode_b8_hq16_hkv8_d256_w1024", "bias", "attn_decode_streamk_mma_scatter"): 65.45e6,
     # attn_prefill_kernel<256, 256, 1, 0>
-    ("prefill_s2048_hq16_hkv8_d256_w1024_spans", "bias"): 43.04e6,
+    ("prefill_s2048_hq16_hkv8_d256_w1024_spans", "bias", "attn_prefill_tcgen05"): 43.04e6,
 }
 
 
@@ -747,8 +749,6 @@ def main(argv=None):
                     help="ncu dram bytes per launch of the dominant kernel (default: the committed capture "
                          "for this workload and mode, if any)")
     args = ap.parse_args(argv)
-    if args.traffic is None:
-        args.traffic = NCU_TRAFFIC.get((args.workload, args.mode))
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     rank, local, world = dist_env()

@@ -35,6 +35,7 @@ size_t decode_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, i
 }
 
 bool decode_supported(const AttnArgs& a) {
+  if (a.decode_variant == kDecodeCluster) return decode_cluster_size(a) > 0;
   if (a.dtype != EXTKV_BF16) return false;
   if (a.Dv != a.D) {
     if (!mixed_pair(a.D, a.Dv) || a.softcap > 0.f) return false;
@@ -56,6 +57,19 @@ bool decode_supported(const AttnArgs& a) {
 }
 
 cudaError_t launch_attn_decode(const AttnArgs& a, const char** name) {
+  // The cluster kernel where every unit gets the full 8 CTAs resident at once
+  // (no plan, tables or merge); stream-K otherwise.  The cluster kernel's time
+  // follows the unit with the most live tiles, stream-K's the average, so with
+  // fewer CTAs per unit (longer shares) stream-K's balance wins (measured: the
+  // global-layer decode, 64 units at head size 512 with 4 CTAs each, 141 us
+  // against 86 us).
+  constexpr int kClusterMin = 8;
+  if (a.decode_variant != kDecodeStreamK) {
+    const int C = decode_cluster_size(a);
+    if (C > 0 && (a.decode_variant == kDecodeCluster || C >= kClusterMin))
+      return launch_attn_decode_cluster(a, C, name);
+    if (a.decode_variant == kDecodeCluster) return cudaErrorInvalidValue;
+  }
   if (a.Dv != a.D) return launch_attn_decode_mixed(a, name);
   switch (a.D) {
     case 64: return launch_d<64, 64>(a, name);

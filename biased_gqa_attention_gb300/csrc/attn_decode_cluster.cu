@@ -1,0 +1,42 @@
+// attn_decode_cluster.cu -- which decode calls the cluster kernel takes, and
+// its dispatch over the head sizes.
+#include "attn_decode_cluster.cuh"
+
+namespace extkv {
+
+int decode_cluster_size(const AttnArgs& a) {
+  if (a.dtype != EXTKV_BF16 || a.Dv != a.D) return 0;
+  if (a.D != 64 && a.D != 128 && a.D != 256 && a.D != 512) return 0;
+  if (a.Hkv <= 0 || a.Hq % a.Hkv) return 0;
+  // one unit of at most 8 query rows per KV head
+  if ((a.Hq / a.Hkv) * a.S_q > kRows || a.S_q > kRows) return 0;
+  // the fused specification's live tiles in closed form (several positions
+  // with spans need a per-tile test)
+  if (a.fused && needs_plan(a)) return 0;
+  // 16-byte rows for the bias / extra-term copies; a materialised bias is
+  // scanned from one copy of the batch's rows
+  if ((a.bias || (a.fused && a.extra)) && a.max_seq % 8) return 0;
+  if (a.bias && a.S_q * a.max_seq * 2 > kScanBytes) return 0;
+  const int64_t max_tiles = (a.max_seq + kTile - 1) / kTile;
+  if (max_tiles > 65535 || a.B * a.Hq * a.S_q > 0x7fffffff) return 0;
+  const int64_t units = a.B * a.Hkv;
+  if (units <= 0 || units > (1 << 20)) return 0;
+  switch (a.D) {
+    case 64: return cluster_size_for<64, 64>(units);
+    case 128: return cluster_size_for<128, 128>(units);
+    case 256: return cluster_size_for<256, 256>(units);
+    default: return cluster_size_for<512, 512>(units);
+  }
+}
+
+cudaError_t launch_attn_decode_cluster(const AttnArgs& a, int C, const char** name) {
+  switch (a.D) {
+    case 64: return launch_dc<64>(a, C, name);
+    case 128: return launch_dc<128>(a, C, name);
+    case 256: return launch_dc<256>(a, C, name);
+    case 512: return launch_dc<512>(a, C, name);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace extkv

@@ -270,6 +270,9 @@ int attention_impl(void* y, const void* q, const void* k_cache, const void* v_ca
   a.stream = static_cast<cudaStream_t>(stream);
   a.wait_limit_plus1 = g_wait_limit_plus1;
   a.prefill_pairs = g_algo == EXTKV_ALGO_PREFILL_PAIR ? 1 : 0;
+  a.decode_variant = g_algo == EXTKV_ALGO_DECODE_STREAMK   ? kDecodeStreamK
+                     : g_algo == EXTKV_ALGO_DECODE_CLUSTER ? kDecodeCluster
+                                                           : kDecodeAuto;
 
   const char* name = "";
   cudaError_t e;
@@ -304,6 +307,8 @@ int attention_impl(void* y, const void* q, const void* k_cache, const void* v_ca
       e = launch_attn_generic(a, &name);
       break;
     case EXTKV_ALGO_DECODE:
+    case EXTKV_ALGO_DECODE_STREAMK:
+    case EXTKV_ALGO_DECODE_CLUSTER:
       if (!decode_supported(a))
         return fail(EXTKV_ERR_UNSUPPORTED, "attention_ext_kv: the decode kernel cannot run this shape/type");
       if (int rc = check_workspace(a, decode_ws)) return rc;
@@ -486,7 +491,7 @@ void extkv_step_free(extkv_step* step) {
 }
 
 int extkv_set_algo(int algo) {
-  if (algo < EXTKV_ALGO_AUTO || algo > EXTKV_ALGO_PREFILL_PAIR)
+  if (algo < EXTKV_ALGO_AUTO || algo > EXTKV_ALGO_DECODE_CLUSTER)
     return fail(EXTKV_ERR_INVALID_ARG, "extkv_set_algo: unknown algorithm %d", algo);
   int prev = g_algo;
   g_algo = algo;

@@ -45,7 +45,13 @@ struct AttnArgs {
   // 1: the prefill at head size 256 may run on CTA pairs (2-SM MMAs); 0: one
   // CTA per query tile only
   int prefill_pairs;
+  // which decode kernel takes a decode call: kDecodeAuto (by shape),
+  // kDecodeStreamK (plan, stream-K decode, merge) or kDecodeCluster (one
+  // cluster per KV head, one kernel)
+  int decode_variant;
 };
+
+constexpr int kDecodeAuto = 0, kDecodeStreamK = 1, kDecodeCluster = 2;
 
 // Each launcher returns cudaSuccess or the launch error; `name` receives the
 // kernel's name for extkv_last_kernel().
@@ -64,6 +70,10 @@ bool decode_supported(const AttnArgs& a);
 size_t decode_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t Dk,
                               int64_t Dv);
 cudaError_t launch_attn_decode(const AttnArgs& a, const char** name);
+// The cluster decode kernel: CTAs per unit it would use for this call (0: it
+// cannot take the call), and its launch with that many.
+int decode_cluster_size(const AttnArgs& a);
+cudaError_t launch_attn_decode_cluster(const AttnArgs& a, int C, const char** name);
 bool prefill_supported(const AttnArgs& a);
 // Dk, Dv: the key and value head sizes (the partial rows of key splits hold Dv columns)
 size_t prefill_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t Dk,

@@ -20,6 +20,7 @@ EXTKV_F32, EXTKV_BF16 = 0, 1
 EXTKV_OK, EXTKV_ERR_INVALID_ARG, EXTKV_ERR_UNSUPPORTED, EXTKV_ERR_CUDA, EXTKV_ERR_DEVICE = 0, -1, -2, -3, -4
 EXTKV_DEV_BAD_WRITE_IDX, EXTKV_DEV_BAD_NONPAD, EXTKV_DEV_TIMEOUT = 0x1, 0x2, 0x4
 ALGO_AUTO, ALGO_GENERIC, ALGO_DECODE, ALGO_PREFILL, ALGO_PREFILL_PAIR = 0, 1, 2, 3, 4
+ALGO_DECODE_STREAMK, ALGO_DECODE_CLUSTER = 5, 6
 
 # Every symbol include/extkv.h declares.
 SYMBOLS = ("ext_kv_scatter", "build_static_cache_bias", "attention_ext_kv_workspace_size",

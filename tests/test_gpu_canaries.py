@@ -52,8 +52,10 @@ def _expected_caches(inp):
 
 
 CASES = [
-    ("decode_bias", wl.small(wl.C2), "bias", ek.ALGO_DECODE),
-    ("decode_fused_extra", wl.small(wl.C4).replace(extra=True), "fused", ek.ALGO_DECODE),
+    ("decode_bias", wl.small(wl.C2), "bias", ek.ALGO_DECODE_STREAMK),
+    ("decode_fused_extra", wl.small(wl.C4).replace(extra=True), "fused", ek.ALGO_DECODE_STREAMK),
+    ("decode_cluster_bias", wl.small(wl.C2), "bias", ek.ALGO_DECODE_CLUSTER),
+    ("decode_cluster_fused_extra", wl.small(wl.C4).replace(extra=True), "fused", ek.ALGO_DECODE_CLUSTER),
     ("prefill_bias", wl.small(wl.C3), "bias", ek.ALGO_PREFILL),
     ("prefill_splits_extra", wl.small(wl.C5), "fused", ek.ALGO_PREFILL),
     ("prefill_pair", PAIR_SHAPE, "bias", ek.ALGO_PREFILL_PAIR),

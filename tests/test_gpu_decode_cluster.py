@@ -1,0 +1,143 @@
+"""The cluster decode kernel: one thread-block cluster per (batch, KV head),
+each CTA streaming an equal share of the unit's live tiles and the shares
+combined through distributed shared memory ("Skill: Attention Optimization":
+decode is memory-bandwidth bound; "ONNX Domain Attention (Opset 23/24) CUDA
+Patterns", section 1: the query heads of a KV group share its K/V rows).
+
+Checked against the oracle element by element with the kernel forced: every
+bias mode, head sizes 64-512, two query positions, units with fewer live
+tiles than CTAs, empty batches, poisoned slots; the decode
+workloads at full size on sampled rows; the automatic choice for the decode
+workload; bit-for-bit repeatability (the shares are combined in a fixed
+order); and the shapes the kernel refuses.
+"""
+import numpy as np
+import pytest
+import torch
+
+from biased_gqa_attention_gb300 import extkv as ek
+from biased_gqa_attention_gb300 import workloads as wl
+from gpu_path import TOL, max_err, oracle_path, run_gpu, sample_rows, spec_of
+from test_gpu_invariants import EXTRA_DECODE
+
+pytestmark = pytest.mark.gpu
+
+CL = "attn_decode_cluster"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from biased_gqa_attention_gb300 import build
+    build.build()
+
+
+SHAPES = [
+    # C2's structure, small: group of 2, window, ragged nonpad
+    wl.small(wl.C2),
+    # units whose live tiles are fewer than the cluster's CTAs (nonpad 1-40:
+    # at most 3 tiles for 8 CTAs, so some CTAs have no tile at all)
+    wl.Workload("cl_short", 401, B=6, Hq=8, Hkv=4, D=256, S_q=1, max_seq=256, dtype=torch.bfloat16,
+                causal=True, window=0, nonpad_range=(1, 40)),
+    # head size 128, group of 8 (8 rows per unit), a long window
+    wl.Workload("cl_d128_g8", 402, B=3, Hq=16, Hkv=2, D=128, S_q=1, max_seq=2048, dtype=torch.bfloat16,
+                causal=True, window=1500, nonpad_range=(600, 2048)),
+    # head size 512 with key spans at one position
+    wl.Workload("cl_d512_spans", 403, B=2, Hq=8, Hkv=2, D=512, S_q=1, max_seq=1536, dtype=torch.bfloat16,
+                causal=True, window=64, nonpad_fixed=1400, n_spans=2, span_len=48,
+                span_start_range=(900, 1300)),
+    # two query positions per head (4 heads x 2 positions = 8 rows), head size 64
+    wl.Workload("cl_d64_sq2", 404, B=4, Hq=8, Hkv=2, D=64, S_q=2, max_seq=4096, dtype=torch.bfloat16,
+                causal=True, window=700, nonpad_range=(2, 4096)),
+] + EXTRA_DECODE
+
+
+@pytest.mark.parametrize("mode", ["bias", "fused", "none"])
+@pytest.mark.parametrize("w", SHAPES, ids=lambda w: w.name)
+def test_cluster_decode_matches_the_oracle(w, mode):
+    inp = wl.make_inputs(w, "cuda")
+    g = run_gpu(inp, mode=mode, algo=ek.ALGO_DECODE_CLUSTER)
+    assert g["kernel"] == CL
+    o = oracle_path(inp, mode=mode)
+    assert max_err(g["y"], o["y"]) <= TOL[w.dtype]
+
+
+@pytest.mark.parametrize("mode", ["bias", "fused"])
+@pytest.mark.parametrize("w", [wl.C2, wl.C4], ids=lambda w: w.name)
+def test_cluster_decode_full_size_sampled_rows(w, mode):
+    inp = wl.make_inputs(w, "cuda")
+    g = run_gpu(inp, mode=mode, algo=ek.ALGO_DECODE_CLUSTER)
+    assert g["kernel"] == CL
+    rows = sample_rows(w, 48)
+    o = oracle_path(inp, rows=rows, mode=mode)
+    assert max_err(g["y"], o["y"], rows=rows) <= TOL[w.dtype]
+
+
+def test_the_decode_workload_runs_on_the_cluster_kernel():
+    inp = wl.make_inputs(wl.C2, "cuda")
+    for mode in ("bias", "fused"):
+        assert run_gpu(inp, mode=mode)["kernel"] == CL
+
+
+@pytest.mark.parametrize("mode", ["bias", "fused"])
+def test_cluster_decode_is_repeatable_bit_for_bit(mode):
+    inp = wl.make_inputs(wl.small(wl.C2), "cuda")
+    a = run_gpu(inp, mode=mode, algo=ek.ALGO_DECODE_CLUSTER)
+    b = run_gpu(inp, mode=mode, algo=ek.ALGO_DECODE_CLUSTER)
+    assert torch.equal(a["y"].view(torch.int16), b["y"].view(torch.int16))
+
+
+@pytest.mark.parametrize("mode", ["bias", "fused"])
+def test_cluster_decode_agrees_with_stream_k(mode):
+    inp = wl.make_inputs(wl.small(wl.C4), "cuda")
+    a = run_gpu(inp, mode=mode, algo=ek.ALGO_DECODE_CLUSTER)
+    b = run_gpu(inp, mode=mode, algo=ek.ALGO_DECODE_STREAMK)
+    assert a["kernel"] == CL and b["kernel"] == "attn_decode_streamk_mma"
+    assert (a["y"].float() - b["y"].float()).abs().max().item() <= TOL[torch.bfloat16]
+
+
+def test_cluster_decode_poison_beyond_nonpad_is_invisible():
+    w = wl.small(wl.C2).replace(name="cl_poison")
+    clean = wl.make_inputs(w, "cuda")
+    poisoned = wl.make_inputs(w, "cuda", poison=True)
+    for mode in ("bias", "fused", "none"):
+        a = run_gpu(clean, mode=mode, algo=ek.ALGO_DECODE_CLUSTER)
+        b = run_gpu(poisoned, mode=mode, algo=ek.ALGO_DECODE_CLUSTER)
+        assert torch.equal(a["y"].view(torch.int16), b["y"].view(torch.int16))
+
+
+def test_cluster_decode_empty_batches_are_zero_rows():
+    w = wl.small(wl.C2).replace(name="cl_empty")
+    inp = wl.make_inputs(w, "cuda")
+    inp.nonpad[1] = 0
+    inp.write_idx[1] = 0
+    for mode in ("bias", "fused", "none"):
+        g = run_gpu(inp, mode=mode, algo=ek.ALGO_DECODE_CLUSTER, scatter=False)
+        o = oracle_path(inp, mode=mode, scatter=False)
+        assert (g["y"][1] == 0).all()
+        assert max_err(g["y"], o["y"]) <= TOL[w.dtype]
+
+
+@pytest.mark.parametrize("w,mode", [
+    (wl.DECODE_G16, "bias"),                                          # 16 rows per KV head
+    (wl.small(wl.C2).replace(name="cl_long", max_seq=8200, nonpad_range=(1, 8200)), "bias"),  # scan > 16 KB
+    (wl.Workload("cl_sq2_spans", 405, B=2, Hq=4, Hkv=2, D=128, S_q=2, max_seq=512, dtype=torch.bfloat16,
+                 causal=True, window=50, nonpad_fixed=500, n_spans=1, span_len=40,
+                 span_start_range=(300, 300)), "fused"),              # spans at two positions
+], ids=["g16", "long_bias", "sq2_spans"])
+def test_the_cluster_kernel_refuses_the_shape(w, mode):
+    inp = wl.make_inputs(w, "cuda")
+    with pytest.raises(ek.ExtKVError) as e:
+        run_gpu(inp, mode=mode, algo=ek.ALGO_DECODE_CLUSTER)
+    assert e.value.code == ek.EXTKV_ERR_UNSUPPORTED
+    # the automatic choice still runs the shape, on another kernel
+    g = run_gpu(inp, mode=mode)
+    assert g["kernel"] != CL
+
+
+def test_cluster_decode_two_head_sizes_are_refused():
+    w = wl.Workload("cl_dk128_dv256", 406, B=2, Hq=8, Hkv=4, D=128, Dv=256, S_q=1, max_seq=512,
+                    dtype=torch.bfloat16, causal=True, window=100, nonpad_range=(1, 512))
+    inp = wl.make_inputs(w, "cuda")
+    with pytest.raises(ek.ExtKVError) as e:
+        run_gpu(inp, mode="bias", algo=ek.ALGO_DECODE_CLUSTER, scatter=False)
+    assert e.value.code == ek.EXTKV_ERR_UNSUPPORTED

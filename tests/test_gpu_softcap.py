@@ -43,8 +43,8 @@ def _run(inp, mode, cap, algo=ek.ALGO_AUTO, k=None, v=None):
 
 
 CASES = [
-    (EXTRA_DECODE[0], "attn_decode_streamk_mma"), (EXTRA_DECODE[3], "attn_decode_streamk_mma"),
-    (wl.small(wl.C2), "attn_decode_streamk_mma"), (wl.small(wl.C4), "attn_decode_streamk_mma"),
+    (EXTRA_DECODE[0], "attn_decode"), (EXTRA_DECODE[3], "attn_decode"),
+    (wl.small(wl.C2), "attn_decode"), (wl.small(wl.C4), "attn_decode"),
     (wl.small(wl.C3), "attn_prefill_tcgen05"), (wl.small(wl.C5), "attn_prefill_tcgen05"),
     (EXTRA_PREFILL[0], "attn_prefill_tcgen05"), (EXTRA_PREFILL[2], "attn_prefill_tcgen05"),
     (wl.C1_PREFILL, "attn_generic_f32"), (wl.C1_DECODE, "attn_generic_f32"),
@@ -90,3 +90,16 @@ def test_invalid_softcap_is_rejected():
         with pytest.raises(ek.ExtKVError) as e:
             ek.attention_ext_kv(y, inp.q, inp.k_cache, inp.v_cache, inp.nonpad, w.scale, softcap=bad)
         assert e.value.code == ek.EXTKV_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("algo,kernel", [(ek.ALGO_DECODE_STREAMK, "attn_decode_streamk_mma"),
+                                         (ek.ALGO_DECODE_CLUSTER, "attn_decode_cluster")],
+                         ids=["streamk", "cluster"])
+@pytest.mark.parametrize("mode", ["bias", "fused"])
+@pytest.mark.parametrize("w", [EXTRA_DECODE[0], EXTRA_DECODE[3], wl.small(wl.C2)], ids=lambda w: w.name)
+def test_softcap_on_each_decode_kernel(w, mode, algo, kernel):
+    inp = wl.make_inputs(w, "cuda")
+    y, ran = _run(inp, mode, 5.0, algo=algo)
+    assert ran == kernel
+    o = oracle_path(inp, mode=mode, scatter=False, softcap=5.0)
+    assert max_err(y, o["y"]) <= TOL[w.dtype]

@@ -18,13 +18,15 @@ from biased_gqa_attention_gb300 import extkv as ek
 from biased_gqa_attention_gb300 import workloads as wl
 from gpu_path import TOL, max_err, oracle_path, run_gpu, spec_of
 
-# two decode shapes, two single-SM prefill shapes (with key splits) and the
+# two decode shapes on each decode kernel, two single-SM prefill shapes (with key splits) and the
 # prefill on CTA pairs, on a shape large enough for the prefill on CTA pairs (head size 256, group of 2)
 PAIR_SHAPE = wl.Workload("timeout_pair", 322, B=2, Hq=8, Hkv=4, D=256, S_q=700, max_seq=2048,
                          dtype=torch.bfloat16, causal=True, window=500, nonpad_fixed=1900)
 CASES = [
-    (ek.ALGO_DECODE, wl.small(wl.C2), "bias"),
-    (ek.ALGO_DECODE, wl.small(wl.C4), "fused"),
+    (ek.ALGO_DECODE_STREAMK, wl.small(wl.C2), "bias"),
+    (ek.ALGO_DECODE_STREAMK, wl.small(wl.C4), "fused"),
+    (ek.ALGO_DECODE_CLUSTER, wl.small(wl.C2), "bias"),
+    (ek.ALGO_DECODE_CLUSTER, wl.small(wl.C4), "fused"),
     (ek.ALGO_PREFILL, wl.small(wl.C5), "bias"),
     (ek.ALGO_PREFILL, wl.small(wl.C3), "fused"),
     (ek.ALGO_PREFILL_PAIR, PAIR_SHAPE, "bias"),
@@ -44,7 +46,7 @@ def test_waits_that_run_out_are_reported_and_the_next_call_is_exact(algo, w, mod
     with ek.use_algo(algo), ek.wait_polls(0):
         ek.attention_ext_kv(y_bad, inp.q, ref["k"], ref["v"], inp.nonpad, w.scale, bias=bias, fused=fused,
                             status=st)
-        assert ek.extkv_last_kernel().startswith("attn_decode" if algo == ek.ALGO_DECODE else "attn_prefill")
+        assert ek.extkv_last_kernel().startswith("attn_decode" if algo in (ek.ALGO_DECODE_STREAMK, ek.ALGO_DECODE_CLUSTER) else "attn_prefill")
     assert ek.extkv_read_status(st) == ek.EXTKV_ERR_DEVICE
     assert "timed out" in ek.extkv_last_error()
     flags = int(st[0].item())
