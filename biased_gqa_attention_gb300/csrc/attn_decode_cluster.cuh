@@ -40,21 +40,60 @@ constexpr int kMaxCluster = 8;                  // portable cluster size
 constexpr int kScanBytes = 16 * 1024;           // bias rows one CTA scans (S_q * max_seq * 2)
 constexpr int kMaxListTiles = kScanBytes / 32;  // live-tile list of one unit
 
+// Stages of a cluster decode CTA's ring: as many as keep four CTAs on an SM
+// (a unit's eight CTAs of the decode workload's 64 units resident at once).
+template <int D>
+struct ClusterCfg;
+template <>
+struct ClusterCfg<64> {
+  static constexpr int SPW = 4;
+};
+template <>
+struct ClusterCfg<128> {
+  static constexpr int SPW = 4;
+};
+template <>
+struct ClusterCfg<256> {
+  static constexpr int SPW = 3;
+};
+template <>
+struct ClusterCfg<512> {
+  static constexpr int SPW = 2;
+};
+
 // Shared memory of a cluster decode CTA.  The stage ring doubles as the
-// buffer of the bias rows, which are scanned before the first K/V request.
+// buffer of the bias rows, which are scanned before the first K/V request,
+// and, once every copy into it has landed, as the share's unnormalised O.
 template <int DK, int DV, int SPW>
 struct CSmem {
   using S = Smem<DK, DV, SPW>;
   static constexpr int kStages = SPW * S::kStageBytes;
   static_assert(kStages >= kScanBytes, "the stage ring holds the scanned bias rows");
+  static_assert(kStages >= kRows * DV * 4, "the stage ring holds the share's O");
   static constexpr int kQ = kStages;                               // Q slot (DK = 512)
   static constexpr int kTerm = kQ + (S::kQReg ? 0 : S::kQBytes);   // per stage: S_q rows x 16 keys
-  static constexpr int kPart = kTerm + SPW * 256;                  // fp32 max[8], sum[8], O[8][DV]
-  static constexpr int kList = kPart + (2 * kRows + kRows * DV) * 4;  // uint16 live tiles
+  static constexpr int kPart = kTerm + SPW * 256;                  // fp32 max[8], sum[8]
+  static constexpr int kList = kPart + 2 * kRows * 4;              // uint16 live tiles
   static constexpr int kBars = kList + kMaxListTiles * 2;          // SPW stages, Q, scan
   static constexpr int kEnd = kBars + (SPW + 2) * 8;
   static constexpr size_t bytes() { return 1024 + kEnd; }
 };
+
+// Whether any of 8 bf16 values is above lowest(bf16), i.e. unmasked.
+__device__ __forceinline__ bool any_above_lowest(const uint4 v) {
+  const __nv_bfloat162 lo2 = __halves2bfloat162(__ushort_as_bfloat16(Elem<__nv_bfloat16>::kLowestBits),
+                                                  __ushort_as_bfloat16(Elem<__nv_bfloat16>::kLowestBits));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t r = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 x;
+    *reinterpret_cast<uint32_t*>(&x) = w[i];
+    const __nv_bfloat162 c = __hgt2(x, lo2);  // 1.0 where x > lowest
+    r |= *reinterpret_cast<const uint32_t*>(&c);
+  }
+  return r != 0;
+}
 
 template <int DK, int DV, int SPW, int MODE, bool CAP>
 __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
@@ -74,7 +113,7 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
   uint64_t* sbar = bars + SPW + 1;
   float* pm = reinterpret_cast<float*>(smem + L::kPart);  // max of each row
   float* pl = pm + kRows;                                  // sum of each row
-  float* po = pm + 2 * kRows;                              // unnormalised O [kRows][DV]
+  float* po = reinterpret_cast<float*>(smem);              // unnormalised O [kRows][DV], over the ring
   uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
   const int lane = threadIdx.x;
   const int rank = static_cast<int>(ptx::cluster_ctarank());
@@ -144,7 +183,7 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
     runs = batch_runs<MODE>(p, b, np64);
     n_live = runs.count();
   } else {
-    if (__any_sync(0xffffffffu, !ptx::mbar_wait_bounded(sbar, 0, p.polls))) {
+    if (__any_sync(0xffffffffu, !ptx::mbar_wait_spin_bounded(sbar, 0, p.polls))) {
       failed = true;
     } else {
       for (int t0 = 0; t0 < n_range; t0 += 32) {
@@ -154,15 +193,22 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
           const int j0 = t * kTile;
           for (int i = 0; i < p.S_q && !live; ++i) {
             const uint16_t* row = reinterpret_cast<const uint16_t*>(smem + static_cast<size_t>(i) * max_seq * 2);
+            if (j0 + kTile <= np) {
+              // a whole tile below nonpad: 8 packed comparisons (NaN compares false)
+              const uint4 v0 = *reinterpret_cast<const uint4*>(row + j0);
+              const uint4 v1 = *reinterpret_cast<const uint4*>(row + j0 + 8);
+              live = any_above_lowest(v0) || any_above_lowest(v1);
+            } else {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              if (j0 + 8 * h >= np) break;
-              const uint4 v = *reinterpret_cast<const uint4*>(row + j0 + 8 * h);
-              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+              for (int h = 0; h < 2; ++h) {
+                if (j0 + 8 * h >= np) break;
+                const uint4 v = *reinterpret_cast<const uint4*>(row + j0 + 8 * h);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const uint16_t bits = static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
-                live = live || (j0 + 8 * h + e < np && bf16_bits_to_float(bits) > lowest);
+                for (int e = 0; e < 8; ++e) {
+                  const uint16_t bits = static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
+                  live = live || (j0 + 8 * h + e < np && bf16_bits_to_float(bits) > lowest);
+                }
               }
             }
           }
@@ -245,14 +291,14 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
   int done = 0;  // items consumed
   for (int k = 0; k < n && !failed; ++k) {
     if (!q_ready) {
-      if (__any_sync(0xffffffffu, !ptx::mbar_wait_bounded(qbar, 0, p.polls))) {
+      if (__any_sync(0xffffffffu, !ptx::mbar_wait_spin_bounded(qbar, 0, p.polls))) {
         failed = true;
         break;
       }
       q_ready = true;
     }
     const int st = k % SPW;
-    if (__any_sync(0xffffffffu, !ptx::mbar_wait_bounded(&bars[st], (k / SPW) & 1, p.polls))) {
+    if (__any_sync(0xffffffffu, !ptx::mbar_wait_spin_bounded(&bars[st], (k / SPW) & 1, p.polls))) {
       failed = true;
       break;
     }
@@ -435,22 +481,26 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
   }
 
   // ---- this CTA's share: (max, sum, unnormalised O) into its shared memory ----
+  // O goes over the ring, whose copies have all landed (a failed share, whose
+  // copies may not have, writes no O: its max of -inf keeps it out of the combine)
   l0 += __shfl_xor_sync(0xffffffffu, l0, 4);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 8);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 16);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 4);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 8);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 16);
+  if (!failed) {
 #pragma unroll
-  for (int mt = 0; mt < DV / 16; ++mt) {
-    const int d = mt * 16 + (lane >> 2);
-    if (ok0) {
-      po[r0 * DV + d] = o[mt][0];
-      po[r0 * DV + d + 8] = o[mt][2];
-    }
-    if (ok1) {
-      po[r1 * DV + d] = o[mt][1];
-      po[r1 * DV + d + 8] = o[mt][3];
+    for (int mt = 0; mt < DV / 16; ++mt) {
+      const int d = mt * 16 + (lane >> 2);
+      if (ok0) {
+        po[r0 * DV + d] = o[mt][0];
+        po[r0 * DV + d + 8] = o[mt][2];
+      }
+      if (ok1) {
+        po[r1 * DV + d] = o[mt][1];
+        po[r1 * DV + d + 8] = o[mt][3];
+      }
     }
   }
   if (lane < 4) {
@@ -542,7 +592,7 @@ inline int cluster_capacity(const void* kern, size_t smem, int C) {
 // the GPU at once; 0: not even single CTAs do.
 template <int DK, int DV>
 int cluster_size_for(int64_t units) {
-  constexpr int SPW = PairCfg<DK, DV>::SPW;
+  constexpr int SPW = ClusterCfg<DK>::SPW;
   const void* kern = reinterpret_cast<const void*>(attn_decode_cluster_kernel<DK, DV, SPW, kBias, false>);
   const size_t smem = CSmem<DK, DV, SPW>::bytes();
   for (int C = kMaxCluster; C >= 1; C >>= 1) {
@@ -555,7 +605,7 @@ int cluster_size_for(int64_t units) {
 template <int DK, int DV, int MODE, bool CAP>
 cudaError_t launch_dcl(const AttnArgs& a, const DecodeParams& prm, const CUtensorMap& kmap,
                        const CUtensorMap& vmap, const CUtensorMap& qmap, const CUtensorMap& tmap, int C) {
-  constexpr int SPW = PairCfg<DK, DV>::SPW;
+  constexpr int SPW = ClusterCfg<DK>::SPW;
   const size_t smem = CSmem<DK, DV, SPW>::bytes();
   auto kern = attn_decode_cluster_kernel<DK, DV, SPW, MODE, CAP>;
   cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), smem);

@@ -70,6 +70,22 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// Bounded wait that polls without suspending for its first kSpinPolls polls
+// (a suspended try_wait wakes some hundreds of nanoseconds after the phase
+// completes; a test_wait poll sees it within a few cycles), then suspends as
+// mbar_wait_bounded does.  `limit` counts every poll of either kind.  For a
+// warp that has its SM sub-partition to itself, where spinning takes issue
+// slots from no one.
+__device__ __forceinline__ bool mbar_wait_spin_bounded(uint64_t* bar, uint32_t parity, uint32_t limit) {
+  constexpr uint32_t kSpinPolls = 4096;
+  uint32_t i = 0;
+  for (; i < limit && i < kSpinPolls; ++i)
+    if (mbar_test_wait(bar, parity)) return true;
+  for (; i < limit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
 // ---- TMA ----------------------------------------------------------------------
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,

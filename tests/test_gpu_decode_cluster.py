@@ -15,9 +15,11 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from biased_gqa_attention_gb300 import extkv as ek
 from biased_gqa_attention_gb300 import workloads as wl
 from gpu_path import TOL, max_err, oracle_path, run_gpu, sample_rows, spec_of
+from helpers import from_raw, raw
 from test_gpu_invariants import EXTRA_DECODE
 
 pytestmark = pytest.mark.gpu
@@ -141,3 +143,35 @@ def test_cluster_decode_two_head_sizes_are_refused():
     with pytest.raises(ek.ExtKVError) as e:
         run_gpu(inp, mode="bias", algo=ek.ALGO_DECODE_CLUSTER, scatter=False)
     assert e.value.code == ek.EXTKV_ERR_UNSUPPORTED
+
+
+def test_cluster_scan_reads_special_bias_values():
+    """The live-tile scan against section 6's rule (a key is unmasked iff it is
+    below nonpad and its bias is above lowest(T); NaN is not above it): a value
+    just above lowest, NaN, -inf and lowest side by side, the only unmasked
+    key in a partial last tile, a zero bias beyond nonpad, an empty batch."""
+    w = wl.Workload("cl_scan", 407, B=4, Hq=8, Hkv=4, D=128, S_q=1, max_seq=512, dtype=torch.bfloat16,
+                    causal=False, window=0, nonpad_fixed=512)
+    inp = wl.make_inputs(w, "cuda")
+    nonpad = np.array([100, 37, 512, 0], np.int64)
+    inp.nonpad = torch.tensor(nonpad, device="cuda")
+    low, neg_inf, nan, one, minus_one = 0xFF7F, 0xFF80, 0x7FC0, 0x3F80, 0xBF80
+    bias = np.full((4, 1, 1, 512), low, np.uint16)
+    bias[0, 0, 0, 5] = 0xFF7E          # the value next above lowest: unmasked
+    bias[0, 0, 0, 50] = nan            # masked
+    bias[0, 0, 0, 99] = 0              # unmasked, the last key below nonpad
+    bias[1, 0, 0, 36] = one            # the only unmasked key, in the partial last tile
+    bias[1, 0, 0, 40] = 0              # beyond nonpad: masked whatever its bias
+    bias[2, 0, 0, ::2] = neg_inf
+    bias[2, 0, 0, 400:416] = nan       # a whole tile of NaN
+    bias[2, 0, 0, 300] = minus_one     # the only unmasked key of the batch
+    y = torch.full_like(inp.q, float("nan"))
+    st = ek.new_status()
+    with ek.use_algo(ek.ALGO_DECODE_CLUSTER):
+        ek.attention_ext_kv(y, inp.q, inp.k_cache, inp.v_cache, inp.nonpad, w.scale,
+                            bias=from_raw(bias, w.dtype).cuda(), status=st)
+        assert ek.extkv_last_kernel() == CL
+    assert ek.extkv_read_status(st) == ek.EXTKV_OK, ek.extkv_last_error()
+    ref = oracle.attention(raw(inp.q), raw(inp.k_cache), raw(inp.v_cache), bias, nonpad, np.float32(w.scale))
+    assert (y[3] == 0).all()
+    assert max_err(y, ref) <= TOL[w.dtype]

@@ -7,8 +7,9 @@ by log2(e) before the row maximum is subtracted overflows fp32 (|b| above
 about 2.36e38) and turns it into a mask.  These tests give whole rows only
 huge finite biases in (lowest, -2.4e38), and single keys +3e38, through a
 materialised bias and through the fused specification's extra term, on the
-decode kernel, the tcgen05 prefill kernel (with and without key splits) and
-the generic kernel, and compare each element with the oracle.
+decode kernels (stream-K and cluster), the tcgen05 prefill kernel (with and
+without key splits) and the generic kernel, and compare each element with the
+oracle.
 """
 import numpy as np
 import pytest
@@ -105,11 +106,13 @@ PREFILL_WIDE = wl.Workload("extreme_prefill_wide", 304, B=4, Hq=16, Hkv=8, D=256
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("algo,name", [(ek.ALGO_DECODE_STREAMK, "attn_decode_streamk_mma"),
+                                       (ek.ALGO_DECODE_CLUSTER, "attn_decode_cluster")], ids=["streamk", "cluster"])
 @pytest.mark.parametrize("mode", ["bias", "fused"])
 @pytest.mark.parametrize("w", [DECODE, DECODE_G], ids=lambda w: w.name)
-def test_decode_kernel_extreme_biases(w, mode):
-    y, ref, kernel = _run(w, ek.ALGO_DECODE, mode, seed=11)
-    assert kernel.startswith("attn_decode"), kernel
+def test_decode_kernel_extreme_biases(w, mode, algo, name):
+    y, ref, kernel = _run(w, algo, mode, seed=11)
+    assert kernel == name, kernel
     assert max_err(y, ref) <= TOL[w.dtype]
 
 
