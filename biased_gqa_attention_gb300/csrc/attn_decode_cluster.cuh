@@ -517,30 +517,34 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
   const int g4 = cpc / 4;
   for (int it = lane; it < R * g4; it += 32) {
     const int row = it / g4, col = rank * cpc + (it - row * g4) * 4;
+    // every share's (max, sum, O columns) in one round of remote loads
     float mj[kMaxCluster], lj[kMaxCluster];
-    float M = -INFINITY;
+    float4 ov[kMaxCluster];
 #pragma unroll
     for (int j = 0; j < kMaxCluster; ++j) {
-      mj[j] = -INFINITY;
-      lj[j] = 0.f;
       if (j < C) {
         mj[j] = ptx::ld_cluster_f32(ptx::map_cluster(pm + row, j));
         lj[j] = ptx::ld_cluster_f32(ptx::map_cluster(pl + row, j));
-        M = fmaxf(M, mj[j]);
+        ov[j] = ptx::ld_cluster_f32x4(ptx::map_cluster(po + row * DV + col, j));
       }
     }
+    float M = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kMaxCluster; ++j)
+      if (j < C) M = fmaxf(M, mj[j]);
     float Lsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < kMaxCluster; ++j) {
-      if (j >= C || mj[j] == -INFINITY) continue;  // a share without an unmasked key adds nothing
+      // a share without an unmasked key (max -inf) adds nothing; its O may not
+      // have been written, so it is left out by selection, not by a zero weight
+      if (j >= C || mj[j] == -INFINITY) continue;
       const float wj = ptx::ex2((mj[j] - M) * kLog2e);
-      const float4 v = ptx::ld_cluster_f32x4(ptx::map_cluster(po + row * DV + col, j));
       Lsum = fmaf(wj, lj[j], Lsum);
-      acc.x = fmaf(v.x, wj, acc.x);
-      acc.y = fmaf(v.y, wj, acc.y);
-      acc.z = fmaf(v.z, wj, acc.z);
-      acc.w = fmaf(v.w, wj, acc.w);
+      acc.x = fmaf(ov[j].x, wj, acc.x);
+      acc.y = fmaf(ov[j].y, wj, acc.y);
+      acc.z = fmaf(ov[j].z, wj, acc.z);
+      acc.w = fmaf(ov[j].w, wj, acc.w);
     }
     const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;  // no unmasked key: zero row
     const uint32_t lo2 = ptx::pack_bf16x2(acc.x * inv, acc.y * inv);
