@@ -351,8 +351,9 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const __nv_b
 // The same table for a materialised bias: each block stages the 128 x 128
 // bias block of one key tile in shared memory (32 KB, so seven blocks fit an
 // SM and a whole query tile's row of blocks is in flight at once) with one
-// bulk copy per row, all in flight together, then thread (g, k) ORs rows
-// g, g + 16, ... of keys 8k .. 8k + 7.  It also writes, per query row and
+// tiled TMA copy (one request: with a copy per row, the 128 requests of each
+// of an SM's seven blocks queued behind one another), then thread (g, k) ORs
+// rows g, g + 16, ... of keys 8k .. 8k + 7.  It also writes, per query row and
 // 128-key tile, the bits of the keys the row may attend (rowmask: 16 bytes
 // per row and tile, rm_stride bytes per row), and per (query tile, 128-key
 // tile) whether the bias holds a value other than 0 and the sentinel inside
@@ -360,7 +361,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const __nv_b
 // the bits: adding a bias of 0 changes no score.
 constexpr int kPlanSmem = kBM * kBN * 2 + 64;
 
-__global__ void __launch_bounds__(kPlanThreads) prefill_plan_bias_kernel(const __nv_bfloat16* __restrict__ bias,
+__global__ void __launch_bounds__(kPlanThreads) prefill_plan_bias_kernel(const __grid_constant__ CUtensorMap bmap,
                                                                         const int64_t* __restrict__ nonpad,
                                                                         uint64_t* __restrict__ colmask, int S_q,
                                                                         int max_seq, int n_pt, int n_words,
@@ -375,6 +376,8 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_bias_kernel(const _
   __shared__ int impure_s;
   const int kt = blockIdx.x, pt = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, kc = tid % (kBN / 8), grp = tid / (kBN / 8);
+  if (tid == 0) ptx::prefetch_tensormap(&bmap);
+  ptx::grid_dependency_wait();    // the bias and nonpad as the preceding kernels left them
   ptx::grid_launch_dependents();  // the attention kernel may start its prologue
   const int64_t np64 = nonpad[b];
   const int np = bad_nonpad(np64, max_seq) ? 0 : static_cast<int>(np64);
@@ -393,15 +396,11 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_bias_kernel(const _
   uint8_t* rm = rowmask + (static_cast<int64_t>(b) * n_pt + pt) * kBM * rm_stride + kt * 16 + kc;
   uint32_t mrow[kBM / kGroups / 4] = {0, 0};  // this thread's byte of its 8 rows
   if (keys > 0) {
-    // whole 16-byte pieces: max_seq % 8 == 0 keeps the rounded row inside the tensor
-    const uint32_t row_bytes = static_cast<uint32_t>((keys + 7) / 8) * 16;
-    // one row copy per thread, issued side by side (a copy costs its issuing
-    // thread a fixed time, so one thread issuing all rows would serialise them)
-    if (tid == 0) ptx::mbar_arrive_expect_tx(bar, row_bytes * rows);
-    __syncthreads();
-    if (tid < rows) {
-      const __nv_bfloat16* src = bias + (static_cast<int64_t>(b) * S_q + q0 + tid) * max_seq + k_begin;
-      ptx::bulk_load(rows_s + tid * kBN, src, row_bytes, bar);
+    // the (rows x 128 keys) block as one box of the (B*S_q, max_seq) view:
+    // rows past S_q or keys past max_seq arrive as zeros and are not read
+    if (tid == 0) {
+      ptx::mbar_arrive_expect_tx(bar, kBM * kBN * 2);
+      ptx::tma_load_2d(rows_s, &bmap, bar, k_begin, b * S_q + q0);
     }
     const bool ok = ptx::mbar_wait_bounded(bar, 0, kWaitPolls);
     if (!ok && tid == 0) report(status, EXTKV_DEV_TIMEOUT);
@@ -1482,12 +1481,28 @@ cudaError_t prefill_setup(const AttnArgs& a, int mode, int dv_chunk, PrefillPara
     if (cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(prefill_plan_bias_kernel), kPlanSmem);
         e != cudaSuccess)
       return e;
-    prefill_plan_bias_kernel<<<dim3(prm.n_kt, prm.n_pt, prm.B), kPlanThreads, kPlanSmem,
-                               a.stream>>>(static_cast<const __nv_bfloat16*>(term), a.nonpad,
-                                           static_cast<uint64_t*>(a.workspace), prm.S_q, prm.max_seq,
-                                           prm.n_pt, prm.n_tiles, wsb + off_rowmask, prm.rm_stride,
-                                           wsb + off_impure, prm.n_kt, a.status);
-    cudaError_t e = cudaGetLastError();
+    // the bias as a (B*S_q rows, max_seq keys) view, boxes of 128 x 128
+    CUtensorMap bmap;
+    const uint64_t b_dims[2] = {static_cast<uint64_t>(a.max_seq), static_cast<uint64_t>(a.B * a.S_q)};
+    const uint64_t b_strides[1] = {static_cast<uint64_t>(a.max_seq) * 2};
+    const uint32_t b_box[2] = {kBN, kBM};
+    if (!make_tensor_map_bf16(&bmap, term, 2, b_dims, b_strides, b_box, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+    // a dependent launch: its blocks may be placed before the preceding kernel ends
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(prm.n_kt, prm.n_pt, prm.B);
+    cfg.blockDim = dim3(kPlanThreads);
+    cfg.dynamicSmemBytes = kPlanSmem;
+    cfg.stream = a.stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_plan_bias_kernel, bmap, a.nonpad,
+                                       static_cast<uint64_t*>(a.workspace), prm.S_q, prm.max_seq, prm.n_pt,
+                                       prm.n_tiles, wsb + off_rowmask, prm.rm_stride, wsb + off_impure,
+                                       prm.n_kt, a.status);
     if (e != cudaSuccess) return e;
   } else if (mode == kFusedExtra) {
     prefill_plan_kernel<true><<<dim3(n_plan_chunks(a.max_seq), prm.n_pt, prm.B), kPlanThreads, 0, a.stream>>>(
