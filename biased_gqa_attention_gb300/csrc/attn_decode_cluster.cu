@@ -8,8 +8,9 @@ int decode_cluster_size(const AttnArgs& a) {
   if (a.dtype != EXTKV_BF16 || a.Dv != a.D) return 0;
   if (a.D != 64 && a.D != 128 && a.D != 256 && a.D != 512) return 0;
   if (a.Hkv <= 0 || a.Hq % a.Hkv) return 0;
-  // one unit of at most 8 query rows per KV head
-  if ((a.Hq / a.Hkv) * a.S_q > kRows || a.S_q > kRows) return 0;
+  // units of at most 8 query rows, up to 8 per KV head; a stage's bias block
+  // holds the 16 keys of every query position (S_q <= 8)
+  if ((a.Hq / a.Hkv) * a.S_q > kRows * kMaxRowGroups || a.S_q > kRows) return 0;
   // the fused specification's live tiles in closed form (several positions
   // with spans need a per-tile test)
   if (a.fused && needs_plan(a)) return 0;
@@ -19,7 +20,7 @@ int decode_cluster_size(const AttnArgs& a) {
   if (a.bias && a.S_q * a.max_seq * 2 > kScanBytes) return 0;
   const int64_t max_tiles = (a.max_seq + kTile - 1) / kTile;
   if (max_tiles > 65535 || a.B * a.Hq * a.S_q > 0x7fffffff) return 0;
-  const int64_t units = a.B * a.Hkv;
+  const int64_t units = a.B * a.Hkv * row_groups((a.Hq / a.Hkv) * a.S_q);
   if (units <= 0 || units > (1 << 20)) return 0;
   switch (a.D) {
     case 64: return cluster_size_for<64, 64>(units);

@@ -9,9 +9,11 @@
 // When every unit can hold C CTAs resident at once, this kernel removes all
 // three:
 //
-//   Unit: one (batch b, KV head) with its R = (Hq/Hkv) * S_q <= 8 query rows
-//     (GQA by reshaping Q, "ONNX Domain Attention (Opset 23/24) CUDA
-//     Patterns", section 1).  A cluster of C one-warp CTAs (C <= 8) per unit.
+//   Unit: one (batch b, KV head, row group): up to 8 of the KV head's
+//     GR = (Hq/Hkv) * S_q <= 64 query rows (GQA by reshaping Q, "ONNX Domain
+//     Attention (Opset 23/24) CUDA Patterns", section 1); the row groups of a
+//     KV head read the same tiles.  A cluster of C one-warp CTAs (C <= 8) per
+//     unit.
 //   Live tiles: every CTA of the unit finds the unit's live 16-key tiles by
 //     itself -- without a bias, the tiles below nonpad; with the fused
 //     specification, the closed-form runs of the rows' allowed intervals;
@@ -118,8 +120,8 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
   const int lane = threadIdx.x;
   const int rank = static_cast<int>(ptx::cluster_ctarank());
   const int unit = static_cast<int>(blockIdx.x) / C;
-  const int b = unit / p.Hkv, kvh = unit - b * p.Hkv;
-  const int bh = unit;  // the K/V views' unit coordinate (b * Hkv + kvh)
+  const int bh = unit / p.n_rg, rg = unit - bh * p.n_rg;  // bh: the K/V views' unit coordinate
+  const int b = bh / p.Hkv, kvh = bh - b * p.Hkv;
   const float lowest = Elem<__nv_bfloat16>::lowest();
   const int max_seq = p.max_seq;
 
@@ -145,16 +147,19 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
   }
   const int64_t np64 = p.nonpad[b];
   const bool bad = bad_nonpad(np64, max_seq);
-  if (bad && kvh == 0 && rank == 0 && lane == 0) report(p.status, EXTKV_DEV_BAD_NONPAD);
+  if (bad && kvh == 0 && rg == 0 && rank == 0 && lane == 0) report(p.status, EXTKV_DEV_BAD_NONPAD);
   const int np = bad ? 0 : static_cast<int>(np64);
   const int n_range = (np + kTile - 1) / kTile;
 
-  // this lane's two query rows of the unit, and the unit's first row of Y
-  const int R = p.GR;
-  const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + static_cast<int64_t>(kvh) * p.g) * p.S_q;
+  // this lane's two query rows of the unit (row r of group rg is the KV head's
+  // row 8 rg + r: head (8 rg + r) / S_q of the group, position (8 rg + r) % S_q),
+  // and the unit's first row of Y
+  const int R = min(kRows, p.GR - rg * kRows);
+  const int64_t row0 =
+      (static_cast<int64_t>(b) * p.Hq + static_cast<int64_t>(kvh) * p.g) * p.S_q + rg * kRows;
   const int r0 = 2 * (lane & 3), r1 = r0 + 1;
   const bool ok0 = r0 < R, ok1 = r1 < R;
-  const int i0 = r0 % p.S_q, i1 = r1 % p.S_q;
+  const int i0 = (rg * kRows + r0) % p.S_q, i1 = (rg * kRows + r1) % p.S_q;
 
   // Q: mma B fragments in registers (DK <= 256), else one TMA box in shared memory
   uint32_t qf[kQReg ? kKSteps : 1][2];
@@ -249,18 +254,19 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
   };
   if (!failed) fill(0);
 
-  // The fused scatter: the unit's new rows, split over the cluster's CTAs.
-  // Loads of this unit's other CTAs may see a row before or after it is
-  // written; a tile that holds new rows is patched from k_new / v_new below.
+  // The fused scatter: the KV head's new rows, split over the CTAs of its
+  // first row group's cluster.  Loads of the KV head's other CTAs may see a
+  // row before or after it is written; a tile that holds new rows is patched
+  // from k_new / v_new below.
   int w_new = -1;  // first new slot of the batch, -1: none or out of range (skipped)
   if (kOneSize && p.k_new) {
     const int64_t w = p.write_idx[b];
     if (w < 0 || w + p.S_new > max_seq) {
-      if (kvh == 0 && rank == 0 && lane == 0) report(p.status, EXTKV_DEV_BAD_WRITE_IDX);
+      if (kvh == 0 && rg == 0 && rank == 0 && lane == 0) report(p.status, EXTKV_DEV_BAD_WRITE_IDX);
     } else {
       w_new = static_cast<int>(w);
       constexpr int vpr = DK / 8;  // 16-byte vectors per row
-      for (int sn = rank; sn < p.S_new; sn += C)
+      for (int sn = rank; rg == 0 && sn < p.S_new; sn += C)
         for (int v = lane; v < vpr; v += 32) {
           const int64_t dst = (static_cast<int64_t>(bh) * max_seq + w + sn) * DK + v * 8;
           const int64_t src = (static_cast<int64_t>(bh) * p.S_new + sn) * DK + v * 8;
@@ -625,7 +631,7 @@ cudaError_t launch_dcl(const AttnArgs& a, const DecodeParams& prm, const CUtenso
   cfg.stream = a.stream;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.Hkv * C));
+  cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.Hkv * prm.n_rg * C));
   cfg.blockDim = dim3(32);
   cfg.dynamicSmemBytes = smem;
   e = cudaLaunchKernelEx(&cfg, kern, kmap, vmap, qmap, tmap, prm, C);
@@ -682,8 +688,8 @@ cudaError_t launch_dc(const AttnArgs& a, int C, const char** name) {
   prm.S_q = static_cast<int>(a.S_q);
   prm.g = static_cast<int>(a.Hq / a.Hkv);
   prm.GR = static_cast<int>(a.Hq / a.Hkv * a.S_q);
-  prm.n_rg = 1;
-  prm.R = prm.GR;
+  prm.n_rg = static_cast<int>(row_groups(prm.GR));
+  prm.R = std::min(prm.GR, kRows);
   prm.D = D;
   prm.max_seq = static_cast<int>(a.max_seq);
   prm.max_tiles = static_cast<int>(max_tiles);

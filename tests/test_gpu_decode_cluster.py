@@ -5,8 +5,9 @@ decode is memory-bandwidth bound; "ONNX Domain Attention (Opset 23/24) CUDA
 Patterns", section 1: the query heads of a KV group share its K/V rows).
 
 Checked against the oracle element by element with the kernel forced: every
-bias mode, head sizes 64-512, two query positions, units with fewer live
-tiles than CTAs, empty batches, poisoned slots; the decode
+bias mode, head sizes 64-512, two and three query positions, row groups (more
+than 8 query rows per KV head), units with fewer live tiles than CTAs, empty
+batches, poisoned slots; the decode
 workloads at full size on sampled rows; the automatic choice for the decode
 workload; bit-for-bit repeatability (the shares are combined in a fixed
 order); and the shapes the kernel refuses.
@@ -50,6 +51,12 @@ SHAPES = [
     # two query positions per head (4 heads x 2 positions = 8 rows), head size 64
     wl.Workload("cl_d64_sq2", 404, B=4, Hq=8, Hkv=2, D=64, S_q=2, max_seq=4096, dtype=torch.bfloat16,
                 causal=True, window=700, nonpad_range=(2, 4096)),
+    # 16 heads per KV head: two row groups, each a cluster of its own
+    wl.Workload("cl_g16", 409, B=3, Hq=32, Hkv=2, D=128, S_q=1, max_seq=1024, dtype=torch.bfloat16,
+                causal=True, window=300, nonpad_range=(1, 1024)),
+    # 6 heads x 3 positions = 18 rows: three groups, the last of 2 rows
+    wl.Workload("cl_g6_s3", 410, B=2, Hq=12, Hkv=2, D=256, S_q=3, max_seq=512, dtype=torch.bfloat16,
+                causal=True, window=100, nonpad_range=(3, 512)),
 ] + EXTRA_DECODE
 
 
@@ -120,12 +127,13 @@ def test_cluster_decode_empty_batches_are_zero_rows():
 
 
 @pytest.mark.parametrize("w,mode", [
-    (wl.DECODE_G16, "bias"),                                          # 16 rows per KV head
+    (wl.Workload("cl_g32_s4", 408, B=2, Hq=32, Hkv=1, D=64, S_q=4, max_seq=256, dtype=torch.bfloat16,
+                 causal=True, window=0, nonpad_range=(10, 256)), "bias"),  # 128 rows per KV head
     (wl.small(wl.C2).replace(name="cl_long", max_seq=8200, nonpad_range=(1, 8200)), "bias"),  # scan > 16 KB
     (wl.Workload("cl_sq2_spans", 405, B=2, Hq=4, Hkv=2, D=128, S_q=2, max_seq=512, dtype=torch.bfloat16,
                  causal=True, window=50, nonpad_fixed=500, n_spans=1, span_len=40,
                  span_start_range=(300, 300)), "fused"),              # spans at two positions
-], ids=["g16", "long_bias", "sq2_spans"])
+], ids=["g32_s4", "long_bias", "sq2_spans"])
 def test_the_cluster_kernel_refuses_the_shape(w, mode):
     inp = wl.make_inputs(w, "cuda")
     with pytest.raises(ek.ExtKVError) as e:
