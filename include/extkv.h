@@ -384,8 +384,8 @@ void extkv_step_free(extkv_step *step);
 #define EXTKV_ALGO_GENERIC 1 /* fp32 SIMT, one warp per query row: any supported shape */
 #define EXTKV_ALGO_DECODE 2  /* the decode kernels: bf16, S_q <= 8, S_q*Hq/Hkv <= 64, up to 1024
                                 batches, D in {64,128,256,512} (and pairs of 128, 256, 512); the
-                                cluster kernel where each KV head's rows (at most 8) can have 8
-                                CTAs resident at once, stream-K otherwise */
+                                cluster kernel where every group of up to 8 of a KV head's query
+                                rows can have 8 CTAs resident at once, stream-K otherwise */
 #define EXTKV_ALGO_PREFILL 3 /* tcgen05/TMEM prefill: bf16, head sizes 64/64 or any pair of 128, 256, 512;
                                 one CTA per query tile */
 #define EXTKV_ALGO_PREFILL_PAIR 4 /* the same prefill on CTA pairs with 2-SM MMAs (two query heads of a
@@ -398,12 +398,13 @@ void extkv_step_free(extkv_step *step);
                                        the decode kernel over equal slices of all live tiles, a
                                        merge kernel for units split across slices */
 #define EXTKV_ALGO_DECODE_CLUSTER 6 /* the cluster decode alone: one kernel, a cluster of up to 8
-                                       CTAs per (batch, KV head) sharing its live tiles, combined
-                                       through distributed shared memory.  bf16, one head size in
-                                       {64,128,256,512}, S_q*Hq/Hkv <= 8, all clusters resident
-                                       at once; a materialised bias with S_q*max_seq <= 8192 (one
-                                       copy of a batch's rows is scanned); with the fused spec, no
-                                       spans when S_q > 1 */
+                                       CTAs per (batch, KV head, group of up to 8 query rows)
+                                       sharing its live tiles, combined through distributed shared
+                                       memory.  bf16, one head size in {64,128,256,512}, S_q <= 8,
+                                       S_q*Hq/Hkv <= 64, all clusters resident at once; a
+                                       materialised bias with S_q*max_seq <= 8192 (one copy of a
+                                       batch's rows is scanned); with the fused spec, no spans
+                                       when S_q > 1 */
 int extkv_set_algo(int algo);
 
 #ifdef __cplusplus

@@ -73,10 +73,15 @@ def test_host_validation_rejects_bad_arguments(lib):
                                 extkv.EXTKV_BF16, None, 0, None, None) == extkv.EXTKV_OK
     assert lib.ext_kv_scatter(None, None, None, None, None, 2, 2, 0, 64, 64, extkv.EXTKV_BF16, None,
                               None) == extkv.EXTKV_OK
-    # algorithm selection
+    # algorithm selection: every value the header defines, nothing past the last
     assert lib.extkv_set_algo(99) == extkv.EXTKV_ERR_INVALID_ARG
+    assert lib.extkv_set_algo(extkv.ALGO_DECODE_CLUSTER + 1) == extkv.EXTKV_ERR_INVALID_ARG
+    assert lib.extkv_set_algo(-1) == extkv.EXTKV_ERR_INVALID_ARG
     prev = lib.extkv_set_algo(extkv.ALGO_GENERIC)
-    assert lib.extkv_set_algo(prev) == extkv.ALGO_GENERIC
+    for algo in (extkv.ALGO_DECODE, extkv.ALGO_PREFILL, extkv.ALGO_PREFILL_PAIR, extkv.ALGO_DECODE_STREAMK,
+                 extkv.ALGO_DECODE_CLUSTER, extkv.ALGO_AUTO):
+        lib.extkv_set_algo(algo)
+    assert lib.extkv_set_algo(prev) == extkv.ALGO_AUTO
 
 
 def test_workspace_size_is_queryable(lib):
