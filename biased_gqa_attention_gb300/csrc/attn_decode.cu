@@ -24,6 +24,26 @@ bool mixed_pair(int64_t Dk, int64_t Dv) {
   return Dk != Dv && in(Dk) && in(Dv);
 }
 
+// Whether the cluster kernel should take a call it can run with C CTAs per
+// unit.  Its time follows the unit with the most live tiles, shared by C
+// CTAs; stream-K's the average over its grid of G CTAs plus its fixed costs
+// (plan, tables, merge: about kClusterSlack tiles of one CTA's streaming).  A
+// unit's live tiles are bounded by max_seq, or, for the fused specification
+// with a causal window and no spans, by the window; a materialised bias
+// gives no bound without reading it.
+constexpr double kClusterSlack = 8.0;
+
+bool cluster_pays(const AttnArgs& a, int C) {
+  const int64_t max_tiles = (a.max_seq + kTile - 1) / kTile;
+  int64_t L = max_tiles;
+  if (a.fused && !a.spans && a.causal && a.window > 0)
+    L = std::min<int64_t>(max_tiles, (a.window + a.S_q - 1 + kTile - 1) / kTile + 1);
+  const int64_t units = a.B * a.Hkv * row_groups((a.Hq / a.Hkv) * a.S_q);
+  const DecodeShape d = shape_for(a.D, a.Dv, a.B, units * max_tiles);
+  const double excess = static_cast<double>(L) * (1.0 / C - static_cast<double>(units) / std::max(d.G, 1));
+  return excess <= kClusterSlack;
+}
+
 }  // namespace
 
 size_t decode_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t Dk,
@@ -57,16 +77,15 @@ bool decode_supported(const AttnArgs& a) {
 }
 
 cudaError_t launch_attn_decode(const AttnArgs& a, const char** name) {
-  // The cluster kernel where every unit gets the full 8 CTAs resident at once
-  // (no plan, tables or merge); stream-K otherwise.  The cluster kernel's time
-  // follows the unit with the most live tiles, stream-K's the average, so with
-  // fewer CTAs per unit (longer shares) stream-K's balance wins (measured: the
-  // global-layer decode, 64 units at head size 512 with 4 CTAs each, 141 us
-  // against 86 us).
-  constexpr int kClusterMin = 8;
+  // The cluster kernel (no plan, tables or merge) where its longest share is
+  // not much longer than stream-K's average one (cluster_pays); stream-K
+  // otherwise.  Measured: the decode workload (64 units, 8 CTAs each) 16.0 us
+  // against 21.7 us; one sequence of 8000 keys (8 units) 60.7 us against
+  // 24.5 us; the global-layer decode (64 units, 4 CTAs each at head size 512)
+  // 141 us against 86 us.
   if (a.decode_variant != kDecodeStreamK) {
     const int C = decode_cluster_size(a);
-    if (C > 0 && (a.decode_variant == kDecodeCluster || C >= kClusterMin))
+    if (C > 0 && (a.decode_variant == kDecodeCluster || cluster_pays(a, C)))
       return launch_attn_decode_cluster(a, C, name);
     if (a.decode_variant == kDecodeCluster) return cudaErrorInvalidValue;
   }
