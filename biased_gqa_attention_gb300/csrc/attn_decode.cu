@@ -32,16 +32,20 @@ bool mixed_pair(int64_t Dk, int64_t Dv) {
 // with a causal window and no spans, by the window; a materialised bias
 // gives no bound without reading it.
 constexpr double kClusterSlack = 8.0;
+// the merge kernel a split into M > 1 clusters per unit adds (its launch and
+// two dependent round trips), in the same units
+constexpr double kMergeTiles = 4.0;
 
-bool cluster_pays(const AttnArgs& a, int C) {
+bool cluster_pays(const AttnArgs& a, int C, int M) {
   const int64_t max_tiles = (a.max_seq + kTile - 1) / kTile;
   int64_t L = max_tiles;
   if (a.fused && !a.spans && a.causal && a.window > 0)
     L = std::min<int64_t>(max_tiles, (a.window + a.S_q - 1 + kTile - 1) / kTile + 1);
   const int64_t units = a.B * a.Hkv * row_groups((a.Hq / a.Hkv) * a.S_q);
   const DecodeShape d = shape_for(a.D, a.Dv, a.B, units * max_tiles);
-  const double excess = static_cast<double>(L) * (1.0 / C - static_cast<double>(units) / std::max(d.G, 1));
-  return excess <= kClusterSlack;
+  const double excess =
+      static_cast<double>(L) * (1.0 / (static_cast<double>(C) * M) - static_cast<double>(units) / std::max(d.G, 1));
+  return excess <= kClusterSlack - (M > 1 ? kMergeTiles : 0.0);
 }
 
 }  // namespace
@@ -85,8 +89,9 @@ cudaError_t launch_attn_decode(const AttnArgs& a, const char** name) {
   // 141 us against 86 us.
   if (a.decode_variant != kDecodeStreamK) {
     const int C = decode_cluster_size(a);
-    if (C > 0 && (a.decode_variant == kDecodeCluster || cluster_pays(a, C)))
-      return launch_attn_decode_cluster(a, C, name);
+    const int M = decode_cluster_split(a, C);
+    if (C > 0 && (a.decode_variant == kDecodeCluster || cluster_pays(a, C, M)))
+      return launch_attn_decode_cluster(a, C, M, name);
     if (a.decode_variant == kDecodeCluster) return cudaErrorInvalidValue;
   }
   if (a.Dv != a.D) return launch_attn_decode_mixed(a, name);

@@ -30,12 +30,24 @@ int decode_cluster_size(const AttnArgs& a) {
   }
 }
 
-cudaError_t launch_attn_decode_cluster(const AttnArgs& a, int C, const char** name) {
+int decode_cluster_split(const AttnArgs& a, int C) {
+  if (C <= 0) return 0;
+  const int64_t max_tiles = (a.max_seq + kTile - 1) / kTile;
+  const int64_t units = a.B * a.Hkv * row_groups((a.Hq / a.Hkv) * a.S_q);
   switch (a.D) {
-    case 64: return launch_dc<64>(a, C, name);
-    case 128: return launch_dc<128>(a, C, name);
-    case 256: return launch_dc<256>(a, C, name);
-    case 512: return launch_dc<512>(a, C, name);
+    case 64: return cluster_split_for<64>(a.B, units, max_tiles, C);
+    case 128: return cluster_split_for<128>(a.B, units, max_tiles, C);
+    case 256: return cluster_split_for<256>(a.B, units, max_tiles, C);
+    default: return cluster_split_for<512>(a.B, units, max_tiles, C);
+  }
+}
+
+cudaError_t launch_attn_decode_cluster(const AttnArgs& a, int C, int M, const char** name) {
+  switch (a.D) {
+    case 64: return launch_dc<64>(a, C, M, name);
+    case 128: return launch_dc<128>(a, C, M, name);
+    case 256: return launch_dc<256>(a, C, M, name);
+    case 512: return launch_dc<512>(a, C, M, name);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -17,9 +17,10 @@
 //   Live tiles: every CTA of the unit finds the unit's live 16-key tiles by
 //     itself -- without a bias, the tiles below nonpad; with the fused
 //     specification, the closed-form runs of the rows' allowed intervals;
-//     with a materialised bias, one bulk copy of the batch's S_q bias rows
-//     into shared memory and a scan (a tile is live when some key below
-//     nonpad has a bias above lowest(T), section 6 of the ORT page).
+//     with a materialised bias, one bulk copy of the batch's S_q bias rows,
+//     multicast by the cluster's first CTA into every CTA's shared memory,
+//     and a scan (a tile is live when some key below nonpad has a bias above
+//     lowest(T), section 6 of the ORT page).
 //   Streaming: CTA r of the cluster takes the r-th of C equal contiguous
 //     shares of the live tiles and streams them with the stream-K kernel's
 //     per-tile pipeline (TMA K/V stages, mma.sync QK^T and PV, online
@@ -31,6 +32,11 @@
 //     depend on timing); a second barrier keeps every CTA's shared memory
 //     alive until its peers have read it.  A row with no unmasked key in any
 //     share is written as zeros.
+//   Few units (one long sequence, say): M clusters per unit, cluster m taking
+//     the m-th of M blocks of the unit's live tiles; each cluster's combine
+//     writes one partial (max, sum, unnormalised output) in the stream-K
+//     kernel's layout instead of Y, and the stream-K merge kernel combines the
+//     M partials in order.
 #pragma once
 
 #include "attn_decode.cuh"
@@ -101,7 +107,7 @@ template <int DK, int DV, int SPW, int MODE, bool CAP>
 __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap tmap,
-    const DecodeParams p, const int C) {
+    const DecodeParams p, const int C, const int M) {
   using S = Smem<DK, DV, SPW>;
   using L = CSmem<DK, DV, SPW>;
   constexpr bool kOneSize = DK == DV;  // the fused scatter takes one head size
@@ -119,7 +125,8 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
   uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
   const int lane = threadIdx.x;
   const int rank = static_cast<int>(ptx::cluster_ctarank());
-  const int unit = static_cast<int>(blockIdx.x) / C;
+  const int cl = static_cast<int>(blockIdx.x) / C;  // cluster
+  const int unit = cl / M, m = cl - unit * M;        // the unit, and which of its M clusters
   const int bh = unit / p.n_rg, rg = unit - bh * p.n_rg;  // bh: the K/V views' unit coordinate
   const int b = bh / p.Hkv, kvh = bh - b * p.Hkv;
   const float lowest = Elem<__nv_bfloat16>::lowest();
@@ -134,20 +141,26 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
     if (kTerm) ptx::prefetch_tensormap(&tmap);
   }
   __syncwarp();
+  // every CTA's barriers are initialised before the first CTA multicasts into them
+  // (the CTAs would wait for the previous kernel here anyway)
+  if (MODE == kBias) ptx::cluster_sync();
   // Nothing above reads an input; everything below may read what the
   // previous kernel in the stream wrote.
   ptx::grid_dependency_wait();
   ptx::grid_launch_dependents();
 
-  // the batch's bias rows, one bulk copy (issued before nonpad is known)
+  // the batch's bias rows: one bulk copy by the first CTA, delivered to all
+  // (issued before nonpad is known); each CTA's barrier expects the bytes
   if (MODE == kBias && lane == 0) {
     const uint32_t bytes = static_cast<uint32_t>(p.S_q) * static_cast<uint32_t>(max_seq) * 2u;
     ptx::mbar_arrive_expect_tx(sbar, bytes);
-    ptx::bulk_load(smem, p.bias + static_cast<int64_t>(b) * p.S_q * max_seq, bytes, sbar);
+    if (rank == 0)
+      ptx::bulk_load_multicast(smem, p.bias + static_cast<int64_t>(b) * p.S_q * max_seq, bytes, sbar,
+                               static_cast<uint16_t>((1u << C) - 1u));
   }
   const int64_t np64 = p.nonpad[b];
   const bool bad = bad_nonpad(np64, max_seq);
-  if (bad && kvh == 0 && rg == 0 && rank == 0 && lane == 0) report(p.status, EXTKV_DEV_BAD_NONPAD);
+  if (bad && kvh == 0 && rg == 0 && m == 0 && rank == 0 && lane == 0) report(p.status, EXTKV_DEV_BAD_NONPAD);
   const int np = bad ? 0 : static_cast<int>(np64);
   const int n_range = (np + kTile - 1) / kTile;
 
@@ -226,9 +239,10 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
     __syncwarp();
     ptx::fence_proxy_async_smem();  // the scan's reads precede the stages' TMA fills
   }
-  // this CTA's share of the live tiles: [lo, lo + n)
-  const int lo = static_cast<int>(static_cast<int64_t>(rank) * n_live / C);
-  const int n = static_cast<int>(static_cast<int64_t>(rank + 1) * n_live / C) - lo;
+  // this CTA's share of the live tiles: share m*C + rank of M*C, [lo, lo + n)
+  const int sh = m * C + rank, n_sh = M * C;
+  const int lo = static_cast<int>(static_cast<int64_t>(sh) * n_live / n_sh);
+  const int n = static_cast<int>(static_cast<int64_t>(sh + 1) * n_live / n_sh) - lo;
   auto tile_of = [&](int k) -> int {
     const int x = lo + k;
     if (MODE == kBias) return list[x];
@@ -262,11 +276,11 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
   if (kOneSize && p.k_new) {
     const int64_t w = p.write_idx[b];
     if (w < 0 || w + p.S_new > max_seq) {
-      if (kvh == 0 && rg == 0 && rank == 0 && lane == 0) report(p.status, EXTKV_DEV_BAD_WRITE_IDX);
+      if (kvh == 0 && rg == 0 && m == 0 && rank == 0 && lane == 0) report(p.status, EXTKV_DEV_BAD_WRITE_IDX);
     } else {
       w_new = static_cast<int>(w);
       constexpr int vpr = DK / 8;  // 16-byte vectors per row
-      for (int sn = rank; rg == 0 && sn < p.S_new; sn += C)
+      for (int sn = rank; rg == 0 && m == 0 && sn < p.S_new; sn += C)
         for (int v = lane; v < vpr; v += 32) {
           const int64_t dst = (static_cast<int64_t>(bh) * max_seq + w + sn) * DK + v * 8;
           const int64_t src = (static_cast<int64_t>(bh) * p.S_new + sn) * DK + v * 8;
@@ -521,6 +535,9 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
   ptx::cluster_sync();
   const int cpc = DV / C;  // columns of Y this CTA writes
   const int g4 = cpc / 4;
+  // with several clusters per unit: this cluster's partial, in the stream-K layout
+  float* part = M > 1 ? p.part + static_cast<int64_t>(unit * M + m) * 2 * p.PS : nullptr;
+  if (M > 1 && m == 0 && rank == 0 && lane == 0) p.info[unit] = make_int4(unit * M, M, 0, 0);
   for (int it = lane; it < R * g4; it += 32) {
     const int row = it / g4, col = rank * cpc + (it - row * g4) * 4;
     // every share's (max, sum, O columns) in one round of remote loads
@@ -534,10 +551,10 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
         ov[j] = ptx::ld_cluster_f32x4(ptx::map_cluster(po + row * DV + col, j));
       }
     }
-    float M = -INFINITY;
+    float M_ = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kMaxCluster; ++j)
-      if (j < C) M = fmaxf(M, mj[j]);
+      if (j < C) M_ = fmaxf(M_, mj[j]);
     float Lsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -545,12 +562,21 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
       // a share without an unmasked key (max -inf) adds nothing; its O may not
       // have been written, so it is left out by selection, not by a zero weight
       if (j >= C || mj[j] == -INFINITY) continue;
-      const float wj = ptx::ex2((mj[j] - M) * kLog2e);
+      const float wj = ptx::ex2((mj[j] - M_) * kLog2e);
       Lsum = fmaf(wj, lj[j], Lsum);
       acc.x = fmaf(ov[j].x, wj, acc.x);
       acc.y = fmaf(ov[j].y, wj, acc.y);
       acc.z = fmaf(ov[j].z, wj, acc.z);
       acc.w = fmaf(ov[j].w, wj, acc.w);
+    }
+    if (part) {
+      // unnormalised, relative to this cluster's max (the merge kernel's input)
+      *reinterpret_cast<float4*>(part + 2 * kRows + row * DV + col) = acc;
+      if (rank == 0 && col == 0) {
+        part[row] = M_;
+        part[kRows + row] = Lsum;
+      }
+      continue;
     }
     const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;  // no unmasked key: zero row
     const uint32_t lo2 = ptx::pack_bf16x2(acc.x * inv, acc.y * inv);
@@ -563,7 +589,10 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
 
 // ---- host ---------------------------------------------------------------------------
 
-// Co-resident clusters of C CTAs of `kern` at `smem` bytes (per device, kernel and C).
+// Co-resident clusters of C CTAs of `kern` at `smem` bytes (per device, kernel
+// and C), derated by 1/16: the occupancy query counted 72 clusters of 8 at four
+// CTAs per SM, but the hardware placed 68 (136 of the 152 SMs took clusters),
+// and the other 4 clusters waited for a whole second wave.
 inline int cluster_capacity(const void* kern, size_t smem, int C) {
   static std::mutex mu;
   struct Entry {
@@ -591,6 +620,7 @@ inline int cluster_capacity(const void* kern, size_t smem, int C) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+    n -= (n + 15) / 16;
   }
   (void)cudaGetLastError();
   if (used < 64) entries[used++] = Entry{kern, dev, C, n};
@@ -614,7 +644,7 @@ int cluster_size_for(int64_t units) {
 
 template <int DK, int DV, int MODE, bool CAP>
 cudaError_t launch_dcl(const AttnArgs& a, const DecodeParams& prm, const CUtensorMap& kmap,
-                       const CUtensorMap& vmap, const CUtensorMap& qmap, const CUtensorMap& tmap, int C) {
+                       const CUtensorMap& vmap, const CUtensorMap& qmap, const CUtensorMap& tmap, int C, int M) {
   constexpr int SPW = ClusterCfg<DK>::SPW;
   const size_t smem = CSmem<DK, DV, SPW>::bytes();
   auto kern = attn_decode_cluster_kernel<DK, DV, SPW, MODE, CAP>;
@@ -631,24 +661,53 @@ cudaError_t launch_dcl(const AttnArgs& a, const DecodeParams& prm, const CUtenso
   cfg.stream = a.stream;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.Hkv * prm.n_rg * C));
+  cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.Hkv * prm.n_rg * M * C));
   cfg.blockDim = dim3(32);
   cfg.dynamicSmemBytes = smem;
-  e = cudaLaunchKernelEx(&cfg, kern, kmap, vmap, qmap, tmap, prm, C);
-  if (e == cudaSuccess) note_launches(1);
+  e = cudaLaunchKernelEx(&cfg, kern, kmap, vmap, qmap, tmap, prm, C, M);
+  if (e != cudaSuccess || M == 1) {
+    if (e == cudaSuccess) note_launches(1);
+    return e;
+  }
+  // the M partials of every unit: the stream-K merge kernel
+  const int n_cg = merge_groups(prm.R, DV);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;  // a dependent launch, no cluster
+  cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.Hkv * prm.n_rg * n_cg));
+  cfg.blockDim = dim3(static_cast<unsigned>((prm.R * (DV / 4 / n_cg) + 31) / 32 * 32));
+  cfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&cfg, decode_merge_kernel<MODE>, prm, n_cg);
+  if (e == cudaSuccess) note_launches(2);
   return e;
 }
 
 template <int DK, int DV, int MODE>
 cudaError_t launch_dclc(const AttnArgs& a, const DecodeParams& prm, const CUtensorMap& kmap,
-                        const CUtensorMap& vmap, const CUtensorMap& qmap, const CUtensorMap& tmap, int C) {
-  return a.softcap > 0.f ? launch_dcl<DK, DV, MODE, true>(a, prm, kmap, vmap, qmap, tmap, C)
-                         : launch_dcl<DK, DV, MODE, false>(a, prm, kmap, vmap, qmap, tmap, C);
+                        const CUtensorMap& vmap, const CUtensorMap& qmap, const CUtensorMap& tmap, int C, int M) {
+  return a.softcap > 0.f ? launch_dcl<DK, DV, MODE, true>(a, prm, kmap, vmap, qmap, tmap, C, M)
+                         : launch_dcl<DK, DV, MODE, false>(a, prm, kmap, vmap, qmap, tmap, C, M);
 }
 
-// One head size D for queries, keys and values.  C: from cluster_size_for.
+// Clusters per unit for C CTAs each: as many as fit the GPU at once beside the
+// other units' (at most kMaxSplit), and whose partials fit the workspace
+// (the stream-K layout: two partial slots per CTA of its grid).
+constexpr int kMaxSplit = 16;
+
 template <int D>
-cudaError_t launch_dc(const AttnArgs& a, int C, const char** name) {
+int cluster_split_for(int64_t B, int64_t units, int64_t max_tiles, int C) {
+  constexpr int SPW = ClusterCfg<D>::SPW;
+  const void* kern = reinterpret_cast<const void*>(attn_decode_cluster_kernel<D, D, SPW, kBias, false>);
+  const int cap = cluster_capacity(kern, CSmem<D, D, SPW>::bytes(), C);
+  const DecodeShape shape = decode_shape<D, D>(B, units * max_tiles);
+  int64_t M = std::min<int64_t>(kMaxSplit, cap / std::max<int64_t>(units, 1));
+  M = std::min<int64_t>(M, shape.G / std::max<int64_t>(units, 1));
+  return static_cast<int>(std::max<int64_t>(M, 1));
+}
+
+// One head size D for queries, keys and values.  C: from cluster_size_for; M:
+// clusters per unit (from cluster_split_for; M > 1 needs the workspace).
+template <int D>
+cudaError_t launch_dc(const AttnArgs& a, int C, int M, const char** name) {
   const int64_t max_tiles = (a.max_seq + kTile - 1) / kTile;
   CUtensorMap kmap, vmap, qmap, tmap;
   // K/V and Q through the same views as the stream-K kernel: one TMA box
@@ -701,12 +760,25 @@ cudaError_t launch_dc(const AttnArgs& a, int C, const char** name) {
   prm.v_new = static_cast<const __nv_bfloat16*>(a.v_new);
   prm.write_idx = a.write_idx;
   prm.S_new = static_cast<int>(a.S_new);
+  if (M > 1) {
+    // the clusters' partials and the units' slice records, where the stream-K
+    // kernels keep theirs
+    const int64_t units = a.B * a.Hkv * prm.n_rg;
+    const DecodeShape shape = decode_shape<D, D>(a.B, units * max_tiles);
+    if (units * M > shape.G) return cudaErrorInvalidValue;
+    const WsLayout ws = ws_layout(a.B, a.Hkv * prm.n_rg, max_tiles, shape.G, prm.R, D);
+    if (!a.workspace || a.ws_bytes < ws.total) return cudaErrorInvalidValue;
+    uint8_t* wsb = static_cast<uint8_t*>(a.workspace);
+    prm.info = reinterpret_cast<int4*>(wsb + ws.info);
+    prm.part = reinterpret_cast<float*>(wsb + ws.part);
+    prm.PS = static_cast<int>(part_floats(prm.R, D));
+  }
   cudaError_t e;
   switch (mode_of(a)) {
-    case kNone: e = launch_dclc<D, D, kNone>(a, prm, kmap, vmap, qmap, tmap, C); break;
-    case kBias: e = launch_dclc<D, D, kBias>(a, prm, kmap, vmap, qmap, tmap, C); break;
-    case kFused: e = launch_dclc<D, D, kFused>(a, prm, kmap, vmap, qmap, tmap, C); break;
-    default: e = launch_dclc<D, D, kFusedExtra>(a, prm, kmap, vmap, qmap, tmap, C); break;
+    case kNone: e = launch_dclc<D, D, kNone>(a, prm, kmap, vmap, qmap, tmap, C, M); break;
+    case kBias: e = launch_dclc<D, D, kBias>(a, prm, kmap, vmap, qmap, tmap, C, M); break;
+    case kFused: e = launch_dclc<D, D, kFused>(a, prm, kmap, vmap, qmap, tmap, C, M); break;
+    default: e = launch_dclc<D, D, kFusedExtra>(a, prm, kmap, vmap, qmap, tmap, C, M); break;
   }
   if (e != cudaSuccess) return e;
   *name = prm.k_new ? "attn_decode_cluster_scatter" : "attn_decode_cluster";

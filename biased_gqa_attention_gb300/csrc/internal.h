@@ -70,10 +70,12 @@ bool decode_supported(const AttnArgs& a);
 size_t decode_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t Dk,
                               int64_t Dv);
 cudaError_t launch_attn_decode(const AttnArgs& a, const char** name);
-// The cluster decode kernel: CTAs per unit it would use for this call (0: it
-// cannot take the call), and its launch with that many.
+// The cluster decode kernel: CTAs per cluster it would use for this call (0:
+// it cannot take the call), clusters per unit (M > 1: each cluster leaves a
+// partial for the stream-K merge kernel), and its launch.
 int decode_cluster_size(const AttnArgs& a);
-cudaError_t launch_attn_decode_cluster(const AttnArgs& a, int C, const char** name);
+int decode_cluster_split(const AttnArgs& a, int C);
+cudaError_t launch_attn_decode_cluster(const AttnArgs& a, int C, int M, const char** name);
 bool prefill_supported(const AttnArgs& a);
 // Dk, Dv: the key and value head sizes (the partial rows of key splits hold Dv columns)
 size_t prefill_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t max_seq, int64_t Dk,

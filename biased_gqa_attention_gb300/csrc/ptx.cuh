@@ -137,6 +137,18 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// The same copy delivered to every CTA of the cluster in `mask`, at the same
+// shared-memory offsets (dst and bar in this CTA's window); each destination's
+// barrier receives the bytes.
+__device__ __forceinline__ void bulk_load_multicast(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                                    uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+
 // 4-byte asynchronous copy global -> shared (both addresses 4-byte aligned);
 // completes for the issuing thread at cp_async_wait_all().
 __device__ __forceinline__ void cp_async_4(void* dst_smem, const void* src) {

@@ -183,3 +183,75 @@ def test_cluster_scan_reads_special_bias_values():
     ref = oracle.attention(raw(inp.q), raw(inp.k_cache), raw(inp.v_cache), bias, nonpad, np.float32(w.scale))
     assert (y[3] == 0).all()
     assert max_err(y, ref) <= TOL[w.dtype]
+
+
+# few units: several clusters per unit, each leaving a partial for the merge kernel
+FEW = [
+    # one sequence: 8 units
+    wl.Workload("cl_b1", 411, B=1, Hq=16, Hkv=8, D=256, S_q=1, max_seq=4096, dtype=torch.bfloat16,
+                causal=True, window=0, nonpad_fixed=4000),
+    # one sequence, two KV heads with two row groups each (8 heads x 2 positions)
+    wl.Workload("cl_b1_rg", 412, B=1, Hq=16, Hkv=2, D=128, S_q=2, max_seq=2048, dtype=torch.bfloat16,
+                causal=True, window=600, nonpad_fixed=1900),
+    # two sequences at head size 64 with a short one (empty shares)
+    wl.Workload("cl_b2_d64", 413, B=2, Hq=8, Hkv=2, D=64, S_q=1, max_seq=1024, dtype=torch.bfloat16,
+                causal=True, window=0, nonpad_range=(5, 1024)),
+]
+
+
+@pytest.mark.parametrize("mode", ["bias", "fused", "none"])
+@pytest.mark.parametrize("w", FEW, ids=lambda w: w.name)
+def test_cluster_decode_split_units_match_the_oracle(w, mode):
+    inp = wl.make_inputs(w, "cuda")
+    g = run_gpu(inp, mode=mode, algo=ek.ALGO_DECODE_CLUSTER)
+    assert g["kernel"] == CL
+    assert ek.extkv_last_launches() == 2  # the clusters, then the merge of their partials
+    o = oracle_path(inp, mode=mode)
+    assert max_err(g["y"], o["y"]) <= TOL[w.dtype]
+
+
+@pytest.mark.parametrize("mode", ["bias", "fused"])
+def test_cluster_decode_split_units_with_the_fused_scatter(mode):
+    w = FEW[0]
+    inp = wl.make_inputs(w, "cuda")
+    ref = run_gpu(inp, mode=mode, algo=ek.ALGO_DECODE_CLUSTER)  # separate scatter, then attention
+    k, v = inp.k_cache.clone(), inp.v_cache.clone()
+    y = torch.empty_like(inp.q)
+    st = ek.new_status()
+    with ek.use_algo(ek.ALGO_DECODE_CLUSTER):
+        ek.attention_ext_kv_scatter(y, inp.q, k, v, inp.k_new, inp.v_new, inp.write_idx, inp.nonpad, w.scale,
+                                    bias=ref["bias"] if mode == "bias" else None,
+                                    fused=spec_of(inp) if mode == "fused" else None, status=st)
+        assert ek.extkv_last_kernel() == CL + "_scatter"
+    assert ek.extkv_read_status(st) == ek.EXTKV_OK, ek.extkv_last_error()
+    assert torch.equal(y.view(torch.int16), ref["y"].view(torch.int16))
+    assert torch.equal(k.view(torch.int16), ref["k"].view(torch.int16))
+    assert torch.equal(v.view(torch.int16), ref["v"].view(torch.int16))
+
+
+def test_cluster_decode_split_units_timeout_is_reported():
+    w = FEW[0]
+    inp = wl.make_inputs(w, "cuda")
+    ref = run_gpu(inp, mode="bias", algo=ek.ALGO_DECODE_CLUSTER)
+    y = torch.empty_like(ref["y"])
+    st = ek.new_status()
+    with ek.use_algo(ek.ALGO_DECODE_CLUSTER), ek.wait_polls(0):
+        ek.attention_ext_kv(y, inp.q, ref["k"], ref["v"], inp.nonpad, w.scale, bias=ref["bias"], status=st)
+    assert int(st[0].item()) & ek.EXTKV_DEV_TIMEOUT
+    y2 = torch.empty_like(ref["y"])
+    st2 = ek.new_status()
+    with ek.use_algo(ek.ALGO_DECODE_CLUSTER):
+        ek.attention_ext_kv(y2, inp.q, ref["k"], ref["v"], inp.nonpad, w.scale, bias=ref["bias"], status=st2)
+    assert ek.extkv_read_status(st2) == ek.EXTKV_OK
+    assert torch.equal(y2.view(torch.int16), ref["y"].view(torch.int16))
+
+
+def test_one_long_sequence_picks_the_split_cluster_kernel():
+    w = wl.Workload("cl_b1_long", 414, B=1, Hq=16, Hkv=8, D=256, S_q=1, max_seq=8192, dtype=torch.bfloat16,
+                    causal=True, window=0, nonpad_fixed=8000)
+    inp = wl.make_inputs(w, "cuda")
+    g = run_gpu(inp, mode="bias")
+    assert g["kernel"] == CL and ek.extkv_last_launches() == 2
+    rows = sample_rows(w, 64)
+    o = oracle_path(inp, rows=rows, mode="bias")
+    assert max_err(g["y"], o["y"], rows=rows) <= TOL[w.dtype]
