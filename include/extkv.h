@@ -397,14 +397,15 @@ void extkv_step_free(extkv_step *step);
 #define EXTKV_ALGO_DECODE_STREAMK 5 /* the stream-K decode alone: a plan kernel (materialised bias),
                                        the decode kernel over equal slices of all live tiles, a
                                        merge kernel for units split across slices */
-#define EXTKV_ALGO_DECODE_CLUSTER 6 /* the cluster decode alone: one kernel, a cluster of up to 8
-                                       CTAs per (batch, KV head, group of up to 8 query rows)
-                                       sharing its live tiles, combined through distributed shared
-                                       memory.  bf16, one head size in {64,128,256,512}, S_q <= 8,
-                                       S_q*Hq/Hkv <= 64, all clusters resident at once; a
-                                       materialised bias with S_q*max_seq <= 8192 (one copy of a
-                                       batch's rows is scanned); with the fused spec, no spans
-                                       when S_q > 1 */
+#define EXTKV_ALGO_DECODE_CLUSTER 6 /* the cluster decode alone: a cluster of up to 8 CTAs per
+                                       (batch, KV head, group of up to 8 query rows) sharing its
+                                       live tiles, combined through distributed shared memory (one
+                                       kernel); with few units, up to 16 clusters per unit whose
+                                       partials the stream-K merge kernel combines.  bf16, one head
+                                       size in {64,128,256,512}, S_q <= 8, S_q*Hq/Hkv <= 64, all
+                                       clusters resident at once; a materialised bias with
+                                       S_q*max_seq <= 8192 (one copy of a batch's rows is
+                                       scanned); with the fused spec, no spans when S_q > 1 */
 int extkv_set_algo(int algo);
 
 #ifdef __cplusplus
