@@ -33,8 +33,9 @@ bool mixed_pair(int64_t Dk, int64_t Dv) {
 // gives no bound without reading it.
 constexpr double kClusterSlack = 8.0;
 // the merge kernel a split into M > 1 clusters per unit adds (its launch and
-// two dependent round trips), in the same units
-constexpr double kMergeTiles = 4.0;
+// two dependent round trips), in the same units (measured: the split wins
+// against stream-K from one to four long sequences)
+constexpr double kMergeTiles = 2.0;
 
 bool cluster_pays(const AttnArgs& a, int C, int M) {
   const int64_t max_tiles = (a.max_seq + kTile - 1) / kTile;
