@@ -578,8 +578,8 @@ def run_e2e(dec: Decoder, K: int, W: int, world: int, device):
     sec_calls = timed(False)
     sec = timed(True)
     assert dec.ek.extkv_read_status(dec.status) == dec.ek.EXTKV_OK, dec.ek.extkv_last_error()
-    # every set's last output reached its pinned host buffer
-    for r in range(R):
+    # the last output of every set the loop ran reached its pinned host buffer
+    for r in range(min(R, max(W, K))):
         assert torch.equal(y_hosts[r], dec.sets[r]["y"].cpu()), "an output copy did not land"
     nonpad, _, spans = wl.structure(w)
     amount, scale, unit = step_work(w, nonpad.numpy(), spans, dec.mode)
