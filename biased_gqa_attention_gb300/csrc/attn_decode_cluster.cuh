@@ -1,13 +1,14 @@
 // attn_decode_cluster.cuh -- decode attention for calls whose units fit the
-// GPU at once: one thread-block cluster per (batch, KV head), one kernel.
+// GPU at once: thread-block clusters per (batch, KV head, row group).
 //
 // The stream-K decode (attn_decode.cuh) balances any number of units over a
 // fixed grid, at the price of a plan kernel (a materialised bias), per-batch
 // tables of the whole call in every CTA and a merge kernel: fixed costs that
 // dominate a call of a few tens of MB ("Skill: Attention Optimization":
 // decode is memory-bandwidth bound, so what is not streaming is overhead).
-// When every unit can hold C CTAs resident at once, this kernel removes all
-// three:
+// When every unit can hold a cluster of C CTAs resident at once, this kernel
+// removes all three (the merge stays only where a unit is split over several
+// clusters):
 //
 //   Unit: one (batch b, KV head, row group): up to 8 of the KV head's
 //     GR = (Hq/Hkv) * S_q <= 64 query rows (GQA by reshaping Q, "ONNX Domain
@@ -22,7 +23,7 @@
 //     and a scan (a tile is live when some key below nonpad has a bias above
 //     lowest(T), section 6 of the ORT page).
 //   Streaming: CTA r of the cluster takes the r-th of C equal contiguous
-//     shares of the live tiles and streams them with the stream-K kernel's
+//     shares of the live tiles (of its cluster's block, below) and streams them with the stream-K kernel's
 //     per-tile pipeline (TMA K/V stages, mma.sync QK^T and PV, online
 //     softmax in natural units, dead keys' V rows zeroed).
 //   Combine: each CTA leaves (max, sum, unnormalised output) of its share in
