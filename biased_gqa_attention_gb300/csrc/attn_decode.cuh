@@ -270,7 +270,9 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeP
   if (staged && tid == 0) {
     ptx::mbar_arrive_expect_tx(bar, row_bytes * p.S_q);
     for (int i = 0; i < p.S_q; ++i)
-      ptx::bulk_load(rows + i * pitch, p.bias + (static_cast<int64_t>(b) * p.S_q + i) * max_seq, row_bytes, bar);
+      if (EXTKV_IN((static_cast<int64_t>(b) * p.S_q + i) * max_seq, max_seq,
+                   static_cast<int64_t>(p.B) * p.S_q * max_seq, p.status))
+        ptx::bulk_load(rows + i * pitch, p.bias + (static_cast<int64_t>(b) * p.S_q + i) * max_seq, row_bytes, bar);
   }
   const int64_t np64 = p.nonpad[b];
   const bool bad = bad_nonpad(np64, max_seq);
@@ -333,8 +335,12 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeP
   int pos = base + incl - cnt;
   uint16_t* list = p.tiles + static_cast<int64_t>(b) * p.max_tiles;
   for (int t = my_lo; t < my_hi; ++t)
-    if (flags[t]) list[pos++] = static_cast<uint16_t>(t);
-  if (tid == 0) p.count[b] = total;
+    if (flags[t]) {
+      if (EXTKV_IN(static_cast<int64_t>(b) * p.max_tiles + pos, 1, static_cast<int64_t>(p.B) * p.max_tiles, p.status))
+        list[pos] = static_cast<uint16_t>(t);
+      ++pos;
+    }
+  if (tid == 0 && EXTKV_IN(b, 1, p.B, p.status)) p.count[b] = total;
 }
 
 // ---- per-batch tables shared by the decode and merge kernels --------------------
@@ -358,6 +364,7 @@ __device__ __forceinline__ int64_t batch_tables(const DecodeParams& p, int lane,
       int cnt;
       if (p.plan) {
         cnt = p.count[b];
+        if (!EXTKV_IN(0, cnt, p.max_tiles, p.status)) cnt = 0;  // a count past the batch's tiles
       } else {
         const Runs r = batch_runs<MODE>(p, b, np64);
         runs_s[b] = r;
@@ -493,6 +500,9 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
         continue;
       }
       const int64_t dst = (bh * p.max_seq + w + sn) * D + v * 8, src = row * D + v * 8;
+      const int64_t n_bh = static_cast<int64_t>(p.B) * p.Hkv;
+      if (!EXTKV_IN(dst, 8, n_bh * p.max_seq * D, p.status) || !EXTKV_IN(src, 8, n_bh * p.S_new * D, p.status))
+        continue;
       *reinterpret_cast<uint4*>(p.kc_w + dst) = __ldg(reinterpret_cast<const uint4*>(p.k_new + src));
       *reinterpret_cast<uint4*>(p.vc_w + dst) = __ldg(reinterpret_cast<const uint4*>(p.v_new + src));
     }
@@ -532,7 +542,8 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
     // the slice's tile numbers, from the plan's per-batch lists
     for (int k = lane; k < n; k += 32) {
       const Cursor q = cursor_at(x0 + k);
-      work[k] = p.tiles[static_cast<int64_t>(q.b) * p.max_tiles + q.kk];
+      const int64_t at = static_cast<int64_t>(q.b) * p.max_tiles + q.kk;
+      work[k] = EXTKV_IN(at, 1, static_cast<int64_t>(p.B) * p.max_tiles, p.status) ? p.tiles[at] : 0;
     }
     __syncwarp();
   }
@@ -586,11 +597,13 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
         if (q_regs) {
           // B fragment of k-step ks: the bf16 pair at (row lane/4, d = 16 ks + 2 (lane%4)), and d + 8
           const int row = lane >> 2;
+          const bool qok =
+              row < p_nr && EXTKV_IN(p_row0 + row, 1, static_cast<int64_t>(p.B) * p.Hq * p.S_q, p.status);
           const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + static_cast<int64_t>(p_row0 + row) * DK) + (lane & 3);
 #pragma unroll
           for (int ks = 0; ks < kKSteps; ++ks) {
-            qn[ks][0] = row < p_nr ? __ldg(qrow + 8 * ks) : 0u;
-            qn[ks][1] = row < p_nr ? __ldg(qrow + 8 * ks + 4) : 0u;
+            qn[ks][0] = qok ? __ldg(qrow + 8 * ks) : 0u;
+            qn[ks][1] = qok ? __ldg(qrow + 8 * ks + 4) : 0u;
           }
         }
       }
@@ -641,14 +654,17 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
       const float inv0 = live0 ? 1.f / l0 : 0.f, inv1 = live1 ? 1.f / l1 : 0.f;
       __nv_bfloat16* y0 = p.y + (row0 + r0) * DV;
       __nv_bfloat16* y1 = p.y + (row0 + r1) * DV;
+      const int64_t n_y = static_cast<int64_t>(p.B) * p.Hq * p.S_q * DV;
+      const bool yok0 = ok0 && EXTKV_IN((row0 + r0) * DV, DV, n_y, p.status);
+      const bool yok1 = ok1 && EXTKV_IN((row0 + r1) * DV, DV, n_y, p.status);
 #pragma unroll
       for (int mt = 0; mt < DV / 16; ++mt) {
         const int d = mt * 16 + (lane >> 2);
-        if (ok0) {
+        if (yok0) {
           y0[d] = __float2bfloat16_rn(o[mt][0] * inv0);
           y0[d + 8] = __float2bfloat16_rn(o[mt][2] * inv0);
         }
-        if (ok1) {
+        if (yok1) {
           y1[d] = __float2bfloat16_rn(o[mt][1] * inv1);
           y1[d + 8] = __float2bfloat16_rn(o[mt][3] * inv1);
         }
@@ -657,6 +673,8 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
     }
     // slot 0: the slice's first unit (it began at or before x0); slot 1: its last
     const int slot = ub <= x0 ? 0 : 1;
+    if (!EXTKV_IN((static_cast<int64_t>(c) * 2 + slot) * p.PS, p.PS, static_cast<int64_t>(p.G) * 2 * p.PS, p.status))
+      return;
     float* part = p.part + (static_cast<int64_t>(c) * 2 + slot) * p.PS;
     float* o0 = part + 2 * kRows + r0 * DV;
     float* o1 = part + 2 * kRows + r1 * DV;
@@ -706,7 +724,9 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
         // this slice holds the unit's first item: record where its partials live
         const int64_t last = ub + cc.cnt - 1;
         const int c_last = static_cast<int>(((last + 1) * G - 1) / T);  // slice holding `last`
-        p.info[(cc.b * p.Hkv + cc.kvh) * p.n_rg + cc.rg] = make_int4(c, c_last - c + 1, ub <= x0 ? 0 : 1, 0);
+        const int64_t at = (static_cast<int64_t>(cc.b) * p.Hkv + cc.kvh) * p.n_rg + cc.rg;
+        if (EXTKV_IN(at, 1, static_cast<int64_t>(p.B) * p.Hkv * p.n_rg, p.status))
+          p.info[at] = make_int4(c, c_last - c + 1, ub <= x0 ? 0 : 1, 0);
       }
       np = np_s[cc.b];
       if (p.k_new) w_new = wi_s[cc.b];  // -1: the scatter skipped this batch, no patch
@@ -749,6 +769,7 @@ __global__ void __launch_bounds__(32) attn_decode_kernel(
         const int r = key - key0, ch = idx % vpr;
         const int off = (ch >> 3) * (kTile * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
         const int64_t src = (nb + (key - w_new)) * D + ch * 8;
+        if (!EXTKV_IN(src, 8, static_cast<int64_t>(p.B) * p.Hkv * p.S_new * D, p.status)) continue;
         *reinterpret_cast<uint4*>(kst + off) = __ldg(reinterpret_cast<const uint4*>(p.k_new + src));
         *reinterpret_cast<uint4*>(kst + S::kKTileBytes + off) = __ldg(reinterpret_cast<const uint4*>(p.v_new + src));
       }
@@ -940,6 +961,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + static_cast<int64_t>(kvh) * p.g) * p.S_q + rg * kRows;
   if (i >= R * cols) return;
   auto store = [&](const float4& acc) {
+    if (!EXTKV_IN((row0 + r) * D + d4, 4, static_cast<int64_t>(p.B) * p.Hq * p.S_q * D, p.status)) return;
     __nv_bfloat16* yr = p.y + (row0 + r) * D + d4;
     uint2 pk;
     pk.x = ptx::pack_bf16x2(acc.x, acc.y);
@@ -952,6 +974,11 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   }
   const int ns = info.y;
   if (ns == 1) return;  // written by the decode kernel
+  // the slices' partials, recorded by the decode kernel: inside the partial slots
+  if (!EXTKV_IN(static_cast<int64_t>(info.x) * 2 * p.PS, static_cast<int64_t>(ns) * 2 * p.PS,
+                static_cast<int64_t>(p.G) * 2 * p.PS, p.status) ||
+      !EXTKV_IN(info.z, 1, 2, p.status))
+    return;
   constexpr int PS = 2 * kRows;  // header floats of a partial
   const int stride = p.PS;
   // slice s of the unit: CTA info.x + s; the unit is the first unit of every

@@ -155,11 +155,12 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
   if (MODE == kBias && lane == 0) {
     const uint32_t bytes = static_cast<uint32_t>(p.S_q) * static_cast<uint32_t>(max_seq) * 2u;
     ptx::mbar_arrive_expect_tx(sbar, bytes);
-    if (rank == 0)
+    if (rank == 0 && EXTKV_IN(static_cast<int64_t>(b) * p.S_q * max_seq, static_cast<int64_t>(p.S_q) * max_seq,
+                              static_cast<int64_t>(p.B) * p.S_q * max_seq, p.status))
       ptx::bulk_load_multicast(smem, p.bias + static_cast<int64_t>(b) * p.S_q * max_seq, bytes, sbar,
                                static_cast<uint16_t>((1u << C) - 1u));
   }
-  const int64_t np64 = p.nonpad[b];
+  const int64_t np64 = EXTKV_IN(b, 1, p.B, p.status) ? p.nonpad[b] : 0;
   const bool bad = bad_nonpad(np64, max_seq);
   if (bad && kvh == 0 && rg == 0 && m == 0 && rank == 0 && lane == 0) report(p.status, EXTKV_DEV_BAD_NONPAD);
   const int np = bad ? 0 : static_cast<int>(np64);
@@ -180,12 +181,13 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
   if constexpr (kQReg) {
     // B fragment of k-step ks: the bf16 pair at (row lane/4, d = 16 ks + 2 (lane%4)), and d + 8
     const int row = lane >> 2;
+    const bool qok = row < R && EXTKV_IN(row0 + row, 1, static_cast<int64_t>(p.B) * p.Hq * p.S_q, p.status);
     const uint32_t* qrow =
         reinterpret_cast<const uint32_t*>(p.q + (row0 + row) * static_cast<int64_t>(DK)) + (lane & 3);
 #pragma unroll
     for (int ks = 0; ks < kKSteps; ++ks) {
-      qf[ks][0] = row < R ? __ldg(qrow + 8 * ks) : 0u;
-      qf[ks][1] = row < R ? __ldg(qrow + 8 * ks + 4) : 0u;
+      qf[ks][0] = qok ? __ldg(qrow + 8 * ks) : 0u;
+      qf[ks][1] = qok ? __ldg(qrow + 8 * ks + 4) : 0u;
     }
   } else if (lane == 0) {
     ptx::mbar_arrive_expect_tx(qbar, S::kQBytes);
@@ -275,7 +277,7 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
   // from k_new / v_new below.
   int w_new = -1;  // first new slot of the batch, -1: none or out of range (skipped)
   if (kOneSize && p.k_new) {
-    const int64_t w = p.write_idx[b];
+    const int64_t w = EXTKV_IN(b, 1, p.B, p.status) ? p.write_idx[b] : -1;
     if (w < 0 || w + p.S_new > max_seq) {
       if (kvh == 0 && rg == 0 && m == 0 && rank == 0 && lane == 0) report(p.status, EXTKV_DEV_BAD_WRITE_IDX);
     } else {
@@ -285,6 +287,9 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
         for (int v = lane; v < vpr; v += 32) {
           const int64_t dst = (static_cast<int64_t>(bh) * max_seq + w + sn) * DK + v * 8;
           const int64_t src = (static_cast<int64_t>(bh) * p.S_new + sn) * DK + v * 8;
+          const int64_t n_bh = static_cast<int64_t>(p.B) * p.Hkv;
+          if (!EXTKV_IN(dst, 8, n_bh * max_seq * DK, p.status) || !EXTKV_IN(src, 8, n_bh * p.S_new * DK, p.status))
+            continue;
           *reinterpret_cast<uint4*>(p.kc_w + dst) = __ldg(reinterpret_cast<const uint4*>(p.k_new + src));
           *reinterpret_cast<uint4*>(p.vc_w + dst) = __ldg(reinterpret_cast<const uint4*>(p.v_new + src));
         }
@@ -339,6 +344,7 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
         const int r = key - key0, ch = idx % vpr;
         const int off = (ch >> 3) * (kTile * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
         const int64_t src = (nb + (key - w_new)) * D + ch * 8;
+        if (!EXTKV_IN(src, 8, static_cast<int64_t>(p.B) * p.Hkv * p.S_new * D, p.status)) continue;
         *reinterpret_cast<uint4*>(kst + off) = __ldg(reinterpret_cast<const uint4*>(p.k_new + src));
         *reinterpret_cast<uint4*>(kst + S::kKTileBytes + off) = __ldg(reinterpret_cast<const uint4*>(p.v_new + src));
       }
@@ -538,7 +544,9 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
   const int g4 = cpc / 4;
   // with several clusters per unit: this cluster's partial, in the stream-K layout
   float* part = M > 1 ? p.part + static_cast<int64_t>(unit * M + m) * 2 * p.PS : nullptr;
-  if (M > 1 && m == 0 && rank == 0 && lane == 0) p.info[unit] = make_int4(unit * M, M, 0, 0);
+  if (M > 1 && m == 0 && rank == 0 && lane == 0 &&
+      EXTKV_IN(unit, 1, static_cast<int64_t>(p.B) * p.Hkv * p.n_rg, p.status))
+    p.info[unit] = make_int4(unit * M, M, 0, 0);
   for (int it = lane; it < R * g4; it += 32) {
     const int row = it / g4, col = rank * cpc + (it - row * g4) * 4;
     // every share's (max, sum, O columns) in one round of remote loads
@@ -572,6 +580,9 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
     }
     if (part) {
       // unnormalised, relative to this cluster's max (the merge kernel's input)
+      if (!EXTKV_IN(static_cast<int64_t>(unit * M + m) * 2 * p.PS + 2 * kRows + row * DV + col, 4,
+                    static_cast<int64_t>(p.G) * 2 * p.PS, p.status))
+        continue;
       *reinterpret_cast<float4*>(part + 2 * kRows + row * DV + col) = acc;
       if (rank == 0 && col == 0) {
         part[row] = M_;
@@ -582,7 +593,8 @@ __global__ void __launch_bounds__(32) attn_decode_cluster_kernel(
     const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;  // no unmasked key: zero row
     const uint32_t lo2 = ptx::pack_bf16x2(acc.x * inv, acc.y * inv);
     const uint32_t hi2 = ptx::pack_bf16x2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(p.y + (row0 + row) * DV + col) = make_uint2(lo2, hi2);
+    if (EXTKV_IN((row0 + row) * DV + col, 4, static_cast<int64_t>(p.B) * p.Hq * p.S_q * DV, p.status))
+      *reinterpret_cast<uint2*>(p.y + (row0 + row) * DV + col) = make_uint2(lo2, hi2);
   }
   __syncwarp();
   ptx::cluster_sync();  // peers may still read this CTA's share until here
@@ -773,6 +785,7 @@ cudaError_t launch_dc(const AttnArgs& a, int C, int M, const char** name) {
     prm.info = reinterpret_cast<int4*>(wsb + ws.info);
     prm.part = reinterpret_cast<float*>(wsb + ws.part);
     prm.PS = static_cast<int>(part_floats(prm.R, D));
+    prm.G = shape.G;  // the partial slots' extent (two per CTA of the stream-K grid)
   }
   cudaError_t e;
   switch (mode_of(a)) {

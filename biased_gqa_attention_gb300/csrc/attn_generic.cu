@@ -71,6 +71,8 @@ __global__ void __launch_bounds__(32 * kWarps) attn_generic_kernel(
       jlo = win.lo();
       jhi = win.hi();
     }
+    // the keys the row reads, inside the cache rows and the bias row
+    if (jhi > jlo && !EXTKV_IN(jlo, jhi - jlo, max_seq, status)) jhi = jlo;
     float m = -INFINITY, l = 0.0f;
     for (int64_t j0 = jlo; j0 < jhi; j0 += 32) {
       // Each lane decides one key of this group of 32; the warp then walks

@@ -440,14 +440,20 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_bias_kernel(const _
   // the row bits, where the attention kernel reads them: tiles that hold a
   // live key and whose bias is 0 or the sentinel throughout
   if (keys > 0 && !impure_s) {
+    const int64_t rm0 = (static_cast<int64_t>(b) * n_pt + pt) * kBM * rm_stride + kt * 16 + kc;
+    const int64_t n_rm = static_cast<int64_t>(gridDim.z) * n_pt * kBM * rm_stride;
 #pragma unroll
     for (int i = 0; i < kBM / kGroups; ++i)
-      rm[static_cast<int64_t>(grp + kGroups * i) * rm_stride] = static_cast<uint8_t>(mrow[i >> 2] >> (8 * (i & 3)));
+      if (EXTKV_IN(rm0 + static_cast<int64_t>(grp + kGroups * i) * rm_stride, 1, n_rm, status))
+        rm[static_cast<int64_t>(grp + kGroups * i) * rm_stride] = static_cast<uint8_t>(mrow[i >> 2] >> (8 * (i & 3)));
   }
-  if (tid == 0) impure[(static_cast<int64_t>(b) * n_pt + pt) * n_kt + kt] = static_cast<uint8_t>(impure_s);
+  if (tid == 0 && EXTKV_IN((static_cast<int64_t>(b) * n_pt + pt) * n_kt + kt, 1,
+                           static_cast<int64_t>(gridDim.z) * n_pt * n_kt, status))
+    impure[(static_cast<int64_t>(b) * n_pt + pt) * n_kt + kt] = static_cast<uint8_t>(impure_s);
   if (tid < kBN / 64) {
     const int t = kt * (kBN / 64) + tid;
-    if (t < n_words)
+    if (t < n_words && EXTKV_IN((static_cast<int64_t>(b) * n_pt + pt) * n_words + t, 1,
+                                static_cast<int64_t>(gridDim.z) * n_pt * n_words, status))
       colmask[(static_cast<int64_t>(b) * n_pt + pt) * n_words + t] =
           static_cast<uint64_t>(words[2 * tid]) | (static_cast<uint64_t>(words[2 * tid + 1]) << 32);
   }
@@ -743,10 +749,12 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
       bool ok = true;
       // term blocks of the tiles that need one, buffers taken in that order;
       // the flag of the next tile is loaded one call ahead (calls come in tile order)
-      bool imp_next = MODE != kBias || (T > 0 && p.impure[imp0 + t_lo] != 0);
+      bool imp_next = MODE != kBias || (T > 0 && EXTKV_IN(imp0 + t_lo, T, static_cast<int64_t>(p.B) * p.n_pt * p.n_kt, p.status) &&
+                                        p.impure[imp0 + t_lo] != 0);
       auto load_term = [&](int j) -> bool {
         const bool imp = imp_next;
-        if (MODE == kBias && j + 1 < T) imp_next = p.impure[imp0 + t_lo + j + 1] != 0;
+        if (MODE == kBias && j + 1 < T)
+          imp_next = EXTKV_IN(imp0 + t_lo + j + 1, 1, static_cast<int64_t>(p.B) * p.n_pt * p.n_kt, p.status) && p.impure[imp0 + t_lo + j + 1] != 0;
         if (!imp) return true;  // the row bits suffice
         const int tb = t_issued % C::kTB;
         if (t_issued >= C::kTB && !wait_or_abort(&bar.t_empty[tb], ((t_issued / C::kTB) - 1) & 1, abort, lim))
@@ -938,15 +946,17 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
       ptx::mbar_arrive(&bar.q_full);
     }
     // whether the bias of a tile holds only 0 and the sentinel: loaded one tile ahead
-    bool pure_next = MODE == kBias && T > 0 && p.impure[imp0 + t_lo] == 0;
+    bool pure_next = MODE == kBias && T > 0 && EXTKV_IN(imp0 + t_lo, T, static_cast<int64_t>(p.B) * p.n_pt * p.n_kt, p.status) &&
+                     p.impure[imp0 + t_lo] == 0;
     for (int j = 0; j < T; ++j) {
       const int tile = t_lo + j, key0 = tile * kBN;
       const bool pure = pure_next;
-      if (MODE == kBias && j + 1 < T) pure_next = p.impure[imp0 + tile + 1] == 0;
+      if (MODE == kBias && j + 1 < T)
+        pure_next = EXTKV_IN(imp0 + tile + 1, 1, static_cast<int64_t>(p.B) * p.n_pt * p.n_kt, p.status) && p.impure[imp0 + tile + 1] == 0;
       // keys of the tile no row of the CTA attends (their V rows are zeroed)
       uint64_t dead0, dead1;
       if (C::kTerm) {
-        dead0 = ~cmrow[2 * tile];
+        dead0 = EXTKV_IN(2 * tile, 1, p.n_tiles, p.status) ? ~cmrow[2 * tile] : ~0ull;
         dead1 = 2 * tile + 1 < p.n_tiles ? ~cmrow[2 * tile + 1] : ~0ull;
       } else {
         dead0 = ~bit_range(rlo - key0, rhi - key0);
@@ -956,8 +966,9 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
       // holds only 0 and the sentinel needs the plan's bits of the row alone
       uint64_t al0, al1;
       if (pure) {
-        const uint4 rb = *reinterpret_cast<const uint4*>(
-            p.rowmask + ((static_cast<int64_t>(b) * p.n_pt + pt) * kBM + prow) * p.rm_stride + tile * 16);
+        const int64_t at = ((static_cast<int64_t>(b) * p.n_pt + pt) * kBM + prow) * p.rm_stride + tile * 16;
+        const bool in = EXTKV_IN(at, 16, static_cast<int64_t>(p.B) * p.n_pt * kBM * p.rm_stride, p.status);
+        const uint4 rb = in ? *reinterpret_cast<const uint4*>(p.rowmask + at) : make_uint4(0, 0, 0, 0);
         al0 = rb.x | (static_cast<uint64_t>(rb.y) << 32);
         al1 = rb.z | (static_cast<uint64_t>(rb.w) << 32);
       } else if (kFusedMode) {
@@ -1237,6 +1248,12 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
       float* prow_out = p.part + ((static_cast<int64_t>(b * p.Hq + h) * p.n_split + sp) * p.S_q + pos) *
                                      part_stride(p.Dv);
       const bool live = ok && T > 0;
+      // (only rows that are written are tested)
+      const bool part_in =
+          !row_valid ||
+          EXTKV_IN(((static_cast<int64_t>(b * p.Hq + h) * p.n_split + sp) * p.S_q + pos) * part_stride(p.Dv),
+                   part_stride(p.Dv), static_cast<int64_t>(p.B) * p.Hq * p.n_split * p.S_q * part_stride(p.Dv),
+                   p.status);
 #pragma unroll 1
       for (int c = c32_lo; c < c32_hi; ++c) {
         uint32_t o[32];
@@ -1247,7 +1264,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = 0;
         }
-        if (row_valid) {
+        if (row_valid && part_in) {
 #pragma unroll
           for (int q = 0; q < 8; ++q)
             *reinterpret_cast<float4*>(prow_out + vc * DV + 32 * c + 4 * q) =
@@ -1255,7 +1272,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
                             __uint_as_float(o[4 * q + 3]));
         }
       }
-      if (row_valid && vc == 0 && hh == 0) {
+      if (row_valid && part_in && vc == 0 && hh == 0) {
         prow_out[p.Dv] = live ? m_run : -INFINITY;
         prow_out[p.Dv + 1] = live ? l_run : 0.f;
       }
@@ -1263,6 +1280,9 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
       // packed rows: a warp's 32 rows may belong to several query heads, so
       // each thread writes its own row (rows past the group's are not written)
       __nv_bfloat16* yrow = p.y + (row_base + row) * p.Dv + vc * DV;
+      const bool y_in = !(ok && row_valid) ||
+                        EXTKV_IN((row_base + row) * p.Dv + vc * DV, DV,
+                                 static_cast<int64_t>(p.B) * p.Hq * p.S_q * p.Dv, p.status);
 #pragma unroll 1
       for (int cb = cb_lo; cb < cb_hi; ++cb) {
         uint32_t o[64];
@@ -1274,7 +1294,7 @@ __global__ void __launch_bounds__(Cfg<DK, DV, MODE>::kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 64; ++e) o[e] = 0;
         }
-        if (ok && row_valid) {
+        if (ok && row_valid && y_in) {
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             uint32_t w[4];
@@ -1377,7 +1397,7 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillParams 
       uint2 pk;
       pk.x = ptx::pack_bf16x2(a.x * inv, a.y * inv);
       pk.y = ptx::pack_bf16x2(a.z * inv, a.w * inv);
-      *reinterpret_cast<uint2*>(p.y + r * D + d) = pk;
+      if (EXTKV_IN(r * D + d, 4, rows * D, p.status)) *reinterpret_cast<uint2*>(p.y + r * D + d) = pk;
     }
   }
 }

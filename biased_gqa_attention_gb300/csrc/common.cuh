@@ -51,6 +51,24 @@ __device__ __forceinline__ void report(int32_t* status, int32_t flag) {
   }
 }
 
+// ---- checked builds ----------------------------------------------------------
+// Built with EXTKV_CHECKED, the kernels test every plain global load or store
+// whose index they compute: elements [first, first + count) must lie in a
+// buffer of n elements, else the access is skipped and EXTKV_DEV_BOUNDS is
+// flagged in the status word (a bounds check in place of a sanitizer: no trap,
+// no fault).  Otherwise the test is the constant true and its arguments are
+// not evaluated.
+#ifdef EXTKV_CHECKED
+__device__ __forceinline__ bool in_bounds(int64_t first, int64_t count, int64_t n, int32_t* status) {
+  if (first >= 0 && count >= 0 && first + count <= n) return true;
+  report(status, EXTKV_DEV_BOUNDS);
+  return false;
+}
+#define EXTKV_IN(first, count, n, status) ::extkv::in_bounds((first), (count), (n), (status))
+#else
+#define EXTKV_IN(first, count, n, status) true
+#endif
+
 // ---- the bias specification, evaluated on the device -----------------------
 
 // Kernel-parameter copy of extkv_bias_spec.

@@ -421,10 +421,11 @@ int extkv_read_status(const int32_t* status, void* stream) {
   e = cudaMemcpy(h, status, sizeof h, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "extkv_read_status: copy");
   if (h[0] == 0) return EXTKV_OK;
-  return fail(EXTKV_ERR_DEVICE, "device status 0x%x (%d unit(s) skipped):%s%s%s", h[0], h[1],
+  return fail(EXTKV_ERR_DEVICE, "device status 0x%x (%d unit(s) skipped):%s%s%s%s", h[0], h[1],
               (h[0] & EXTKV_DEV_BAD_WRITE_IDX) ? " write_idx out of range;" : "",
               (h[0] & EXTKV_DEV_BAD_NONPAD) ? " nonpad out of range;" : "",
-              (h[0] & EXTKV_DEV_TIMEOUT) ? " pipeline wait timed out;" : "");
+              (h[0] & EXTKV_DEV_TIMEOUT) ? " pipeline wait timed out;" : "",
+              (h[0] & EXTKV_DEV_BOUNDS) ? " access outside a buffer skipped (checked build);" : "");
 }
 
 const char* extkv_last_error(void) { return g_error; }

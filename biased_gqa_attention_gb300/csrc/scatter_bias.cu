@@ -60,12 +60,15 @@ __global__ void __launch_bounds__(256) scatter_kernel(uint4* __restrict__ k_cach
     const int64_t s = r % S_new;
     const int64_t bh = r / S_new;
     const int64_t b = bh / Hkv;
+    const int64_t n_bh = total / (S_new * row_vecs);  // batches x KV heads
+    if (!EXTKV_IN(b, 1, n_bh / Hkv, status)) continue;
     const int64_t w = write_idx[b];
     if (w < 0 || w > max_seq - S_new) {
       if (v == 0 && s == 0 && bh % Hkv == 0) report(status, EXTKV_DEV_BAD_WRITE_IDX);
       continue;
     }
     const int64_t dst = (bh * max_seq + w + s) * row_vecs + v;
+    if (!EXTKV_IN(dst, 1, n_bh * max_seq * row_vecs, status)) continue;
     const uint4 kx = __ldg(k_new + idx);
     const uint4 vx = __ldg(v_new + idx);
     k_cache[dst] = kx;
@@ -124,6 +127,7 @@ __global__ void __launch_bounds__(256) bias_kernel(uint4* __restrict__ bias, Bia
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {  // r = b*S_q + i
     const int64_t i = r % S_q;
     const int64_t b = r / S_q;
+    if (!EXTKV_IN(b, 1, rows / S_q, status)) continue;
     const int64_t np = nonpad[b];
     uint4* out = bias + r * row_vecs;
     const uint4* ext = extra ? extra + r * row_vecs : nullptr;
@@ -157,7 +161,7 @@ __global__ void __launch_bounds__(256) bias_kernel(uint4* __restrict__ bias, Bia
           v.e[e] = ok ? x.e[e] : low.e[e];
         }
       }
-      out[jv] = v.u;
+      if (EXTKV_IN(r * row_vecs + jv, 1, rows * row_vecs, status)) out[jv] = v.u;
     }
   }
 }

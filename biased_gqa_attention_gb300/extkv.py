@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libextkv.so")
 
 EXTKV_F32, EXTKV_BF16 = 0, 1
 EXTKV_OK, EXTKV_ERR_INVALID_ARG, EXTKV_ERR_UNSUPPORTED, EXTKV_ERR_CUDA, EXTKV_ERR_DEVICE = 0, -1, -2, -3, -4
-EXTKV_DEV_BAD_WRITE_IDX, EXTKV_DEV_BAD_NONPAD, EXTKV_DEV_TIMEOUT = 0x1, 0x2, 0x4
+EXTKV_DEV_BAD_WRITE_IDX, EXTKV_DEV_BAD_NONPAD, EXTKV_DEV_TIMEOUT, EXTKV_DEV_BOUNDS = 0x1, 0x2, 0x4, 0x8
 ALGO_AUTO, ALGO_GENERIC, ALGO_DECODE, ALGO_PREFILL, ALGO_PREFILL_PAIR = 0, 1, 2, 3, 4
 ALGO_DECODE_STREAMK, ALGO_DECODE_CLUSTER = 5, 6
 

@@ -69,6 +69,9 @@ typedef enum {
 #define EXTKV_DEV_BAD_WRITE_IDX 0x1 /* write_idx[b] < 0 or write_idx[b] + S_new > max_seq */
 #define EXTKV_DEV_BAD_NONPAD 0x2    /* nonpad[b] < 0 or nonpad[b] > max_seq */
 #define EXTKV_DEV_TIMEOUT 0x4       /* a bounded pipeline wait gave up; the tile was abandoned */
+#define EXTKV_DEV_BOUNDS 0x8        /* a library built with EXTKV_CHECKED skipped a global access whose
+                                       index fell outside its buffer (device bounds checks in place
+                                       of a sanitizer: no trap, no fault) */
 
 /*
  * The bias specification of mobius issue #366 (deliverable: causal + sliding
