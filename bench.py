@@ -730,7 +730,7 @@ NCU_TRAFFIC = {
     # attn_decode_cluster_kernel<256, 256, 3, 1, 0> (the step's call, with the fused scatter)
     ("decode_b8_hq16_hkv8_d256_w1024", "bias", "attn_decode_cluster_scatter"): 65.22e6,
     # attn_prefill_kernel<256, 256, 1, 0>
-    ("prefill_s2048_hq16_hkv8_d256_w1024_spans", "bias", "attn_prefill_tcgen05"): 43.15e6,
+    ("prefill_s2048_hq16_hkv8_d256_w1024_spans", "bias", "attn_prefill_tcgen05"): 43.00e6,
 }
 
 
